@@ -1,0 +1,211 @@
+/*
+ * awq.h -- C ABI of libawq: the activation-aware weight quantization (AWQ)
+ * per-layer scale search on one NVIDIA B300 (sm_103a).
+ *
+ * What the library computes (passages by page title and section):
+ *  - "AWQ explained" (hungho77.github.io), "Scaling instead of mixed
+ *    precision": for a linear layer Y = W X, W' = W diag(s) and
+ *    X' = diag(s)^-1 X leave the product unchanged before quantization;
+ *    s = sX^alpha with sX the average activation magnitude per input channel;
+ *    alpha is grid-searched in [0, 1] to minimise the layer-output error
+ *    after quantization, with no backpropagation.
+ *  - "AWQ Explained: Protecting the Weights That Matter Most" (multigrid.ai),
+ *    "Scaling instead of mixed precision": the grid step is the group's range
+ *    divided by the number of levels; "How the scale is chosen":
+ *    alpha* = argmin over the grid of || W x - Q(W diag(s)) diag(s)^-1 x ||,
+ *    and the knobs bits (4), group_size (128), zero_point (true).
+ *  - "activation-aware weight quantization (AWQ)" (realpython.com): codes
+ *    packed at 3 or 4 bits in groups, commonly 128.
+ *  - "AWQ" (ai360xpert.com), "How It Works", step 4: round-to-nearest.
+ *
+ * Conventions for every call:
+ *  - Pointers documented "device" must be device (or managed) memory of the
+ *    current CUDA device; the library checks this and returns
+ *    AWQ_ERR_INVALID otherwise, before launching anything.
+ *  - fp16 matrices are row-major IEEE binary16, 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *    enqueued on it; calls return before the GPU finishes.  Outputs are valid
+ *    once the caller has synchronised the stream.
+ *  - No exception crosses the ABI.  On failure a call returns a non-zero
+ *    awq_status and awq_last_error() (per thread) describes it; argument
+ *    errors are detected before any launch.
+ *  - Device-side waits inside the tensor-core kernels are bounded (2 s); an
+ *    expired wait is reported as AWQ_ERR_TIMEOUT through a status word
+ *    (never a trap), see awq_result_check and awq_reference_output.
+ *
+ * Quantizer (fp32, every operation correctly rounded, none fused), per group
+ * of `group_size` consecutive input channels of one output row:
+ *   w' = w * s_k;  rng = max w' - min w';  step = max(rng, 1e-5) / (2^b - 1);
+ *   scale = fp16_rne(step);  rcp = 1 / float(scale);
+ *   zero = clamp(rne(-min w' * rcp), 0, 2^b - 1);
+ *   code = clamp(rne(w' * rcp) + zero, 0, 2^b - 1);   rne = half to even.
+ * Scale vector: u_k = max(sX_k, 1e-4)^alpha (fp64),
+ *   s_k = fp32(u_k / sqrt(max_k u * min_k u)),  alpha_i = i / n_grid.
+ * Loss: ||W X^T - deq(Q(W diag(s))) diag(s)^-1 X^T||_F^2 / (N T), summed over
+ *   the weights of one call; alpha* = first index of the minimum.
+ * Packed codes: INT4 row n, word j = sum_m code[n][8j+m] << 4m;
+ *   INT3 row n = little-endian bit stream, code k in bits [3k, 3k+3),
+ *   32 codes per 3 words.
+ */
+#ifndef AWQ_H
+#define AWQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AWQ_ABI_VERSION 1
+#define AWQ_MAX_GRID 64
+#define AWQ_MAX_WEIGHTS 16
+
+typedef enum awq_status {
+  AWQ_OK = 0,
+  AWQ_ERR_INVALID = 1,     /* bad argument (null, misaligned, host pointer, bad size) */
+  AWQ_ERR_UNSUPPORTED = 2, /* well-formed configuration this build does not implement */
+  AWQ_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  AWQ_ERR_OOM = 4,         /* device memory exhausted */
+  AWQ_ERR_TIMEOUT = 5      /* a bounded device-side wait expired */
+} awq_status;
+
+/* Quantizer configuration ("AWQ Explained", multigrid.ai, "How the scale is
+ * chosen": bits, group_size, zero_point).  Supported: bits 3 or 4,
+ * group_size 64 or 128, zero_point 1, n_grid 1..AWQ_MAX_GRID (20 is the
+ * default grid alpha = 0, 0.05, ..., 0.95). */
+typedef struct awq_qconfig {
+  int bits;
+  int group_size;
+  int zero_point;
+  int n_grid;
+} awq_qconfig;
+
+/* One weight matrix of a search call: device fp16 [N][K] row-major
+ * (the nn.Linear.weight layout), N >= 1. */
+typedef struct awq_weight {
+  const void* W;
+  int64_t N;
+} awq_weight;
+
+/* Opaque search result, owned by the library until awq_free. */
+typedef struct awq_result awq_result;
+
+/* ABI version of the loaded library (AWQ_ABI_VERSION). */
+int awq_abi_version(void);
+
+/* Message of the last failed call on this thread ("" if none).  Owned by
+ * the library, valid until the next call on the same thread. */
+const char* awq_last_error(void);
+
+/* Constant name of a status code. */
+const char* awq_status_string(int status);
+
+/* uint32 words of N packed rows of K codes at `bits` (3 or 4); -1 if the
+ * shape is invalid (K % 8 for INT4, K % 32 for INT3).  Host-only. */
+int64_t awq_packed_words(int64_t N, int64_t K, int bits);
+
+/* Channel statistic sX_k = (1/T) sum_t |X[t][k]| ("AWQ explained",
+ * "Scaling instead of mixed precision": average activation magnitude per
+ * input channel).
+ *   X  : device fp16 [T][K], T >= 1, K >= 8 and K % 8 == 0.
+ *   sX : device fp64 [K], written.  The channel sums are exact (64-bit
+ *        integer accumulation of |x| in units of 2^-24); the mean is one
+ *        correctly rounded fp64 division.
+ * Allocates K*8 bytes of stream-ordered scratch from the library's pool. */
+awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stream);
+
+/* Scale vectors for every grid point ("AWQ explained": s = sX^alpha).
+ *   sX : device fp64 [K], K >= 1.
+ *   s  : device fp32 [n_grid][K], written; row i uses alpha = i / n_grid.
+ * Allocates n_grid*K*8 bytes of stream-ordered scratch. */
+awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s, void* stream);
+
+/* Scale, group-quantize and pack one weight ("AWQ Explained", multigrid.ai,
+ * "Scaling instead of mixed precision"; realpython glossary: 3/4-bit codes in
+ * groups).  One pass over W; allocates nothing.
+ *   W      : device fp16 [N][K]; N >= 0 (N = 0 is a no-op), K % group == 0.
+ *   s      : device fp32 [K] (the per-input-channel scale).
+ *   codes  : device uint32 [awq_packed_words(N, K, bits)], written.
+ *   scales : device fp16 [N][K/group], written.
+ *   zeros  : device uint8 [N][K/group], written. */
+awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s,
+                             const awq_qconfig* cfg, uint32_t* codes, void* scales,
+                             uint8_t* zeros, void* stream);
+
+/* Inverse of the packing: q[n][k] = code k of row n.
+ *   codes : device uint32 [awq_packed_words(N, K, bits)];  q : device uint8 [N][K]. */
+awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
+                            void* stream);
+
+/* Layer output before quantization, Y = W X^T ("AWQ Explained", multigrid.ai,
+ * "How the scale is chosen": the W x term), on tcgen05 tensor cores.
+ *   W : device fp16 [N][K];  X : device fp16 [T][K];  K % 64 == 0.
+ *   Y : device fp32 [N][T], written.
+ *   status_dev : optional device int (caller zeroes it); receives a non-zero
+ *                code if a bounded device wait expired.  May be NULL. */
+awq_status awq_reference_output(const void* W, int64_t N, const void* X, int64_t T, int64_t K,
+                                float* Y, int* status_dev, void* stream);
+
+/* The whole per-layer scale search ("AWQ explained", "Scaling instead of
+ * mixed precision"; "AWQ Explained", multigrid.ai, "How the scale is chosen").
+ *   X   : device fp16 [T][K] calibration activations, T >= 1, K % group == 0.
+ *   sX  : optional device fp64 [K]; NULL computes it with awq_stats.
+ *   Ws  : host array of n_w (1..AWQ_MAX_WEIGHTS) weights sharing X (one s,
+ *         one alpha; the loss is the sum of their losses).
+ *   cfg : quantizer configuration.
+ *   out : receives a library-owned result (free with awq_free).
+ * Steps, all stream-ordered on the device: sX; s for every grid point; for
+ * every weight and grid point the fp16 quantization residual
+ * W - deq(Q(W diag(s))) diag(s)^-1 (the same quantizer as awq_quantize_pack);
+ * one tcgen05 GEMM of all residuals with X whose epilogue sums the squared
+ * layer-output errors per row; losses and argmin; the final quantization at
+ * the chosen alpha (read on the device, no host round trip).  Scratch is
+ * n_grid * sum_i(round_up(N_i, 128)) * K * 2 bytes of residuals plus small
+ * buffers.  Device memory for the result and the scratch comes from a
+ * library-owned stream-ordered pool;
+ * the scratch is released in stream order before the call returns. */
+awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* sX,
+                            const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
+                            awq_result** out);
+
+/* After the search's stream is synchronised: AWQ_OK, or AWQ_ERR_TIMEOUT if a
+ * bounded device wait expired during the search. */
+awq_status awq_result_check(const awq_result* r);
+
+/* Result accessors.  Host values (alpha, best index, losses) are valid once
+ * the stream is synchronised.  Device pointers stay valid until awq_free. */
+int awq_result_n_grid(const awq_result* r);
+int awq_result_n_weights(const awq_result* r);
+int awq_result_best_index(const awq_result* r);        /* host */
+double awq_result_alpha(const awq_result* r);          /* host: best / n_grid */
+const double* awq_result_losses(const awq_result* r);  /* host fp64 [n_grid] */
+const float* awq_result_s(const awq_result* r);        /* device fp32 [K], s at alpha* */
+const float* awq_result_s_grid(const awq_result* r);   /* device fp32 [n_grid][K] */
+const double* awq_result_row_losses(const awq_result* r); /* device fp64 [n_grid][sum N_i]:
+                                                              sum_t error^2 per output row,
+                                                              weights concatenated in order */
+const uint32_t* awq_result_codes(const awq_result* r, int i);  /* device packed codes of W_i */
+const void* awq_result_scales(const awq_result* r, int i);     /* device fp16 [N_i][K/group] */
+const uint8_t* awq_result_zeros(const awq_result* r, int i);   /* device uint8 [N_i][K/group] */
+
+/* Release a result.  Its device memory returns to the library's pool in the
+ * order of the stream the search ran on, so call this before destroying that
+ * stream.  NULL is ignored. */
+void awq_free(awq_result* r);
+
+/* Return the library pool's cached, unused device memory on the current
+ * device to the driver (synchronises the device). */
+awq_status awq_release_cached_memory(void);
+
+/* Self-test of the bounded device wait: launches one CTA that waits on a
+ * barrier nothing arrives at, with a limit of limit_ns nanoseconds
+ * (1e3..5e9), synchronises, and returns AWQ_ERR_TIMEOUT when the wait expired
+ * and was reported as it should (AWQ_OK would mean the wait did not expire).
+ * Exists for testing the failure path without faulting the GPU. */
+awq_status awq_selftest_bounded_wait(int64_t limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_H */

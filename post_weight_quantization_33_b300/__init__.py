@@ -1,0 +1,357 @@
+"""AWQ activation-aware scale search on one B300 (sm_103a).
+
+A thin ctypes binding over ``libawq.so`` (declared in ``include/awq.h``).  It
+only marshals arguments: every step of the search runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  There is no
+CPU fallback: if the library is missing or the device cannot run it, calls
+raise.
+
+Functions mirror the C entry points:
+
+``stats(X)``                      sX = mean_t |X[t, k]|                (awq_stats)
+``scales(sX, n_grid)``            s for every grid point               (awq_scales)
+``quantize_pack(W, s, bits, g)``  packed codes, fp16 scales, u8 zeros  (awq_quantize_pack)
+``unpack_codes(codes, N, K, b)``  codes as uint8 [N, K]                (awq_unpack_codes)
+``reference_output(W, X)``        Y = W X^T in fp32                    (awq_reference_output)
+``search(X, Ws, ...)``            the full per-layer search            (awq_search_layer)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+__all__ = [
+    "AwqError", "lib", "library_path", "stats", "scales", "quantize_pack", "unpack_codes",
+    "reference_output", "search", "search_host", "SearchResult", "packed_words",
+    "release_cached_memory", "selftest_bounded_wait", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libawq.so")
+_lib = None
+
+AWQ_OK, AWQ_ERR_INVALID, AWQ_ERR_UNSUPPORTED, AWQ_ERR_CUDA, AWQ_ERR_OOM, AWQ_ERR_TIMEOUT = range(6)
+
+# Every symbol include/awq.h declares.
+EXPORTED_SYMBOLS = (
+    "awq_abi_version", "awq_last_error", "awq_status_string", "awq_packed_words",
+    "awq_stats", "awq_scales", "awq_quantize_pack", "awq_unpack_codes",
+    "awq_reference_output", "awq_search_layer", "awq_result_check", "awq_result_n_grid",
+    "awq_result_n_weights", "awq_result_best_index", "awq_result_alpha", "awq_result_losses",
+    "awq_result_s", "awq_result_s_grid", "awq_result_row_losses", "awq_result_codes",
+    "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
+    "awq_selftest_bounded_wait",
+)
+
+
+class AwqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(message)
+
+
+class QConfig(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int), ("group_size", ctypes.c_int),
+                ("zero_point", ctypes.c_int), ("n_grid", ctypes.c_int)]
+
+
+class Weight(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("N", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libawq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -m post_weight_quantization_33_b300.build`")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int
+    sig = {
+        "awq_abi_version": (i32, []),
+        "awq_last_error": (ctypes.c_char_p, []),
+        "awq_status_string": (ctypes.c_char_p, [i32]),
+        "awq_packed_words": (i64, [i64, i64, i32]),
+        "awq_stats": (st, [vp, i64, i64, vp, vp]),
+        "awq_scales": (st, [vp, i64, i32, vp, vp]),
+        "awq_quantize_pack": (st, [vp, i64, i64, vp, ctypes.POINTER(QConfig), vp, vp, vp, vp]),
+        "awq_unpack_codes": (st, [vp, i64, i64, i32, vp, vp]),
+        "awq_reference_output": (st, [vp, i64, vp, i64, i64, vp, vp, vp]),
+        "awq_search_layer": (st, [vp, i64, i64, vp, ctypes.POINTER(Weight), i32,
+                                  ctypes.POINTER(QConfig), vp, ctypes.POINTER(vp)]),
+        "awq_result_check": (st, [vp]),
+        "awq_result_n_grid": (i32, [vp]),
+        "awq_result_n_weights": (i32, [vp]),
+        "awq_result_best_index": (i32, [vp]),
+        "awq_result_alpha": (ctypes.c_double, [vp]),
+        "awq_result_losses": (ctypes.POINTER(ctypes.c_double), [vp]),
+        "awq_result_s": (vp, [vp]),
+        "awq_result_s_grid": (vp, [vp]),
+        "awq_result_row_losses": (vp, [vp]),
+        "awq_result_codes": (vp, [vp, i32]),
+        "awq_result_scales": (vp, [vp, i32]),
+        "awq_result_zeros": (vp, [vp, i32]),
+        "awq_free": (None, [vp]),
+        "awq_release_cached_memory": (st, []),
+        "awq_selftest_bounded_wait": (st, [i64]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != AWQ_OK:
+        L = lib()
+        name = L.awq_status_string(status).decode()
+        msg = L.awq_last_error().decode()
+        raise AwqError(status, f"{name}: {msg}")
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _require(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cfg(bits: int, group: int, n_grid: int = 20) -> QConfig:
+    return QConfig(bits, group, 1, n_grid)
+
+
+def packed_words(N: int, K: int, bits: int) -> int:
+    """uint32 words of N packed rows (-1 for an invalid shape)."""
+    return int(lib().awq_packed_words(N, K, bits))
+
+
+def stats(X: torch.Tensor) -> torch.Tensor:
+    """sX [K] fp64 = mean over tokens of |X| (X: fp16 [T, K] on the GPU)."""
+    _require(X, "X", torch.float16, 2)
+    T, K = X.shape
+    sX = torch.empty(K, dtype=torch.float64, device=X.device)
+    _check(lib().awq_stats(X.data_ptr(), T, K, sX.data_ptr(), _stream()))
+    return sX
+
+
+def scales(sX: torch.Tensor, n_grid: int = 20) -> torch.Tensor:
+    """s [n_grid, K] fp32, row i at alpha = i / n_grid."""
+    _require(sX, "sX", torch.float64, 1)
+    K = sX.shape[0]
+    s = torch.empty((n_grid, K), dtype=torch.float32, device=sX.device)
+    _check(lib().awq_scales(sX.data_ptr(), K, n_grid, s.data_ptr(), _stream()))
+    return s
+
+
+def quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: int = 128):
+    """(codes int32 [words] holding the uint32 bit patterns, scales fp16 [N, K/g], zeros u8)."""
+    _require(W, "W", torch.float16, 2)
+    _require(s, "s", torch.float32, 1)
+    N, K = W.shape
+    words = packed_words(N, K, bits)
+    if words < 0:
+        raise ValueError(f"cannot pack K={K} at {bits} bits")
+    codes = torch.empty(max(words, 1), dtype=torch.int32, device=W.device)[:words]
+    sc = torch.empty((N, K // group), dtype=torch.float16, device=W.device)
+    z = torch.empty((N, K // group), dtype=torch.uint8, device=W.device)
+    cfg = _cfg(bits, group)
+    _check(lib().awq_quantize_pack(W.data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg),
+                                   codes.data_ptr(), sc.data_ptr(), z.data_ptr(), _stream()))
+    return codes, sc, z
+
+
+def unpack_codes(codes: torch.Tensor, N: int, K: int, bits: int) -> torch.Tensor:
+    """uint8 [N, K] codes from the packed words."""
+    _require(codes, "codes", torch.int32, 1)
+    q = torch.empty((N, K), dtype=torch.uint8, device=codes.device)
+    _check(lib().awq_unpack_codes(codes.data_ptr(), N, K, bits, q.data_ptr(), _stream()))
+    return q
+
+
+def reference_output(W: torch.Tensor, X: torch.Tensor, check: bool = True) -> torch.Tensor:
+    """Y = W X^T in fp32 [N, T] on the tensor cores."""
+    _require(W, "W", torch.float16, 2)
+    _require(X, "X", torch.float16, 2)
+    N, K = W.shape
+    T = X.shape[0]
+    Y = torch.empty((N, T), dtype=torch.float32, device=W.device)
+    status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    _check(lib().awq_reference_output(W.data_ptr(), N, X.data_ptr(), T, K, Y.data_ptr(),
+                                      status.data_ptr(), _stream()))
+    if check and int(status.item()) != 0:
+        raise AwqError(AWQ_ERR_TIMEOUT, f"bounded device wait expired (code {int(status.item())})")
+    return Y
+
+
+class _DevArray:
+    """__cuda_array_interface__ over library-owned device memory (no copy)."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {
+            "shape": tuple(int(s) for s in shape), "typestr": typestr,
+            "data": (int(ptr), False), "version": 2, "strides": None}
+
+
+def _alias(ptr: int, shape, typestr: str, device) -> torch.Tensor:
+    if int(np.prod(shape)) == 0:
+        dt = {"<f4": torch.float32, "<f8": torch.float64, "<f2": torch.float16,
+              "<i4": torch.int32, "|u1": torch.uint8}[typestr]
+        return torch.empty(shape, dtype=dt, device=device)
+    with torch.cuda.device(device):
+        return torch.as_tensor(_DevArray(ptr, shape, typestr), device=device)
+
+
+class SearchResult:
+    """Owns one awq_result.  Host values need the stream synchronised (the
+    accessors below do it); tensors returned are copies owned by torch."""
+
+    def __init__(self, handle: int, Ns: Sequence[int], K: int, T: int, bits: int, group: int,
+                 n_grid: int, device):
+        self._h = ctypes.c_void_p(handle)
+        self.Ns = list(Ns)
+        self.K, self.T, self.bits, self.group, self.n_grid = K, T, bits, group, n_grid
+        self.device = device
+
+    def _handle(self):
+        if not self._h:
+            raise RuntimeError("result already freed")
+        return self._h
+
+    def synchronize(self) -> "SearchResult":
+        torch.cuda.current_stream(self.device).synchronize()
+        return self
+
+    def check(self) -> None:
+        self.synchronize()
+        _check(lib().awq_result_check(self._handle()))
+
+    @property
+    def best(self) -> int:
+        self.synchronize()
+        return int(lib().awq_result_best_index(self._handle()))
+
+    @property
+    def alpha(self) -> float:
+        self.synchronize()
+        return float(lib().awq_result_alpha(self._handle()))
+
+    @property
+    def losses(self) -> np.ndarray:
+        self.synchronize()
+        p = lib().awq_result_losses(self._handle())
+        return np.array([p[i] for i in range(self.n_grid)], dtype=np.float64)
+
+    def s(self) -> torch.Tensor:
+        return _alias(lib().awq_result_s(self._handle()), (self.K,), "<f4", self.device).clone()
+
+    def s_grid(self) -> torch.Tensor:
+        return _alias(lib().awq_result_s_grid(self._handle()), (self.n_grid, self.K), "<f4",
+                      self.device).clone()
+
+    def row_losses(self) -> torch.Tensor:
+        return _alias(lib().awq_result_row_losses(self._handle()), (self.n_grid, sum(self.Ns)),
+                      "<f8", self.device).clone()
+
+    def codes(self, i: int = 0) -> torch.Tensor:
+        words = packed_words(self.Ns[i], self.K, self.bits)
+        return _alias(lib().awq_result_codes(self._handle(), i), (words,), "<i4",
+                      self.device).clone()
+
+    def scales(self, i: int = 0) -> torch.Tensor:
+        return _alias(lib().awq_result_scales(self._handle(), i),
+                      (self.Ns[i], self.K // self.group), "<f2", self.device).clone()
+
+    def zeros(self, i: int = 0) -> torch.Tensor:
+        return _alias(lib().awq_result_zeros(self._handle(), i),
+                      (self.Ns[i], self.K // self.group), "|u1", self.device).clone()
+
+    def free(self) -> None:
+        if self._h:
+            lib().awq_free(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def search(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: int = 128,
+           n_grid: int = 20, sX: Optional[torch.Tensor] = None) -> SearchResult:
+    """Run awq_search_layer for the weights ``Ws`` sharing activations ``X``."""
+    _require(X, "X", torch.float16, 2)
+    T, K = X.shape
+    arr = (Weight * len(Ws))()
+    for i, W in enumerate(Ws):
+        _require(W, f"Ws[{i}]", torch.float16, 2)
+        if W.shape[1] != K:
+            raise ValueError(f"Ws[{i}] has K={W.shape[1]}, X has K={K}")
+        arr[i].W = W.data_ptr()
+        arr[i].N = W.shape[0]
+    sxp = None
+    if sX is not None:
+        _require(sX, "sX", torch.float64, 1)
+        sxp = sX.data_ptr()
+    cfg = _cfg(bits, group, n_grid)
+    out = ctypes.c_void_p()
+    _check(lib().awq_search_layer(X.data_ptr(), T, K, sxp, arr, len(Ws), ctypes.byref(cfg),
+                                  _stream(), ctypes.byref(out)))
+    return SearchResult(out.value, [W.shape[0] for W in Ws], K, T, bits, group, n_grid, X.device)
+
+
+def search_host(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: int = 128,
+                n_grid: int = 20, device="cuda") -> dict:
+    """Search with host (CPU, ideally pinned) inputs; returns host outputs.
+
+    Copies X and the weights to the device, runs ``search`` and copies the
+    results back (codes, scales, zeros per weight, s, losses, alpha)."""
+    Xd = X.to(device, non_blocking=True)
+    Wd = [W.to(device, non_blocking=True) for W in Ws]
+    r = search(Xd, Wd, bits, group, n_grid)
+    try:
+        out = {
+            "codes": [r.codes(i).to("cpu", non_blocking=True) for i in range(len(Ws))],
+            "scales": [r.scales(i).to("cpu", non_blocking=True) for i in range(len(Ws))],
+            "zeros": [r.zeros(i).to("cpu", non_blocking=True) for i in range(len(Ws))],
+            "s": r.s().to("cpu", non_blocking=True),
+        }
+        r.check()
+        out["losses"] = r.losses
+        out["best"] = r.best
+        out["alpha"] = r.alpha
+    finally:
+        r.free()
+    return out
+
+
+def release_cached_memory() -> None:
+    _check(lib().awq_release_cached_memory())
+
+
+def selftest_bounded_wait(limit_ns: int = 20_000_000) -> int:
+    """Run the bounded-wait self-test; returns the status (AWQ_ERR_TIMEOUT expected)."""
+    return int(lib().awq_selftest_bounded_wait(limit_ns))

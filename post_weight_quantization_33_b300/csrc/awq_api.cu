@@ -1,0 +1,553 @@
+// C ABI of libawq (declarations and contracts in include/awq.h).
+//
+// Host-side only: argument validation (before any launch), a per-device
+// stream-ordered memory pool, and the ordering of the kernels that make up
+// the scale search.  All arithmetic runs in the kernels of awq_stats.cu,
+// awq_quant.cu, awq_gemm.cu and awq_reduce.cu.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "awq.h"
+#include "awq_internal.h"
+
+using namespace awq;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+awq_status fail(awq_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+awq_status ok() {
+  g_last_error[0] = '\0';
+  return AWQ_OK;
+}
+
+awq_status cuda_fail(cudaError_t e, const char* what) {
+  const awq_status st = (e == cudaErrorMemoryAllocation) ? AWQ_ERR_OOM : AWQ_ERR_CUDA;
+  return fail(st, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define AWQ_CUDA(expr, what)                 \
+  do {                                       \
+    cudaError_t e_ = (expr);                 \
+    if (e_ != cudaSuccess) {                 \
+      cleanup();                             \
+      return cuda_fail(e_, what);            \
+    }                                        \
+  } while (0)
+
+// True if p is device or managed memory usable on the current device.
+bool device_ptr(const void* p) {
+  if (p == nullptr) return false;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeManaged) return true;
+  if (a.type != cudaMemoryTypeDevice) return false;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  return a.device == dev;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+awq_status check_dev(const void* p, const char* name, uintptr_t align) {
+  if (p == nullptr) return fail(AWQ_ERR_INVALID, "%s is NULL", name);
+  if (!aligned(p, align))
+    return fail(AWQ_ERR_INVALID, "%s is not %d-byte aligned", name, static_cast<int>(align));
+  if (!device_ptr(p))
+    return fail(AWQ_ERR_INVALID, "%s is not device memory of the current device", name);
+  return AWQ_OK;
+}
+
+awq_status check_cfg(const awq_qconfig* cfg) {
+  if (cfg == nullptr) return fail(AWQ_ERR_INVALID, "cfg is NULL");
+  if (cfg->bits != 3 && cfg->bits != 4)
+    return fail(AWQ_ERR_UNSUPPORTED, "bits=%d (supported: 3, 4)", cfg->bits);
+  if (cfg->group_size != 64 && cfg->group_size != 128)
+    return fail(AWQ_ERR_UNSUPPORTED, "group_size=%d (supported: 64, 128)", cfg->group_size);
+  if (cfg->zero_point != 1)
+    return fail(AWQ_ERR_UNSUPPORTED, "zero_point=%d (supported: 1, asymmetric)", cfg->zero_point);
+  if (cfg->n_grid < 1 || cfg->n_grid > kMaxGrid)
+    return fail(AWQ_ERR_INVALID, "n_grid=%d (1..%d)", cfg->n_grid, kMaxGrid);
+  return AWQ_OK;
+}
+
+// ---------------------------------------------------------------- memory pool
+cudaMemPool_t pool_for_current_device(cudaError_t* err) {
+  static std::mutex mu;
+  static std::map<int, cudaMemPool_t> pools;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = pools.find(dev);
+  if (it != pools.end()) return it->second;
+  cudaMemPoolProps props;
+  memset(&props, 0, sizeof(props));
+  props.allocType = cudaMemAllocationTypePinned;
+  props.handleTypes = cudaMemHandleTypeNone;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaMemPool_t pool = nullptr;
+  *err = cudaMemPoolCreate(&pool, &props);
+  if (*err != cudaSuccess) return nullptr;
+  uint64_t keep = ~0ull;   // keep freed blocks cached for the next call
+  cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  pools[dev] = pool;
+  return pool;
+}
+
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t st) {
+  cudaError_t e;
+  cudaMemPool_t pool = pool_for_current_device(&e);
+  if (pool == nullptr) return e;
+  return cudaMallocFromPoolAsync(p, bytes < 256 ? 256 : bytes, pool, st);
+}
+
+// Carves 256-byte-aligned pieces out of one allocation.
+struct Carver {
+  size_t off = 0;
+  template <typename T>
+  size_t take(int64_t count) {
+    const size_t at = off;
+    off += (static_cast<size_t>(count) * sizeof(T) + 255) & ~static_cast<size_t>(255);
+    return at;
+  }
+};
+
+// Pinned host mirror of the small outputs, recycled across calls.
+struct HostMirror {
+  int best;
+  int status;
+  double alpha;
+  double losses[kMaxGrid];
+};
+
+std::mutex g_mirror_mu;
+std::vector<HostMirror*> g_mirrors;
+
+HostMirror* take_mirror() {
+  {
+    std::lock_guard<std::mutex> lock(g_mirror_mu);
+    if (!g_mirrors.empty()) {
+      HostMirror* m = g_mirrors.back();
+      g_mirrors.pop_back();
+      return m;
+    }
+  }
+  HostMirror* m = nullptr;
+  if (cudaMallocHost(reinterpret_cast<void**>(&m), sizeof(HostMirror)) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return m;
+}
+
+void give_mirror(HostMirror* m) {
+  if (m == nullptr) return;
+  std::lock_guard<std::mutex> lock(g_mirror_mu);
+  g_mirrors.push_back(m);
+}
+
+}  // namespace
+
+struct awq_result {
+  cudaStream_t stream = nullptr;
+  int n_grid = 0, n_w = 0, bits = 0, group = 0;
+  int64_t K = 0, T = 0, n_total = 0;
+  int64_t rows[kMaxWeights] = {};
+  void* block = nullptr;
+  HostMirror* host = nullptr;
+  float* s = nullptr;
+  float* s_grid = nullptr;
+  int* best = nullptr;
+  double* alpha = nullptr;
+  double* losses = nullptr;
+  double* row_losses = nullptr;
+  int* status = nullptr;
+  uint32_t* codes[kMaxWeights] = {};
+  __half* scales[kMaxWeights] = {};
+  uint8_t* zeros[kMaxWeights] = {};
+};
+
+extern "C" {
+
+int awq_abi_version(void) { return AWQ_ABI_VERSION; }
+
+const char* awq_last_error(void) { return g_last_error; }
+
+const char* awq_status_string(int status) {
+  switch (status) {
+    case AWQ_OK: return "AWQ_OK";
+    case AWQ_ERR_INVALID: return "AWQ_ERR_INVALID";
+    case AWQ_ERR_UNSUPPORTED: return "AWQ_ERR_UNSUPPORTED";
+    case AWQ_ERR_CUDA: return "AWQ_ERR_CUDA";
+    case AWQ_ERR_OOM: return "AWQ_ERR_OOM";
+    case AWQ_ERR_TIMEOUT: return "AWQ_ERR_TIMEOUT";
+    default: return "AWQ_ERR_UNKNOWN";
+  }
+}
+
+int64_t awq_packed_words(int64_t N, int64_t K, int bits) {
+  if (N < 0 || K <= 0) return -1;
+  if (bits == 4) return (K % 8) ? -1 : N * (K / 8);
+  if (bits == 3) return (K % 32) ? -1 : N * (3 * K / 32);
+  return -1;
+}
+
+awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stream) {
+  if (T < 1) return fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
+  if (K < 8 || K % 8) return fail(AWQ_ERR_INVALID, "K=%lld (must be a positive multiple of 8)",
+                                  static_cast<long long>(K));
+  if (T > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    return fail(AWQ_ERR_INVALID, "T or K too large");
+  awq_status st;
+  if ((st = check_dev(X, "X", 16)) != AWQ_OK) return st;
+  if ((st = check_dev(sX, "sX", 8)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  auto cleanup = [&] {
+    if (ws) cudaFreeAsync(ws, s);
+  };
+  AWQ_CUDA(pool_alloc(&ws, sizeof(unsigned long long) * K, s), "scratch allocation");
+  auto* acc = static_cast<unsigned long long*>(ws);
+  AWQ_CUDA(launch_stats_accumulate(static_cast<const __half*>(X), T, K, acc, s), "stats kernel");
+  AWQ_CUDA(launch_stats_finalize(acc, T, K, sX, s), "stats finalize kernel");
+  AWQ_CUDA(cudaFreeAsync(ws, s), "scratch release");
+  return ok();
+}
+
+awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s_out, void* stream) {
+  if (K < 1 || K > (int64_t(1) << 31))
+    return fail(AWQ_ERR_INVALID, "K=%lld", static_cast<long long>(K));
+  if (n_grid < 1 || n_grid > kMaxGrid)
+    return fail(AWQ_ERR_INVALID, "n_grid=%d (1..%d)", n_grid, kMaxGrid);
+  awq_status st;
+  if ((st = check_dev(sX, "sX", 8)) != AWQ_OK) return st;
+  if ((st = check_dev(s_out, "s", 4)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  auto cleanup = [&] {
+    if (ws) cudaFreeAsync(ws, s);
+  };
+  Carver c;
+  const size_t o_u = c.take<double>(int64_t(n_grid) * K);
+  const size_t o_mm = c.take<unsigned long long>(2 * n_grid);
+  AWQ_CUDA(pool_alloc(&ws, c.off, s), "scratch allocation");
+  char* b = static_cast<char*>(ws);
+  AWQ_CUDA(launch_scales(sX, K, n_grid, reinterpret_cast<double*>(b + o_u),
+                         reinterpret_cast<unsigned long long*>(b + o_mm), s_out, nullptr, s),
+           "scale kernels");
+  AWQ_CUDA(cudaFreeAsync(ws, s), "scratch release");
+  return ok();
+}
+
+awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s_vec,
+                             const awq_qconfig* cfg, uint32_t* codes, void* scales,
+                             uint8_t* zeros, void* stream) {
+  awq_status st;
+  if ((st = check_cfg(cfg)) != AWQ_OK) return st;
+  if (N < 0) return fail(AWQ_ERR_INVALID, "N=%lld", static_cast<long long>(N));
+  if (K < 1 || K % cfg->group_size || K > (int64_t(1) << 31))
+    return fail(AWQ_ERR_INVALID, "K=%lld (must be a positive multiple of group_size=%d)",
+                static_cast<long long>(K), cfg->group_size);
+  if (N == 0) return ok();
+  if ((st = check_dev(W, "W", 16)) != AWQ_OK) return st;
+  if ((st = check_dev(s_vec, "s", 16)) != AWQ_OK) return st;
+  if ((st = check_dev(codes, "codes", 4)) != AWQ_OK) return st;
+  if ((st = check_dev(scales, "scales", 2)) != AWQ_OK) return st;
+  if ((st = check_dev(zeros, "zeros", 1)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto cleanup = [] {};
+  AWQ_CUDA(launch_quant_final(static_cast<const __half*>(W), N, K, cfg->bits, cfg->group_size,
+                              s_vec, nullptr, codes, static_cast<__half*>(scales), zeros, s),
+           "quantize kernel");
+  return ok();
+}
+
+awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
+                            void* stream) {
+  if (awq_packed_words(N, K, bits) < 0)
+    return fail(AWQ_ERR_INVALID, "invalid shape N=%lld K=%lld bits=%d",
+                static_cast<long long>(N), static_cast<long long>(K), bits);
+  if (N == 0) return ok();
+  awq_status st;
+  if ((st = check_dev(codes, "codes", 4)) != AWQ_OK) return st;
+  if ((st = check_dev(q, "q", 1)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto cleanup = [] {};
+  AWQ_CUDA(launch_unpack(codes, N, K, bits, q, s), "unpack kernel");
+  return ok();
+}
+
+awq_status awq_reference_output(const void* W, int64_t N, const void* X, int64_t T, int64_t K,
+                                float* Y, int* status_dev, void* stream) {
+  if (N < 1 || T < 1 || K < 64 || K % 64)
+    return fail(AWQ_ERR_INVALID, "N=%lld T=%lld K=%lld (N, T >= 1; K a positive multiple of 64)",
+                static_cast<long long>(N), static_cast<long long>(T), static_cast<long long>(K));
+  if (N > (int64_t(1) << 30) || T > (int64_t(1) << 30) || K > (int64_t(1) << 30) ||
+      ceil_div(N, kTileM) * ceil_div(T, kTileN) > (int64_t(1) << 30))
+    return fail(AWQ_ERR_INVALID, "shape too large");
+  awq_status st;
+  if ((st = check_dev(W, "W", 16)) != AWQ_OK) return st;
+  if ((st = check_dev(X, "X", 16)) != AWQ_OK) return st;
+  if ((st = check_dev(Y, "Y", 4)) != AWQ_OK) return st;
+  if (status_dev != nullptr && (st = check_dev(status_dev, "status_dev", 4)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto cleanup = [] {};
+  AWQ_CUDA(launch_gemm_reference(static_cast<const __half*>(W), N, static_cast<const __half*>(X),
+                                 T, K, Y, status_dev, s),
+           "reference GEMM");
+  return ok();
+}
+
+awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* sX,
+                            const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
+                            awq_result** out) {
+  if (out == nullptr) return fail(AWQ_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  awq_status st;
+  if ((st = check_cfg(cfg)) != AWQ_OK) return st;
+  if (T < 1) return fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
+  if (K < 1 || K % cfg->group_size)
+    return fail(AWQ_ERR_INVALID, "K=%lld (must be a positive multiple of group_size=%d)",
+                static_cast<long long>(K), cfg->group_size);
+  if (Ws == nullptr || n_w < 1 || n_w > kMaxWeights)
+    return fail(AWQ_ERR_INVALID, "n_w=%d (1..%d) with a non-NULL Ws", n_w, kMaxWeights);
+  if ((st = check_dev(X, "X", 16)) != AWQ_OK) return st;
+  if (sX != nullptr && (st = check_dev(sX, "sX", 8)) != AWQ_OK) return st;
+  RowMap map{};
+  map.n_w = n_w;
+  int64_t n_pad = 0, n_total = 0;
+  for (int i = 0; i < n_w; ++i) {
+    if (Ws[i].N < 1)
+      return fail(AWQ_ERR_INVALID, "Ws[%d].N=%lld (must be >= 1)", i,
+                  static_cast<long long>(Ws[i].N));
+    char name[32];
+    snprintf(name, sizeof(name), "Ws[%d].W", i);
+    if ((st = check_dev(Ws[i].W, name, 16)) != AWQ_OK) return st;
+    map.pad_off[i] = n_pad;
+    map.rows[i] = Ws[i].N;
+    map.cum[i] = n_total;
+    n_pad += ceil_div(Ws[i].N, kTileM) * kTileM;
+    n_total += Ws[i].N;
+  }
+  const int G = cfg->n_grid;
+  const int64_t groups = K / cfg->group_size;
+  const int64_t n_tiles = ceil_div(T, kTileN);
+  if (K > (int64_t(1) << 30) || T > (int64_t(1) << 30) || n_pad > (int64_t(1) << 30) ||
+      (n_pad / kTileM) * n_tiles * G > (int64_t(1) << 30))
+    return fail(AWQ_ERR_INVALID, "shape too large for one call");
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  awq_result* r = new (std::nothrow) awq_result();
+  if (r == nullptr) return fail(AWQ_ERR_OOM, "host allocation failed");
+  void* ws = nullptr;
+  auto cleanup = [&] {
+    if (ws) cudaFreeAsync(ws, s);
+    if (r) {
+      if (r->block) cudaFreeAsync(r->block, s);
+      give_mirror(r->host);
+      delete r;
+      r = nullptr;
+    }
+  };
+  r->stream = s;
+  r->n_grid = G;
+  r->n_w = n_w;
+  r->bits = cfg->bits;
+  r->group = cfg->group_size;
+  r->K = K;
+  r->T = T;
+  r->n_total = n_total;
+  for (int i = 0; i < n_w; ++i) r->rows[i] = Ws[i].N;
+  r->host = take_mirror();
+  if (r->host == nullptr) {
+    cleanup();
+    return fail(AWQ_ERR_OOM, "pinned host allocation failed");
+  }
+
+  // Result block.
+  Carver rc;
+  const size_t o_s = rc.take<float>(K);
+  const size_t o_sg = rc.take<float>(int64_t(G) * K);
+  const size_t o_best = rc.take<int>(1);
+  const size_t o_alpha = rc.take<double>(1);
+  const size_t o_loss = rc.take<double>(G);
+  const size_t o_rows = rc.take<double>(int64_t(G) * n_total);
+  const size_t o_status = rc.take<int>(1);
+  size_t o_codes[kMaxWeights], o_scales[kMaxWeights], o_zeros[kMaxWeights];
+  for (int i = 0; i < n_w; ++i) {
+    o_codes[i] = rc.take<uint32_t>(awq_packed_words(Ws[i].N, K, cfg->bits));
+    o_scales[i] = rc.take<__half>(Ws[i].N * groups);
+    o_zeros[i] = rc.take<uint8_t>(Ws[i].N * groups);
+  }
+  // Scratch block.
+  Carver wc;
+  const size_t o_acc = wc.take<unsigned long long>(K);
+  const size_t o_sx = wc.take<double>(K);
+  const size_t o_u = wc.take<double>(int64_t(G) * K);
+  const size_t o_mm = wc.take<unsigned long long>(2 * G);
+  const size_t o_r = wc.take<float>(int64_t(G) * K);
+  const size_t o_d = wc.take<__half>(int64_t(G) * n_pad * K);
+  const size_t o_pt = wc.take<float>(int64_t(G) * n_tiles * n_pad);
+
+  AWQ_CUDA(pool_alloc(&r->block, rc.off, s), "result allocation");
+  AWQ_CUDA(pool_alloc(&ws, wc.off, s), "scratch allocation");
+  char* rb = static_cast<char*>(r->block);
+  char* wb = static_cast<char*>(ws);
+  r->s = reinterpret_cast<float*>(rb + o_s);
+  r->s_grid = reinterpret_cast<float*>(rb + o_sg);
+  r->best = reinterpret_cast<int*>(rb + o_best);
+  r->alpha = reinterpret_cast<double*>(rb + o_alpha);
+  r->losses = reinterpret_cast<double*>(rb + o_loss);
+  r->row_losses = reinterpret_cast<double*>(rb + o_rows);
+  r->status = reinterpret_cast<int*>(rb + o_status);
+  for (int i = 0; i < n_w; ++i) {
+    r->codes[i] = reinterpret_cast<uint32_t*>(rb + o_codes[i]);
+    r->scales[i] = reinterpret_cast<__half*>(rb + o_scales[i]);
+    r->zeros[i] = reinterpret_cast<uint8_t*>(rb + o_zeros[i]);
+  }
+  auto* acc = reinterpret_cast<unsigned long long*>(wb + o_acc);
+  auto* sx_ws = reinterpret_cast<double*>(wb + o_sx);
+  auto* u_ws = reinterpret_cast<double*>(wb + o_u);
+  auto* mm_ws = reinterpret_cast<unsigned long long*>(wb + o_mm);
+  auto* r_ws = reinterpret_cast<float*>(wb + o_r);
+  auto* delta = reinterpret_cast<__half*>(wb + o_d);
+  auto* partials = reinterpret_cast<float*>(wb + o_pt);
+  const __half* Xh = static_cast<const __half*>(X);
+
+  AWQ_CUDA(cudaMemsetAsync(r->status, 0, sizeof(int), s), "status reset");
+  // Padding rows of the residual (between weights) must be exactly 0.
+  for (int i = 0; i < n_w; ++i) {
+    const int64_t pad_rows = ceil_div(Ws[i].N, kTileM) * kTileM - Ws[i].N;
+    if (pad_rows == 0) continue;
+    AWQ_CUDA(cudaMemset2DAsync(delta + (map.pad_off[i] + Ws[i].N) * K,
+                               sizeof(__half) * n_pad * K, 0, sizeof(__half) * pad_rows * K, G,
+                               s),
+             "residual padding reset");
+  }
+  // 1. channel statistic
+  const double* sxp = sX;
+  if (sxp == nullptr) {
+    AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, s), "stats kernel");
+    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s), "stats finalize kernel");
+    sxp = sx_ws;
+  }
+  // 2. scales (and their fp32 reciprocals) for every grid point
+  AWQ_CUDA(launch_scales(sxp, K, G, u_ws, mm_ws, r->s_grid, r_ws, s), "scale kernels");
+  // 3. quantize every weight at every grid point; keep the fp16 residual
+  for (int i = 0; i < n_w; ++i)
+    AWQ_CUDA(launch_quant_residual(static_cast<const __half*>(Ws[i].W), Ws[i].N, K, cfg->bits,
+                                   cfg->group_size, r->s_grid, r_ws, G, map.pad_off[i], n_pad,
+                                   delta, s),
+             "quantize kernel (residual)");
+  // 4. error GEMM for every grid point: per-row sums of (residual X^T)^2
+  AWQ_CUDA(launch_gemm_error(delta, Xh, T, K, n_pad, G, partials, r->status, s), "error GEMM");
+  // 5. losses and argmin
+  AWQ_CUDA(launch_loss_reduce(partials, G, static_cast<int>(n_tiles), n_pad, T, map, n_total,
+                              r->row_losses, r->losses, r->best, r->alpha, s),
+           "loss reduction");
+  // 6. final quantization at the chosen grid point (index read on the device)
+  for (int i = 0; i < n_w; ++i)
+    AWQ_CUDA(launch_quant_final(static_cast<const __half*>(Ws[i].W), Ws[i].N, K, cfg->bits,
+                                cfg->group_size, r->s_grid, r->best, r->codes[i], r->scales[i],
+                                r->zeros[i], s),
+             "quantize kernel (final)");
+  AWQ_CUDA(launch_copy_selected(r->s_grid, r->best, K, r->s, s), "scale copy");
+  // 7. small outputs to pinned host memory
+  AWQ_CUDA(cudaMemcpyAsync(r->host->losses, r->losses, sizeof(double) * G, cudaMemcpyDeviceToHost,
+                           s),
+           "loss copy");
+  AWQ_CUDA(cudaMemcpyAsync(&r->host->best, r->best, sizeof(int), cudaMemcpyDeviceToHost, s),
+           "index copy");
+  AWQ_CUDA(cudaMemcpyAsync(&r->host->alpha, r->alpha, sizeof(double), cudaMemcpyDeviceToHost, s),
+           "alpha copy");
+  AWQ_CUDA(cudaMemcpyAsync(&r->host->status, r->status, sizeof(int), cudaMemcpyDeviceToHost, s),
+           "status copy");
+  AWQ_CUDA(cudaFreeAsync(ws, s), "scratch release");
+  ws = nullptr;
+  *out = r;
+  return ok();
+}
+
+awq_status awq_result_check(const awq_result* r) {
+  if (r == nullptr) return fail(AWQ_ERR_INVALID, "result is NULL");
+  if (r->host->status != 0)
+    return fail(AWQ_ERR_TIMEOUT, "a bounded device wait expired (device code %d)",
+                r->host->status);
+  return ok();
+}
+
+int awq_result_n_grid(const awq_result* r) { return r ? r->n_grid : 0; }
+int awq_result_n_weights(const awq_result* r) { return r ? r->n_w : 0; }
+int awq_result_best_index(const awq_result* r) { return r ? r->host->best : -1; }
+double awq_result_alpha(const awq_result* r) { return r ? r->host->alpha : -1.0; }
+const double* awq_result_losses(const awq_result* r) { return r ? r->host->losses : nullptr; }
+const float* awq_result_s(const awq_result* r) { return r ? r->s : nullptr; }
+const float* awq_result_s_grid(const awq_result* r) { return r ? r->s_grid : nullptr; }
+const double* awq_result_row_losses(const awq_result* r) { return r ? r->row_losses : nullptr; }
+const uint32_t* awq_result_codes(const awq_result* r, int i) {
+  return (r && i >= 0 && i < r->n_w) ? r->codes[i] : nullptr;
+}
+const void* awq_result_scales(const awq_result* r, int i) {
+  return (r && i >= 0 && i < r->n_w) ? r->scales[i] : nullptr;
+}
+const uint8_t* awq_result_zeros(const awq_result* r, int i) {
+  return (r && i >= 0 && i < r->n_w) ? r->zeros[i] : nullptr;
+}
+
+void awq_free(awq_result* r) {
+  if (r == nullptr) return;
+  if (r->block) cudaFreeAsync(r->block, r->stream);
+  give_mirror(r->host);
+  delete r;
+}
+
+awq_status awq_release_cached_memory(void) {
+  cudaError_t e;
+  cudaMemPool_t pool = pool_for_current_device(&e);
+  if (pool == nullptr) return cuda_fail(e, "pool lookup");
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+  e = cudaMemPoolTrimTo(pool, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "pool trim");
+  return ok();
+}
+
+awq_status awq_selftest_bounded_wait(int64_t limit_ns) {
+  if (limit_ns < 1000 || limit_ns > 5000000000ll)
+    return fail(AWQ_ERR_INVALID, "limit_ns=%lld (1e3..5e9)", static_cast<long long>(limit_ns));
+  int* status = nullptr;
+  auto cleanup = [&] {
+    if (status) cudaFree(status);
+  };
+  AWQ_CUDA(cudaMalloc(&status, sizeof(int)), "status allocation");
+  AWQ_CUDA(cudaMemset(status, 0, sizeof(int)), "status reset");
+  AWQ_CUDA(launch_wait_selftest(static_cast<unsigned long long>(limit_ns), status, nullptr),
+           "self-test launch");
+  AWQ_CUDA(cudaDeviceSynchronize(), "self-test synchronize");
+  int h = 0;
+  AWQ_CUDA(cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost), "status copy");
+  cleanup();
+  if (h == kDevTimeoutSelfTest)
+    return fail(AWQ_ERR_TIMEOUT, "bounded wait expired as expected (device code %d)", h);
+  if (h != 0) return fail(AWQ_ERR_CUDA, "unexpected device code %d", h);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,396 @@
+// The one dense contraction of the scale search, on tcgen05 tensor cores.
+//
+// AWQ Explained (multigrid.ai), "How the scale is chosen": alpha* minimises
+// || W x - Q(W diag(s)) diag(s)^-1 x || over the calibration batch.  Written
+// as (W - deq(Q(W diag(s))) diag(s)^-1) x, the error of every grid point is
+// one GEMM of the fp16 quantization residual (produced by the quantizer pass)
+// with the calibration activations.  One persistent, warp-specialised kernel
+// evaluates all grid points:
+//
+//   warp 4      TMA producer: residual tile [128 x 64] and X tile [256 x 64],
+//               both 128-byte swizzled, into a 4-stage shared-memory ring;
+//   warp 5      owns TMEM (2 x 256 fp32 columns) and issues tcgen05.mma
+//               (M 128, N 256, K 16, fp16 in, fp32 accumulate);
+//   warps 0-3   epilogue: tcgen05.ld the finished accumulator (warp w reads
+//               lanes 32w..32w+31 = tile rows), square and sum each row over
+//               the tile's 256 tokens, write one fp32 partial per row.
+//
+// The same kernel with a row-major fp32 store in the epilogue computes the
+// reference output Y = W X^T.
+#include <mutex>
+
+#include "awq_internal.h"
+#include "awq_ptx.cuh"
+
+namespace awq {
+namespace {
+
+constexpr int BM = kTileM, BN = kTileN, BK = kTileK;
+constexpr int STAGES = 4;
+constexpr int kEpilogueWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 32 * kEpilogueWarps;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t A_BYTES = BM * BK * 2;   // fp16 A tile
+constexpr uint32_t B_BYTES = BN * BK * 2;   // fp16 X tile
+
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_BYTES;
+constexpr uint32_t NUM_BARS = 2 * STAGES + 5;   // full, empty, tfull x2, tempty x2, drain
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // slack to align the base to 1024
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
+
+constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+
+struct GemmArgs {
+  int num_m_tiles;   // tiles along weight rows
+  int num_n_tiles;   // tiles along tokens
+  int num_alpha;     // grid points (1 for the reference output)
+  int k_blocks;      // K / BK
+  int64_t T;         // real tokens
+  int64_t n_pad;     // rows of the partials layout (error mode)
+  int64_t n_rows;    // real rows (reference mode)
+  float* y;          // reference mode: [n_rows][T]
+  float* partials;   // error mode: [alpha][n_tiles][n_pad]
+  int* status;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& a, int& nt,
+                                            int& mt) {
+  const int per_alpha = p.num_m_tiles * p.num_n_tiles;
+  a = tile / per_alpha;
+  const int rem = tile - a * per_alpha;
+  nt = rem / p.num_m_tiles;
+  mt = rem - nt * p.num_m_tiles;
+}
+
+template <bool kError>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+           const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + OFF_BAR;
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, kEpilogueThreads);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = p.num_m_tiles * p.num_n_tiles * p.num_alpha;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, fills = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        int a, nt, mt;
+        decode_tile(tile, p, a, nt, mt);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status,
+                                 kDevTimeoutEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+          if (kError)
+            tma_load_3d(sbase + OFF_A + stage * A_BYTES, &tmap_a, fb, kb * BK, mt * BM, a);
+          else
+            tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, fb, kb * BK, mt * BM);
+          tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmap_b, fb, kb * BK, nt * BN);
+          ++fills;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before shared memory is released.
+        for (uint32_t s = 0; s < STAGES && s < fills; ++s) {
+          const uint32_t n_s = (fills - s + STAGES - 1) / STAGES;   // fills of stage s
+          mbar_wait_bounded(bar_full + 8 * s, (n_s - 1u) & 1u, nullptr, p.status,
+                            kDevTimeoutDrain, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true, issued = false;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+        const uint32_t acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status,
+                               kDevTimeoutTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status,
+                                 kDevTimeoutFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + OFF_A + stage * A_BYTES;
+          const uint32_t b_addr = sbase + OFF_B + stage * B_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            umma_f16(d_tmem, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k),
+                     kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(bar_tfull + 8 * acc);
+      }
+      if (!ok && issued) {
+        // Wait for the MMAs in flight before TMEM is released.
+        umma_commit(bar_drain);
+        mbar_wait_bounded(bar_drain, 0, nullptr, p.status, kDevTimeoutDrain, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp;               // TMEM lane quarter (warps 0-3)
+    const int row = q * 32 + lane;    // tile row
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+      int a, nt, mt;
+      decode_tile(tile, p, a, nt, mt);
+      const uint32_t acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      // tcgen05.ld is warp-collective: decide together and reconverge.
+      const bool ready = __all_sync(0xFFFFFFFFu,
+                                    mbar_wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag,
+                                                      p.status, kDevTimeoutTmemFull));
+      if (!ready) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (kError) {
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float e0 = __uint_as_float(v[j]);
+            const float e1 = __uint_as_float(v[j + 1]);
+            sum0 = fmaf(e0, e0, sum0);
+            sum1 = fmaf(e1, e1, sum1);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_tempty + 8 * acc);
+        p.partials[(static_cast<int64_t>(a) * p.num_n_tiles + nt) * p.n_pad +
+                   static_cast<int64_t>(mt) * BM + row] = sum0 + sum1;
+      } else {
+        const int64_t grow = static_cast<int64_t>(mt) * BM + row;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (grow < p.n_rows) {
+            float* yr = p.y + grow * p.T;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int64_t col = static_cast<int64_t>(nt) * BN + c * 32 + j;
+              if (col < p.T) yr[col] = __uint_as_float(v[j]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_tempty + 8 * acc);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void k_wait_selftest(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  const uint32_t bar = smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on this barrier: the wait must give up.
+    mbar_wait_bounded(bar, 0, nullptr, status, kDevTimeoutSelfTest, limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// fp16 tensor [depth][rows][cols] (cols contiguous), box 64 x box_rows (x 1),
+// 128-byte swizzle; depth 1 gives a 2-D map.
+bool make_tmap_f16(CUtensorMap* m, const void* base, int64_t depth, int64_t rows, int64_t cols,
+                   int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(depth)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                                 static_cast<cuuint64_t>(cols) * 2 * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t rank = depth > 1 ? 3 : 2;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <bool kError>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
+                   cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_gemm<kError>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int total = args.num_m_tiles * args.num_n_tiles * args.num_alpha;
+  const int grid = total < sm_count() ? total : sm_count();
+  k_gemm<kError><<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, int64_t T,
+                                  int64_t K, float* y, int* status, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_tmap_f16(&ta, W, 1, N, K, BM) || !make_tmap_f16(&tb, X, 1, T, K, BN))
+    return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.num_m_tiles = static_cast<int>(ceil_div(N, BM));
+  a.num_n_tiles = static_cast<int>(ceil_div(T, BN));
+  a.num_alpha = 1;
+  a.k_blocks = static_cast<int>(K / BK);
+  a.T = T;
+  a.n_rows = N;
+  a.y = y;
+  a.status = status;
+  return launch<false>(ta, tb, a, st);
+}
+
+cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
+                              int64_t n_pad, int n_alpha, float* partials, int* status,
+                              cudaStream_t st) {
+  CUtensorMap ta, tb;
+  // A 3-D map even for one grid point keeps the kernel's coordinates uniform.
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(n_pad),
+                                static_cast<cuuint64_t>(n_alpha)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
+                                   static_cast<cuuint64_t>(K) * 2 * static_cast<cuuint64_t>(n_pad)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BM), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(delta), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (!make_tmap_f16(&tb, X, 1, T, K, BN)) return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.num_m_tiles = static_cast<int>(n_pad / BM);
+  a.num_n_tiles = static_cast<int>(ceil_div(T, BN));
+  a.num_alpha = n_alpha;
+  a.k_blocks = static_cast<int>(K / BK);
+  a.T = T;
+  a.n_pad = n_pad;
+  a.partials = partials;
+  a.status = status;
+  return launch<true>(ta, tb, a, st);
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st) {
+  k_wait_selftest<<<1, 32, 0, st>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace awq

@@ -1,0 +1,92 @@
+// Host-side launchers shared between the C ABI (awq_api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace awq {
+
+// Device status codes written to the per-call status word.
+enum DeviceError : int {
+  kDevOk = 0,
+  kDevTimeoutFull = 1,      // producer data never arrived
+  kDevTimeoutEmpty = 2,     // a stage was never released
+  kDevTimeoutAReady = 3,    // dequantized operand never arrived
+  kDevTimeoutTmemFull = 4,  // accumulator never completed
+  kDevTimeoutTmemEmpty = 5, // accumulator never drained
+  kDevTimeoutDrain = 6,     // in-flight copies/MMAs did not finish on abort
+  kDevTimeoutSelfTest = 7,  // the self-test wait expired (expected there)
+};
+
+constexpr int kMaxWeights = 16;
+constexpr int kMaxGrid = 64;
+
+// ---- error GEMM geometry (one CTA tile = 128 weight rows x 256 tokens)
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kTileK = 64;
+
+// Map from the padded "virtual row" space used by the error GEMM (every
+// weight's rows start on a multiple of kTileM) to the compact row order of
+// the result (weights concatenated).
+struct RowMap {
+  int n_w;
+  int64_t pad_off[kMaxWeights];   // first virtual row of weight i
+  int64_t rows[kMaxWeights];      // N_i
+  int64_t cum[kMaxWeights];       // first compact row of weight i
+};
+
+// ---- statistics and scales (awq_stats.cu)
+cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
+                                    unsigned long long* acc, cudaStream_t st);
+cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int64_t K,
+                                  double* sX, cudaStream_t st);
+// u_ws: [n_grid][K] fp64 scratch; maxmin_ws: [2*n_grid] u64 scratch that this
+// launcher initialises itself.  r (nullable): fp32 1/s [n_grid][K].
+cudaError_t launch_scales(const double* sX, int64_t K, int n_grid, double* u_ws,
+                          unsigned long long* maxmin_ws, float* s, float* r,
+                          cudaStream_t st);
+
+// ---- group quantizer (awq_quant.cu)
+// Search output: delta[a][row_off + n][k] = fp16(w - (q - z) * scale / s_k)
+// for every grid point a, rows of weight i placed at row_off in a row space
+// of n_pad rows.
+cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bits, int group,
+                                  const float* s_grid, const float* r_grid, int n_alpha,
+                                  int64_t row_off, int64_t n_pad, __half* delta,
+                                  cudaStream_t st);
+// Result layout: packed codes, fp16 scales [N][K/group], u8 zeros [N][K/group].
+// The scale vector is s + (*sel) * K when sel is non-null, else s.
+cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, int group,
+                               const float* s, const int* sel, uint32_t* codes,
+                               __half* scales, uint8_t* zeros, cudaStream_t st);
+cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
+                          cudaStream_t st);
+cudaError_t launch_copy_selected(const float* s_grid, const int* sel, int64_t K, float* s_out,
+                                 cudaStream_t st);
+
+// ---- tcgen05 GEMMs (awq_gemm.cu)
+// Y = W X^T in fp32, row-major [N][T].
+cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, int64_t T,
+                                  int64_t K, float* y, int* status, cudaStream_t st);
+// partials[a][n_tile][n_pad] = sum over the tile's tokens of (delta[a] X^T)^2
+// for every grid point a (delta: fp16 [n_alpha][n_pad][K]).
+cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
+                              int64_t n_pad, int n_alpha, float* partials, int* status,
+                              cudaStream_t st);
+// Self-test of the bounded wait: one CTA waits on an mbarrier nothing
+// arrives at; *status receives kDevTimeoutSelfTest after ~limit_ns.
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st);
+
+// ---- loss reduction (awq_reduce.cu)
+cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
+                               int64_t T, const RowMap& map, int64_t n_total,
+                               double* row_losses, double* losses, int* best,
+                               double* alpha_out, cudaStream_t st);
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace awq

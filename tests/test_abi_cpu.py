@@ -1,0 +1,115 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol include/awq.h declares, and rejects bad arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import post_weight_quantization_33_b300 as awq
+from post_weight_quantization_33_b300 import build as awq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    awq_build.build()
+    return awq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(awq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(awq.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_no_oracle_in_library_sources():
+    csrc = os.path.join(ROOT, "post_weight_quantization_33_b300")
+    for dirpath, _, files in os.walk(csrc):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_version_and_status_strings(L):
+    assert L.awq_abi_version() == 1
+    assert L.awq_status_string(0) == b"AWQ_OK"
+    assert L.awq_status_string(5) == b"AWQ_ERR_TIMEOUT"
+    assert L.awq_status_string(99) == b"AWQ_ERR_UNKNOWN"
+
+
+def test_packed_words(L):
+    assert L.awq_packed_words(4096, 4096, 4) == 4096 * 512
+    assert L.awq_packed_words(3, 4096, 3) == 3 * 384
+    assert L.awq_packed_words(1, 100, 4) == -1
+    assert L.awq_packed_words(1, 48, 3) == -1
+    assert L.awq_packed_words(1, 64, 5) == -1
+    assert L.awq_packed_words(0, 64, 4) == 0
+
+
+def _cfg(bits=4, group=128, zp=1, n_grid=20):
+    return ctypes.byref(awq.QConfig(bits, group, zp, n_grid))
+
+
+def test_invalid_arguments_rejected_before_launch(L):
+    INVALID, UNSUPPORTED = awq.AWQ_ERR_INVALID, awq.AWQ_ERR_UNSUPPORTED
+    assert L.awq_stats(None, 16, 64, None, None) == INVALID
+    assert b"X" in L.awq_last_error()
+    assert L.awq_stats(None, 0, 64, None, None) == INVALID
+    assert b"T=0" in L.awq_last_error()
+    assert L.awq_stats(None, 4, 60, None, None) == INVALID
+    assert L.awq_scales(None, 64, 0, None, None) == INVALID
+    assert L.awq_scales(None, 64, 65, None, None) == INVALID
+    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(bits=5), None, None, None, None) == UNSUPPORTED
+    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(group=32), None, None, None, None) == UNSUPPORTED
+    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(zp=0), None, None, None, None) == UNSUPPORTED
+    assert L.awq_quantize_pack(None, 4, 200, None, _cfg(), None, None, None, None) == INVALID
+    assert L.awq_quantize_pack(None, 4, 256, None, None, None, None, None, None) == INVALID
+    # N = 0 is a valid no-op and touches no pointer.
+    assert L.awq_quantize_pack(None, 0, 256, None, _cfg(), None, None, None, None) == 0
+    assert L.awq_unpack_codes(None, 2, 100, 4, None, None) == INVALID
+    assert L.awq_reference_output(None, 4, None, 4, 100, None, None, None) == INVALID
+    out = ctypes.c_void_p()
+    w = (awq.Weight * 1)()
+    assert L.awq_search_layer(None, 16, 256, None, w, 1, _cfg(), None, None) == INVALID
+    assert L.awq_search_layer(None, 0, 256, None, w, 1, _cfg(), None, ctypes.byref(out)) == INVALID
+    assert L.awq_search_layer(None, 16, 256, None, w, 0, _cfg(), None, ctypes.byref(out)) == INVALID
+    assert L.awq_search_layer(None, 16, 256, None, w, 17, _cfg(), None, ctypes.byref(out)) == INVALID
+    assert L.awq_search_layer(None, 16, 256, None, w, 1, _cfg(n_grid=0), None,
+                              ctypes.byref(out)) == INVALID
+    assert out.value is None
+    assert L.awq_selftest_bounded_wait(10) == INVALID
+    assert L.awq_result_check(None) == INVALID
+    L.awq_free(None)   # ignored
+
+
+def test_host_pointer_rejected(L):
+    # A host buffer must be refused by the pointer check, never launched on.
+    buf = (ctypes.c_char * 4096)()
+    sx = (ctypes.c_double * 64)()
+    st = L.awq_stats(ctypes.addressof(buf), 16, 64, ctypes.addressof(sx), None)
+    assert st == awq.AWQ_ERR_INVALID
+
+
+def test_binding_validates_tensors():
+    X = torch.zeros((4, 64), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        awq.stats(X)                       # CPU tensor
+    with pytest.raises(TypeError):
+        awq.stats(X.float())
+    with pytest.raises(ValueError):
+        awq.stats(torch.zeros(64, dtype=torch.float16))

@@ -1,0 +1,319 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bars: bit-exact for codes, packed words, zeros, fp16 scales and the exact
+channel statistic; per-grid-point loss within 1e-3 relative; the chosen alpha
+equal unless the oracle's two best losses are within 1e-3 relative; s within
+1 ulp (the fp64 pow of the two sides may differ in its last bit).
+"""
+import numpy as np
+import pytest
+import torch
+
+import post_weight_quantization_33_b300 as awq
+import workloads
+from oracle import awq_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+LOSS_RTOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    awq.lib()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def words_u32(t):
+    return host(t).view(np.uint32)
+
+
+# --------------------------------------------------------------------------
+# Failure path: the bounded wait expires, reports, and the context survives.
+# --------------------------------------------------------------------------
+def test_bounded_wait_expires_and_context_survives():
+    assert awq.selftest_bounded_wait(20_000_000) == awq.AWQ_ERR_TIMEOUT
+    X = cuda(np.ones((4, 64), np.float16))
+    assert np.all(host(awq.stats(X)) == 1.0)
+
+
+# --------------------------------------------------------------------------
+# Channel statistic: exact.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("T,K", [(1, 8), (17, 64), (64, 512), (333, 4104), (2048, 1024)])
+def test_stats_bit_exact(T, K):
+    rng = workloads.weight_rng(T * 7 + K)
+    X = (rng.standard_normal((T, K)) * rng.uniform(0.01, 100, K)).astype(np.float16)
+    assert np.array_equal(host(awq.stats(cuda(X))), O.channel_magnitude(X))
+
+
+def test_stats_extreme_values():
+    X = np.zeros((40, 64), np.float16)
+    X[:, 0] = np.float16(65504.0)
+    X[:, 1] = np.float16(-65504.0)
+    X[:, 2] = np.float16(2.0 ** -24)          # smallest subnormal
+    X[::2, 3] = np.float16(-(2.0 ** -14))     # smallest normal
+    X[:, 4] = np.float16(1.0)
+    assert np.array_equal(host(awq.stats(cuda(X))), O.channel_magnitude(X))
+
+
+# --------------------------------------------------------------------------
+# Scales.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("K", [1, 100, 4096, 11008])
+def test_scales_match_oracle(K):
+    rng = workloads.weight_rng(K)
+    sX = np.exp(rng.uniform(-3, 5, K))
+    if K > 4:
+        sX[:3] = [0.0, 1e-7, 1e-4]
+    s = host(awq.scales(cuda(sX), 20))
+    assert np.all(s[0] == 1.0)
+    same = 0
+    for i, a in enumerate(O.alpha_grid(20)):
+        want = O.scale_vector(sX, a)
+        np.testing.assert_array_max_ulp(s[i], want, maxulp=1)
+        same += int(np.sum(s[i] == want))
+    assert same >= 0.999 * 20 * K
+
+
+# --------------------------------------------------------------------------
+# Quantize + pack: bit-exact.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("bits,group", [(4, 128), (4, 64), (3, 128), (3, 64)])
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (300, 1024), (129, 4096)])
+def test_quantize_pack_bit_exact(bits, group, N, K):
+    rng = workloads.weight_rng(N * 31 + K + bits * 7 + group)
+    W = (rng.standard_t(4, (N, K)) * 0.02).astype(np.float16)
+    W[0, :group] = 0                                   # a constant (all-zero) group
+    s = np.exp(rng.uniform(-1.5, 1.5, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group)
+    oc, osc, oz = O.quantize_groups(W, s, bits, group)
+    assert np.array_equal(words_u32(codes).reshape(N, -1), O.pack_codes(oc, bits))
+    assert np.array_equal(host(sc).view(np.uint16), osc.view(np.uint16))
+    assert np.array_equal(host(z), oz)
+
+
+def test_quantize_pack_empty():
+    W = torch.empty((0, 128), dtype=torch.float16, device="cuda")
+    s = torch.ones(128, dtype=torch.float32, device="cuda")
+    codes, sc, z = awq.quantize_pack(W, s, 4, 128)
+    assert codes.numel() == 0 and sc.numel() == 0 and z.numel() == 0
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_unpack_roundtrip(bits):
+    rng = workloads.weight_rng(40 + bits)
+    q = rng.integers(0, 1 << bits, (37, 512)).astype(np.uint8)
+    packed = O.pack_codes(q, bits).reshape(-1).view(np.int32)
+    got = host(awq.unpack_codes(cuda(packed), 37, 512, bits))
+    assert np.array_equal(got, q)
+
+
+# --------------------------------------------------------------------------
+# Reference GEMM Y = W X^T (tcgen05).
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("N,T,K", [(128, 256, 64), (1, 1, 64), (200, 300, 192), (256, 64, 512),
+                                   (1000, 1000, 1024), (384, 520, 4096)])
+def test_reference_output(N, T, K):
+    rng = workloads.weight_rng(N + T + K)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    X = rng.standard_normal((T, K)).astype(np.float16)
+    Y = host(awq.reference_output(cuda(W), cuda(X)))
+    W64, X64 = W.astype(np.float64), X.astype(np.float64)
+    want = W64 @ X64.T
+    mag = np.abs(W64) @ np.abs(X64).T
+    err = np.abs(Y - want)
+    assert np.all(err <= 1e-6 * mag + 1e-30), float((err / (mag + 1e-30)).max())
+
+
+# --------------------------------------------------------------------------
+# Full search vs the oracle.
+# --------------------------------------------------------------------------
+def _argmin_ok(gpu_best, oracle_losses):
+    ob = int(np.argmin(oracle_losses))
+    if gpu_best == ob:
+        return True
+    order = np.argsort(oracle_losses)
+    lo, second = oracle_losses[order[0]], oracle_losses[order[1]]
+    close = (second - lo) <= LOSS_RTOL * lo
+    return close and gpu_best in (order[0], order[1])
+
+
+def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=2e-3):
+    res = awq.search(cuda(X), [cuda(W) for W in Ws], bits, group, n_grid)
+    res.check()
+    ref = O.search(X, Ws, bits, group, n_grid)
+    losses = res.losses
+    np.testing.assert_allclose(losses, ref["losses"], rtol=LOSS_RTOL, atol=0)
+    assert _argmin_ok(res.best, ref["losses"]), (res.best, ref["losses"])
+    assert res.best == O.first_argmin(losses)
+    assert res.alpha == res.best / n_grid
+    s_best = host(res.s())
+    s_grid = host(res.s_grid())
+    np.testing.assert_array_max_ulp(s_grid, ref["s_grid"], maxulp=1)
+    assert np.array_equal(s_best, s_grid[res.best])
+    rl = host(res.row_losses())
+    off = 0
+    for i, W in enumerate(Ws):
+        n = W.shape[0]
+        np.testing.assert_allclose(rl[:, off:off + n], ref["row_losses"][i], rtol=rows_rtol,
+                                   atol=1e-12 * max(1.0, float(ref["row_losses"][i].max())))
+        off += n
+        # codes at the GPU's alpha, bit-exact against the oracle quantizer fed the GPU's s
+        oc, osc, oz = O.quantize_groups(W, s_best, bits, group)
+        assert np.array_equal(words_u32(res.codes(i)).reshape(n, -1), O.pack_codes(oc, bits))
+        assert np.array_equal(host(res.scales(i)).view(np.uint16), osc.view(np.uint16))
+        assert np.array_equal(host(res.zeros(i)), oz)
+    # and the loss vector is the normalised sum of the row losses
+    tot = np.zeros(n_grid)
+    off = 0
+    T = X.shape[0]
+    for W in Ws:
+        n = W.shape[0]
+        tot += rl[:, off:off + n].sum(axis=1) / (n * T)
+        off += n
+    np.testing.assert_allclose(losses, tot, rtol=1e-12)
+    res.free()
+    return ref
+
+
+def test_search_tiny_workload():
+    t = workloads.generate("tiny")
+    ref = _compare_search(t["X"], [t["W"]], 4, 128)
+    assert ref["best"] > 0
+
+
+@pytest.mark.parametrize("case", [
+    dict(N=(1,), K=128, T=64, bits=4, group=128),
+    dict(N=(200,), K=256, T=300, bits=4, group=128),
+    dict(N=(130, 60), K=256, T=77, bits=4, group=64),
+    dict(N=(96,), K=512, T=40, bits=3, group=64),
+    dict(N=(128,), K=384, T=256, bits=3, group=128),
+    dict(N=(256,), K=64, T=513, bits=4, group=64),
+], ids=lambda c: f"N{c['N']}-K{c['K']}-T{c['T']}-b{c['bits']}-g{c['group']}")
+def test_search_edge_shapes(case):
+    Ws = []
+    X = None
+    for j, n in enumerate(case["N"]):
+        W, X0 = workloads.random_layer(n, case["K"], case["T"], seed=100 + j + n,
+                                       outliers=(1, case["K"] // 2), factor=25.0)
+        Ws.append(W)
+        X = X0 if X is None else X
+    _compare_search(X, Ws, case["bits"], case["group"])
+
+
+def test_search_single_row_single_token_within_rounding_bound():
+    """N = T = 1: the loss of each grid point is one squared dot product
+    E = sum_k delta_k x_k, which can cancel to almost nothing, so a relative
+    bar does not apply.  The residual is rounded to fp16 (|error| <= 2^-11 of
+    each term) and accumulated in fp32, so |E_gpu - E| <= B with
+    B = (2^-11 + K 2^-23) * sum_k |delta_k x_k|; check |sqrt(loss)| within B."""
+    W, X = workloads.random_layer(1, 128, 1, seed=101, outliers=(1, 64), factor=25.0)
+    res = awq.search(cuda(X), [cuda(W)], 4, 128)
+    res.check()
+    ref = O.search(X, [W], 4, 128)
+    s_grid = host(res.s_grid())
+    for a in range(20):
+        c, sc, z = O.quantize_groups(W, s_grid[a], 4, 128)
+        delta = W.astype(np.float64) - O.dequantize_scaled(c, sc, z, 128) / s_grid[a].astype(
+            np.float64)
+        mag = float(np.abs(delta[0] * X[0].astype(np.float64)).sum())
+        bound = (2.0 ** -11 + 128 * 2.0 ** -23) * mag
+        assert abs(np.sqrt(res.losses[a]) - np.sqrt(ref["losses"][a])) <= bound, a
+    res.free()
+
+
+def test_search_degenerate_inputs():
+    rng = workloads.weight_rng(77)
+    W = (rng.standard_normal((64, 256)) * 0.02).astype(np.float16)
+    W[:5] = 0                                  # all-zero rows: exact, zero loss
+    X = rng.standard_normal((50, 256)).astype(np.float16)
+    X[:, 7] = 0                                # a dead input channel (sX = 0)
+    X[:, 200] *= np.float16(300)               # a huge outlier channel
+    _compare_search(X, [W], 4, 128)
+
+
+def test_search_given_sx_and_small_grid():
+    W, X = workloads.random_layer(128, 256, 64, seed=5, outliers=(9,), factor=40.0)
+    sX = O.channel_magnitude(X)
+    res = awq.search(cuda(X), [cuda(W)], 4, 128, n_grid=5, sX=cuda(sX))
+    res.check()
+    ref = O.search(X, [W], 4, 128, n_grid=5, sX=sX)
+    np.testing.assert_allclose(res.losses, ref["losses"], rtol=LOSS_RTOL)
+    res.free()
+
+
+def test_search_deterministic():
+    t = workloads.generate("tiny")
+    a = awq.search(cuda(t["X"]), [cuda(t["W"])])
+    b = awq.search(cuda(t["X"]), [cuda(t["W"])])
+    assert np.array_equal(a.losses, b.losses)
+    assert np.array_equal(host(a.row_losses()), host(b.row_losses()))
+    assert np.array_equal(words_u32(a.codes()), words_u32(b.codes()))
+
+
+def test_bad_pointers_rejected_on_gpu():
+    X = cuda(np.ones((8, 128), np.float16))
+    Xmis = X.view(-1)[1:1 + 8 * 64].view(8, 64)      # 2-byte offset: misaligned for TMA
+    with pytest.raises(awq.AwqError) as e:
+        awq.stats(Xmis)
+    assert e.value.status == awq.AWQ_ERR_INVALID
+    L = awq.lib()
+    sx = torch.empty(128, dtype=torch.float64, device="cuda")
+    host_buf = np.ones((8, 128), np.float16)
+    assert L.awq_stats(host_buf.ctypes.data, 8, 128, sx.data_ptr(), None) == awq.AWQ_ERR_INVALID
+
+
+# --------------------------------------------------------------------------
+# Full-size workloads, sampled rows (the configuration the benchmark times).
+# --------------------------------------------------------------------------
+def _sample_rows(n):
+    return np.unique(np.array([0, 1, 127, 128, n // 2, n - 129, n - 1]).clip(0, n - 1))
+
+
+@pytest.mark.parametrize("name", ["llama7b_attn", "llama7b_mlp", "llama70b", "int3_stress"])
+def test_full_size_workload_sampled(name):
+    wl = workloads.WORKLOADS[name]
+    data = workloads.generate(name)
+    for call in wl.calls:
+        X = data[call.x]
+        Ws = [data[w] for w in call.ws]
+        T = X.shape[0]
+        res = awq.search(cuda(X), [cuda(W) for W in Ws], call.bits, call.group)
+        res.check()
+        losses = res.losses
+        assert res.best == O.first_argmin(losses)
+        rl = host(res.row_losses())
+        s_grid = host(res.s_grid())
+        sX = O.channel_magnitude(X)
+        want_s = np.stack([O.scale_vector(sX, a) for a in O.alpha_grid(20)])
+        np.testing.assert_array_max_ulp(s_grid, want_s, maxulp=1)
+        rows = [_sample_rows(W.shape[0]) for W in Ws]
+        ref = O.search(X, Ws, call.bits, call.group, sX=sX, rows=rows)
+        off = 0
+        tot = np.zeros(20)
+        for i, W in enumerate(Ws):
+            n = W.shape[0]
+            np.testing.assert_allclose(rl[:, off + rows[i]], ref["row_losses"][i], rtol=2e-3)
+            tot += rl[:, off:off + n].sum(axis=1) / (n * T)
+            off += n
+            s_best = s_grid[res.best]
+            oc, osc, oz = O.quantize_groups(W, s_best, call.bits, call.group)
+            assert np.array_equal(words_u32(res.codes(i)).reshape(n, -1),
+                                  O.pack_codes(oc, call.bits))
+            assert np.array_equal(host(res.scales(i)).view(np.uint16), osc.view(np.uint16))
+            assert np.array_equal(host(res.zeros(i)), oz)
+        np.testing.assert_allclose(losses, tot, rtol=1e-12)
+        res.free()
