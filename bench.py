@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Throughput of the AWQ per-layer scale search on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl awq|reference]
+
+One step is one full search (channel statistic, scales, residuals for the
+20-point grid, tcgen05 error GEMM, losses, argmin, final quantize + pack) of
+the workload's calls.  The default workload is the LLaMA-7B attention
+projection: W 4096x4096 fp16, X 4096 tokens x 4096 fp16 with 1 % outlier
+channels, INT4 group 128.  Metric: weights searched per second (sum of N*K
+over the searched weights / time).  Timing: CUDA events on the launching
+stream around each step, L2 flushed (256 MiB write) between steps outside the
+events, a barrier and a device synchronisation on both sides of the timed
+region, the maximum over ranks.  Under torchrun every rank searches its own
+replica of the workload (independent layers: no collective on the data path,
+weak scaling).
+
+``--impl reference`` times the CPU oracle (numpy, fp64) on the host cores on
+a bounded row sample of the same workload, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "AWQ search: weights searched/s (20-α grid, T calib tokens); % of roofline"
+UNIT = "weights/s"
+N_GRID = 20
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "error_gemm_llama7b_attn.md")
+GEMM_SOURCES = [os.path.join(ROOT, "post_weight_quantization_33_b300", "csrc", f)
+                for f in ("awq_gemm.cu", "awq_ptx.cuh")]
+
+
+# --------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), tflops=float(p["bf16_tflops"]),
+                    tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6400.0, tflops=1800.0, tflops_sustained=1400.0, source="fallback")
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per error-GEMM launch from the committed ncu summary, if the
+    kernel sources are unchanged since the capture; else None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    vals = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            line = line.strip().lstrip("-").strip()
+            if line.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != gemm_source_hash():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, interval_ms: int = 50):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", gpu_id, "-lms", str(interval_ms)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) >= 9]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(wl) -> int:
+    """Bytes the method itself must move: statistic over X, quantize (read W,
+    write codes + fp16 scale + u8 zero per group) and the error GEMM's operand
+    reads (codes-sized weights and X), per grid point."""
+    total = 0
+    for call in wl.calls:
+        x = wl.spec(call.x)
+        total += 2 * x.rows * x.cols
+        for w in call.ws:
+            s = wl.spec(w)
+            nk = s.rows * s.cols
+            per_grid = (2 * nk + nk * call.bits // 8 + 3 * nk // call.group) + \
+                       (nk * call.bits // 8 + 3 * nk // call.group + 2 * x.rows * x.cols)
+            total += N_GRID * per_grid
+    return total
+
+
+def config_for(name: str, sample: str | None = None) -> dict:
+    wl = workloads.WORKLOADS[name]
+    calls = []
+    for c in wl.calls:
+        x = wl.spec(c.x)
+        calls.append({"X": [x.rows, x.cols],
+                      "W": [[wl.spec(w).rows, wl.spec(w).cols] for w in c.ws],
+                      "bits": c.bits, "group": c.group})
+    cfg = {"workload": f"{name}: {wl.description}", "calls": calls, "grid_points": N_GRID,
+           "l2": "flushed between timed steps (256 MiB write, outside the step events)"}
+    if sample:
+        cfg["sample"] = sample
+    return cfg
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_step(data, wl, rows_per_weight: int):
+    from oracle import awq_oracle as O
+    done = 0
+    for call in wl.calls:
+        X = data[call.x]
+        Ws = [data[w] for w in call.ws]
+        rows = [np.arange(min(rows_per_weight, W.shape[0])) for W in Ws]
+        O.search(X, Ws, call.bits, call.group, N_GRID, rows=rows)
+        done += sum(len(r) * W.shape[1] for r, W in zip(rows, Ws))
+    return done
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else 1
+    except Exception:
+        return 1
+
+
+def cpu_baseline(data, wl, target_s: float = 15.0) -> dict:
+    """The oracle as it stands on a bounded row sample (about target_s of CPU work)."""
+    rows = 64
+    t0 = time.perf_counter()
+    oracle_step(data, wl, rows)
+    dt = time.perf_counter() - t0
+    max_rows = min(wl.spec(w).rows for c in wl.calls for w in c.ws)
+    rows = int(min(max_rows, max(64, rows * target_s / max(dt, 1e-3))))
+    rows = max(64, rows // 64 * 64)
+    t0 = time.perf_counter()
+    n = oracle_step(data, wl, rows)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid "
+                      f"points ({n} weights searched in {dt:.1f} s; numpy fp64, BLAS threads as "
+                      f"in 'cores', elementwise work single-threaded)"}
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    wl = workloads.WORKLOADS[args.workload]
+    data = workloads.generate(args.workload)
+    rows = args.reference_rows
+    for _ in range(args.warmup):
+        oracle_step(data, wl, rows)
+    times, n = [], 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        n = oracle_step(data, wl, rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = n * args.steps / total
+    sample = (f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid points "
+              f"per step ({n} weights)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_for(args.workload, sample),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_awq(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import post_weight_quantization_33_b300 as awq
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    awq.lib()
+    wl = workloads.WORKLOADS[args.workload]
+    data = workloads.generate(args.workload)
+    calls = []
+    for c in wl.calls:
+        calls.append((torch.from_numpy(data[c.x]).to(dev),
+                      [torch.from_numpy(data[w]).to(dev) for w in c.ws], c.bits, c.group))
+    weights_per_step = wl.weights_searched()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def step():
+        res = [awq.search(X, Ws, bits, group, N_GRID) for X, Ws, bits, group in calls]
+        return res
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    awq.set_stage_timing(True)
+    for _ in range(args.warmup):
+        for r in step():
+            r.check()
+            r.free()
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kept = []
+    barrier()
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    gpu_id = (f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:"
+              f"{getattr(props, 'pci_device_id', 0):02X}.0") if bus is not None else str(local_rank)
+    clocks = ClockSampler(gpu_id)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i)
+        starts[i].record(stream)
+        kept.append(step())
+        ends[i].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    launches = 0
+    gemm_ms = []
+    for res in kept:
+        for r in res:
+            r.check()
+            launches += r.kernel_launches
+            gemm_ms.append(r.stage_ms()["error_gemm"])
+            r.free()
+    awq.set_stage_timing(False)
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    value = weights_per_step * args.steps * world / (total_ms / 1e3)
+
+    # End to end through the public API with host (pinned) buffers.
+    host_calls = [(torch.from_numpy(data[c.x]).pin_memory(),
+                   [torch.from_numpy(data[w]).pin_memory() for w in c.ws], c.bits, c.group)
+                  for c in wl.calls]
+    h2d = sum(X.numel() * 2 + sum(W.numel() * 2 for W in Ws) for X, Ws, _, _ in host_calls)
+    d2h = 0
+    for X, Ws, bits, group in host_calls:
+        for W in Ws:
+            n, k = W.shape
+            d2h += awq.packed_words(n, k, bits) * 4 + 3 * n * (k // group)
+        d2h += X.shape[1] * 4 + N_GRID * 8
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        for X, Ws, bits, group in host_calls:
+            awq.search_host(X, Ws, bits, group, N_GRID, device=dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(e2e_steps):
+        flush.fill_(i)
+        e0.record(stream)
+        for X, Ws, bits, group in host_calls:
+            awq.search_host(X, Ws, bits, group, N_GRID, device=dev)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_value = weights_per_step * e2e_steps * world / (float(t.item()) / 1e3)
+
+    if rank != 0:
+        return
+    pk = peaks()
+    # One error-GEMM launch per call; with several calls this is their average.
+    flops_per_launch = wl.gemm_flops(N_GRID) / len(wl.calls)
+    gemm_avg_ms = statistics.mean(gemm_ms)
+    achieved = flops_per_launch / (gemm_avg_ms / 1e3) / 1e12
+    ideal_s = max(wl.gemm_flops(N_GRID) / (pk["tflops"] * 1e12),
+                  algorithmic_bytes(wl) / (pk["hbm_gbs"] * 1e9))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": config_for(args.workload),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / pk["tflops"],
+                     "traffic": profiled_traffic(),
+                     "kernel": "k_gemm<true> (tcgen05 error GEMM), fp16 operands, f32 accumulate",
+                     "peak_source": f"{pk['source']} bf16 burst (dense fp16 taken equal)",
+                     "launch_ms": gemm_avg_ms},
+        "step_roofline": {"ideal_ms": ideal_s * 1e3, "frac": ideal_s * 1e3 / (total_ms / args.steps)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s": t_wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(data, wl)
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["awq", "reference"], default="awq")
+    ap.add_argument("--workload", default="llama7b_attn", choices=list(workloads.WORKLOAD_ORDER))
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (used for profiler runs)")
+    ap.add_argument("--reference-rows", type=int, default=64,
+                    help="output rows per weight in each oracle step of --impl reference")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_awq(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

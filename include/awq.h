@@ -60,6 +60,15 @@ extern "C" {
 #define AWQ_MAX_GRID 64
 #define AWQ_MAX_WEIGHTS 16
 
+/* Stages of awq_search_layer, in order (for awq_result_stage_ms). */
+#define AWQ_STAGE_STATS 0       /* channel statistic (skipped when sX is given) */
+#define AWQ_STAGE_SCALES 1      /* s and 1/s for every grid point */
+#define AWQ_STAGE_RESIDUAL 2    /* quantizer residual for every weight and grid point */
+#define AWQ_STAGE_ERROR_GEMM 3  /* tcgen05 GEMM + squared-error epilogue */
+#define AWQ_STAGE_LOSS 4        /* per-row and per-grid-point losses, argmin */
+#define AWQ_STAGE_FINAL 5       /* quantize + pack at the chosen grid point */
+#define AWQ_NUM_STAGES 6
+
 typedef enum awq_status {
   AWQ_OK = 0,
   AWQ_ERR_INVALID = 1,     /* bad argument (null, misaligned, host pointer, bad size) */
@@ -187,6 +196,18 @@ const double* awq_result_row_losses(const awq_result* r); /* device fp64 [n_grid
 const uint32_t* awq_result_codes(const awq_result* r, int i);  /* device packed codes of W_i */
 const void* awq_result_scales(const awq_result* r, int i);     /* device fp16 [N_i][K/group] */
 const uint8_t* awq_result_zeros(const awq_result* r, int i);   /* device uint8 [N_i][K/group] */
+
+/* Number of kernels the search enqueued (host value, valid on return). */
+int awq_result_kernel_launches(const awq_result* r);
+
+/* Turn per-stage timing of later awq_search_layer calls on (1) or off (0),
+ * process-wide.  When on, each search records CUDA events on its stream at
+ * the stage boundaries (a few microseconds of overhead). */
+void awq_set_stage_timing(int enable);
+
+/* Milliseconds the GPU spent in `stage` (AWQ_STAGE_*) of a search that ran
+ * with stage timing on; valid once the stream is synchronised. */
+awq_status awq_result_stage_ms(const awq_result* r, int stage, float* ms);
 
 /* Release a result.  Its device memory returns to the library's pool in the
  * order of the stream the search ran on, so call this before destroying that

@@ -27,7 +27,8 @@ import torch
 __all__ = [
     "AwqError", "lib", "library_path", "stats", "scales", "quantize_pack", "unpack_codes",
     "reference_output", "search", "search_host", "SearchResult", "packed_words",
-    "release_cached_memory", "selftest_bounded_wait", "EXPORTED_SYMBOLS",
+    "release_cached_memory", "selftest_bounded_wait", "set_stage_timing", "STAGES",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,8 +45,12 @@ EXPORTED_SYMBOLS = (
     "awq_result_n_weights", "awq_result_best_index", "awq_result_alpha", "awq_result_losses",
     "awq_result_s", "awq_result_s_grid", "awq_result_row_losses", "awq_result_codes",
     "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
-    "awq_selftest_bounded_wait",
+    "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
+    "awq_result_stage_ms",
 )
+
+# Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
+STAGES = ("stats", "scales", "residual", "error_gemm", "loss", "final")
 
 
 class AwqError(RuntimeError):
@@ -105,6 +110,9 @@ def lib() -> ctypes.CDLL:
         "awq_free": (None, [vp]),
         "awq_release_cached_memory": (st, []),
         "awq_selftest_bounded_wait": (st, [i64]),
+        "awq_result_kernel_launches": (i32, [vp]),
+        "awq_set_stage_timing": (None, [i32]),
+        "awq_result_stage_ms": (st, [vp, i32, ctypes.POINTER(ctypes.c_float)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -288,6 +296,20 @@ class SearchResult:
         return _alias(lib().awq_result_zeros(self._handle(), i),
                       (self.Ns[i], self.K // self.group), "|u1", self.device).clone()
 
+    @property
+    def kernel_launches(self) -> int:
+        return int(lib().awq_result_kernel_launches(self._handle()))
+
+    def stage_ms(self) -> dict:
+        """GPU milliseconds per stage (needs set_stage_timing(True) before the search)."""
+        self.synchronize()
+        out = {}
+        for i, name in enumerate(STAGES):
+            v = ctypes.c_float()
+            _check(lib().awq_result_stage_ms(self._handle(), i, ctypes.byref(v)))
+            out[name] = float(v.value)
+        return out
+
     def free(self) -> None:
         if self._h:
             lib().awq_free(self._h)
@@ -346,6 +368,11 @@ def search_host(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, grou
     finally:
         r.free()
     return out
+
+
+def set_stage_timing(enable: bool) -> None:
+    """Record CUDA events at stage boundaries of later searches (see stage_ms)."""
+    lib().awq_set_stage_timing(1 if enable else 0)
 
 
 def release_cached_memory() -> None:

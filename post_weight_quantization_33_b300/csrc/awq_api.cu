@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <vector>
@@ -137,6 +138,8 @@ struct HostMirror {
   double losses[kMaxGrid];
 };
 
+std::atomic<int> g_stage_timing{0};
+
 std::mutex g_mirror_mu;
 std::vector<HostMirror*> g_mirrors;
 
@@ -165,6 +168,9 @@ void give_mirror(HostMirror* m) {
 
 }  // namespace
 
+struct awq_result;
+static void destroy_events(awq_result* r);
+
 struct awq_result {
   cudaStream_t stream = nullptr;
   int n_grid = 0, n_w = 0, bits = 0, group = 0;
@@ -182,7 +188,15 @@ struct awq_result {
   uint32_t* codes[kMaxWeights] = {};
   __half* scales[kMaxWeights] = {};
   uint8_t* zeros[kMaxWeights] = {};
+  int launches = 0;                     // kernels this call enqueued
+  cudaEvent_t ev[AWQ_NUM_STAGES + 1] = {};   // stage boundaries (timing enabled)
+  bool timed = false;
 };
+
+static void destroy_events(awq_result* r) {
+  for (int e = 0; e <= AWQ_NUM_STAGES; ++e)
+    if (r->ev[e]) cudaEventDestroy(r->ev[e]);
+}
 
 extern "C" {
 
@@ -362,6 +376,7 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
     if (r) {
       if (r->block) cudaFreeAsync(r->block, s);
       give_mirror(r->host);
+      destroy_events(r);
       delete r;
       r = nullptr;
     }
@@ -441,34 +456,59 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
                                s),
              "residual padding reset");
   }
+  // Optional stage boundaries (awq_set_stage_timing): events on this stream.
+  if (g_stage_timing.load()) {
+    for (int e = 0; e <= AWQ_NUM_STAGES; ++e)
+      AWQ_CUDA(cudaEventCreate(&r->ev[e]), "event creation");
+    r->timed = true;
+  }
+  auto mark = [&](int e) -> cudaError_t {
+    return r->timed ? cudaEventRecord(r->ev[e], s) : cudaSuccess;
+  };
+  AWQ_CUDA(mark(AWQ_STAGE_STATS), "event record");
   // 1. channel statistic
   const double* sxp = sX;
   if (sxp == nullptr) {
     AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, s), "stats kernel");
     AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s), "stats finalize kernel");
+    r->launches += 2;
     sxp = sx_ws;
   }
+  AWQ_CUDA(mark(AWQ_STAGE_SCALES), "event record");
   // 2. scales (and their fp32 reciprocals) for every grid point
   AWQ_CUDA(launch_scales(sxp, K, G, u_ws, mm_ws, r->s_grid, r_ws, s), "scale kernels");
+  r->launches += 3;
+  AWQ_CUDA(mark(AWQ_STAGE_RESIDUAL), "event record");
   // 3. quantize every weight at every grid point; keep the fp16 residual
-  for (int i = 0; i < n_w; ++i)
+  for (int i = 0; i < n_w; ++i) {
     AWQ_CUDA(launch_quant_residual(static_cast<const __half*>(Ws[i].W), Ws[i].N, K, cfg->bits,
                                    cfg->group_size, r->s_grid, r_ws, G, map.pad_off[i], n_pad,
                                    delta, s),
              "quantize kernel (residual)");
+    r->launches += 1;
+  }
+  AWQ_CUDA(mark(AWQ_STAGE_ERROR_GEMM), "event record");
   // 4. error GEMM for every grid point: per-row sums of (residual X^T)^2
   AWQ_CUDA(launch_gemm_error(delta, Xh, T, K, n_pad, G, partials, r->status, s), "error GEMM");
+  r->launches += 1;
+  AWQ_CUDA(mark(AWQ_STAGE_LOSS), "event record");
   // 5. losses and argmin
   AWQ_CUDA(launch_loss_reduce(partials, G, static_cast<int>(n_tiles), n_pad, T, map, n_total,
                               r->row_losses, r->losses, r->best, r->alpha, s),
            "loss reduction");
+  r->launches += 3;
+  AWQ_CUDA(mark(AWQ_STAGE_FINAL), "event record");
   // 6. final quantization at the chosen grid point (index read on the device)
-  for (int i = 0; i < n_w; ++i)
+  for (int i = 0; i < n_w; ++i) {
     AWQ_CUDA(launch_quant_final(static_cast<const __half*>(Ws[i].W), Ws[i].N, K, cfg->bits,
                                 cfg->group_size, r->s_grid, r->best, r->codes[i], r->scales[i],
                                 r->zeros[i], s),
              "quantize kernel (final)");
+    r->launches += 1;
+  }
   AWQ_CUDA(launch_copy_selected(r->s_grid, r->best, K, r->s, s), "scale copy");
+  r->launches += 1;
+  AWQ_CUDA(mark(AWQ_NUM_STAGES), "event record");
   // 7. small outputs to pinned host memory
   AWQ_CUDA(cudaMemcpyAsync(r->host->losses, r->losses, sizeof(double) * G, cudaMemcpyDeviceToHost,
                            s),
@@ -515,7 +555,22 @@ void awq_free(awq_result* r) {
   if (r == nullptr) return;
   if (r->block) cudaFreeAsync(r->block, r->stream);
   give_mirror(r->host);
+  destroy_events(r);
   delete r;
+}
+
+void awq_set_stage_timing(int enable) { g_stage_timing.store(enable ? 1 : 0); }
+
+int awq_result_kernel_launches(const awq_result* r) { return r ? r->launches : -1; }
+
+awq_status awq_result_stage_ms(const awq_result* r, int stage, float* ms) {
+  if (r == nullptr || ms == nullptr) return fail(AWQ_ERR_INVALID, "result or ms is NULL");
+  if (stage < 0 || stage >= AWQ_NUM_STAGES)
+    return fail(AWQ_ERR_INVALID, "stage=%d (0..%d)", stage, AWQ_NUM_STAGES - 1);
+  if (!r->timed) return fail(AWQ_ERR_INVALID, "stage timing was off during this search");
+  const cudaError_t e = cudaEventElapsedTime(ms, r->ev[stage], r->ev[stage + 1]);
+  if (e != cudaSuccess) return cuda_fail(e, "event elapsed time");
+  return ok();
 }
 
 awq_status awq_release_cached_memory(void) {

@@ -264,6 +264,25 @@ def test_search_deterministic():
     assert np.array_equal(words_u32(a.codes()), words_u32(b.codes()))
 
 
+def test_stage_timing_and_launch_count():
+    W, X = workloads.random_layer(256, 512, 300, seed=6)
+    awq.set_stage_timing(True)
+    try:
+        r = awq.search(cuda(X), [cuda(W)])
+        r.check()
+        ms = r.stage_ms()
+        assert set(ms) == set(awq.STAGES) and all(v >= 0 for v in ms.values())
+        assert ms["error_gemm"] > 0
+        assert r.kernel_launches == 12   # 2 stats + 3 scales + 1 residual + 1 GEMM + 3 loss + 2 final
+        r.free()
+    finally:
+        awq.set_stage_timing(False)
+    r = awq.search(cuda(X), [cuda(W)])
+    with pytest.raises(awq.AwqError):
+        r.stage_ms()
+    r.free()
+
+
 def test_bad_pointers_rejected_on_gpu():
     X = cuda(np.ones((8, 128), np.float16))
     Xmis = X.view(-1)[1:1 + 8 * 64].view(8, 64)      # 2-byte offset: misaligned for TMA
