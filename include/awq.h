@@ -218,6 +218,27 @@ void awq_free(awq_result* r);
  * device to the driver (synchronises the device). */
 awq_status awq_release_cached_memory(void);
 
+/* The channel statistic of awq_stats, computed without allocating any device
+ * memory (no counterpart on the AWQ pages: this is an operational variant).
+ * For callers that cannot let a library allocate: processes that give all
+ * device memory to their own allocator at start-up and forbid later
+ * allocations, latency-critical loops in which cudaMalloc/cudaFree would
+ * synchronise the device, or code running inside another allocator's
+ * callback.  The 64-bit accumulator lives in a fixed array inside the
+ * library (AWQ_STATS_NOALLOC_MAX_K * 8 bytes = 512 KiB, held on every device
+ * that loads the library until the process exits).
+ *   X, T, K, sX, stream : as awq_stats; K <= AWQ_STATS_NOALLOC_MAX_K, else
+ *                         AWQ_ERR_INVALID (use awq_stats for wider layers).
+ * The first call on each device looks the array's device address up (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array, which keeps the last call's
+ * sums; each call clears the K entries it uses, on its stream, before
+ * accumulating.  Calls whose work overlaps on the GPU (different streams, or
+ * different host threads without ordering) race on the array and give wrong
+ * results: order them. */
+#define AWQ_STATS_NOALLOC_MAX_K 65536
+awq_status awq_stats_noalloc(const void* X, int64_t T, int64_t K, double* sX, void* stream);
+
 /* Self-test of the bounded device wait: launches one CTA that waits on a
  * barrier nothing arrives at, with a limit of limit_ns nanoseconds
  * (1e3..5e9), synchronises, and returns AWQ_ERR_TIMEOUT when the wait expired

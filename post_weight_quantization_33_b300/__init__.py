@@ -25,7 +25,7 @@ import numpy as np
 import torch
 
 __all__ = [
-    "AwqError", "lib", "library_path", "stats", "scales", "quantize_pack", "unpack_codes",
+    "AwqError", "lib", "library_path", "stats", "stats_noalloc", "scales", "quantize_pack", "unpack_codes",
     "reference_output", "search", "search_host", "SearchResult", "packed_words",
     "release_cached_memory", "selftest_bounded_wait", "set_stage_timing", "STAGES",
     "EXPORTED_SYMBOLS",
@@ -46,7 +46,7 @@ EXPORTED_SYMBOLS = (
     "awq_result_s", "awq_result_s_grid", "awq_result_row_losses", "awq_result_codes",
     "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
     "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
-    "awq_result_stage_ms",
+    "awq_result_stage_ms", "awq_stats_noalloc",
 )
 
 # Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
         "awq_status_string": (ctypes.c_char_p, [i32]),
         "awq_packed_words": (i64, [i64, i64, i32]),
         "awq_stats": (st, [vp, i64, i64, vp, vp]),
+        "awq_stats_noalloc": (st, [vp, i64, i64, vp, vp]),
         "awq_scales": (st, [vp, i64, i32, vp, vp]),
         "awq_quantize_pack": (st, [vp, i64, i64, vp, ctypes.POINTER(QConfig), vp, vp, vp, vp]),
         "awq_unpack_codes": (st, [vp, i64, i64, i32, vp, vp]),
@@ -162,6 +163,17 @@ def stats(X: torch.Tensor) -> torch.Tensor:
     T, K = X.shape
     sX = torch.empty(K, dtype=torch.float64, device=X.device)
     _check(lib().awq_stats(X.data_ptr(), T, K, sX.data_ptr(), _stream()))
+    return sX
+
+
+def stats_noalloc(X: torch.Tensor) -> torch.Tensor:
+    """As stats(), through awq_stats_noalloc: the library allocates no device
+    memory (its accumulator is a fixed array inside the library; K <= 65536).
+    Calls must not overlap on the GPU."""
+    _require(X, "X", torch.float16, 2)
+    T, K = X.shape
+    sX = torch.empty(K, dtype=torch.float64, device=X.device)
+    _check(lib().awq_stats_noalloc(X.data_ptr(), T, K, sX.data_ptr(), _stream()))
     return sX
 
 

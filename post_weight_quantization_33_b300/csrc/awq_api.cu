@@ -606,3 +606,25 @@ awq_status awq_selftest_bounded_wait(int64_t limit_ns) {
 }
 
 }  // extern "C"
+
+// Status helpers for entry points defined in other translation units; they
+// share this file's thread-local error message.  Not exported.
+#define AWQ_HIDDEN __attribute__((visibility("hidden")))
+
+AWQ_HIDDEN awq_status awq_internal_fail(awq_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+AWQ_HIDDEN awq_status awq_internal_ok() { return ok(); }
+
+AWQ_HIDDEN awq_status awq_internal_check_dev(const void* p, const char* name, uintptr_t align) {
+  return check_dev(p, name, align);
+}
+
+AWQ_HIDDEN awq_status awq_internal_cuda_fail(cudaError_t e, const char* what) {
+  return cuda_fail(e, what);
+}
