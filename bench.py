@@ -292,11 +292,15 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     launches = 0
     gemm_ms = []
+    stage_sum = {name: 0.0 for name in awq.STAGES}
     for res in kept:
         for r in res:
             r.check()
             launches += r.kernel_launches
-            gemm_ms.append(r.stage_ms()["error_gemm"])
+            st = r.stage_ms()
+            gemm_ms.append(st["error_gemm"])
+            for name in stage_sum:
+                stage_sum[name] += st[name]
             r.free()
     awq.set_stage_timing(False)
     total_ms = sum(step_ms)
@@ -362,6 +366,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches,
+        "stages_ms_per_step": {k: v / args.steps for k, v in stage_sum.items()},
         "clocks": clk,
         "wall_s": t_wall,
     }

@@ -420,6 +420,7 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   const size_t o_r = wc.take<float>(int64_t(G) * K);
   const size_t o_d = wc.take<__half>(int64_t(G) * n_pad * K);
   const size_t o_pt = wc.take<float>(int64_t(G) * n_tiles * n_pad);
+  const size_t o_cnt = wc.take<unsigned int>(1);
 
   AWQ_CUDA(pool_alloc(&r->block, rc.off, s), "result allocation");
   AWQ_CUDA(pool_alloc(&ws, wc.off, s), "scratch allocation");
@@ -444,6 +445,7 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   auto* r_ws = reinterpret_cast<float*>(wb + o_r);
   auto* delta = reinterpret_cast<__half*>(wb + o_d);
   auto* partials = reinterpret_cast<float*>(wb + o_pt);
+  auto* counter = reinterpret_cast<unsigned int*>(wb + o_cnt);
   const __half* Xh = static_cast<const __half*>(X);
 
   AWQ_CUDA(cudaMemsetAsync(r->status, 0, sizeof(int), s), "status reset");
@@ -470,14 +472,15 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   const double* sxp = sX;
   if (sxp == nullptr) {
     AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, s), "stats kernel");
-    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s), "stats finalize kernel");
+    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s, mm_ws, G), "stats finalize kernel");
     r->launches += 2;
     sxp = sx_ws;
   }
   AWQ_CUDA(mark(AWQ_STAGE_SCALES), "event record");
   // 2. scales (and their fp32 reciprocals) for every grid point
-  AWQ_CUDA(launch_scales(sxp, K, G, u_ws, mm_ws, r->s_grid, r_ws, s), "scale kernels");
-  r->launches += 3;
+  AWQ_CUDA(launch_scales(sxp, K, G, u_ws, mm_ws, r->s_grid, r_ws, s, sX == nullptr),
+           "scale kernels");
+  r->launches += (sX == nullptr) ? 2 : 3;
   AWQ_CUDA(mark(AWQ_STAGE_RESIDUAL), "event record");
   // 3. quantize every weight at every grid point; keep the fp16 residual
   for (int i = 0; i < n_w; ++i) {
@@ -494,9 +497,10 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   AWQ_CUDA(mark(AWQ_STAGE_LOSS), "event record");
   // 5. losses and argmin
   AWQ_CUDA(launch_loss_reduce(partials, G, static_cast<int>(n_tiles), n_pad, T, map, n_total,
-                              r->row_losses, r->losses, r->best, r->alpha, s),
+                              r->row_losses, r->losses, r->best, r->alpha, r->s_grid, K, r->s,
+                              counter, s),
            "loss reduction");
-  r->launches += 3;
+  r->launches += 2;
   AWQ_CUDA(mark(AWQ_STAGE_FINAL), "event record");
   // 6. final quantization at the chosen grid point (index read on the device)
   for (int i = 0; i < n_w; ++i) {
@@ -506,8 +510,6 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
              "quantize kernel (final)");
     r->launches += 1;
   }
-  AWQ_CUDA(launch_copy_selected(r->s_grid, r->best, K, r->s, s), "scale copy");
-  r->launches += 1;
   AWQ_CUDA(mark(AWQ_NUM_STAGES), "event record");
   // 7. small outputs to pinned host memory
   AWQ_CUDA(cudaMemcpyAsync(r->host->losses, r->losses, sizeof(double) * G, cudaMemcpyDeviceToHost,

@@ -42,13 +42,17 @@ struct RowMap {
 // ---- statistics and scales (awq_stats.cu)
 cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
                                     unsigned long long* acc, cudaStream_t st);
+// maxmin (nullable): also write the starting values of launch_scales'
+// max/min words for n_grid grid points.
 cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int64_t K,
-                                  double* sX, cudaStream_t st);
-// u_ws: [n_grid][K] fp64 scratch; maxmin_ws: [2*n_grid] u64 scratch that this
-// launcher initialises itself.  r (nullable): fp32 1/s [n_grid][K].
+                                  double* sX, cudaStream_t st,
+                                  unsigned long long* maxmin = nullptr, int n_grid = 0);
+// u_ws: [n_grid][K] fp64 scratch; maxmin_ws: [2*n_grid] u64 scratch, which
+// this launcher initialises unless maxmin_ready (done by launch_stats_finalize).
+// r (nullable): fp32 1/s [n_grid][K].
 cudaError_t launch_scales(const double* sX, int64_t K, int n_grid, double* u_ws,
-                          unsigned long long* maxmin_ws, float* s, float* r,
-                          cudaStream_t st);
+                          unsigned long long* maxmin_ws, float* s, float* r, cudaStream_t st,
+                          bool maxmin_ready = false);
 
 // ---- group quantizer (awq_quant.cu)
 // Search output: delta[a][row_off + n][k] = fp16(w - (q - z) * scale / s_k)
@@ -65,8 +69,6 @@ cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, 
                                __half* scales, uint8_t* zeros, cudaStream_t st);
 cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                           cudaStream_t st);
-cudaError_t launch_copy_selected(const float* s_grid, const int* sel, int64_t K, float* s_out,
-                                 cudaStream_t st);
 
 // ---- tcgen05 GEMMs (awq_gemm.cu)
 // Y = W X^T in fp32, row-major [N][T].
@@ -82,10 +84,12 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st);
 
 // ---- loss reduction (awq_reduce.cu)
+// Also copies s_grid[best] (K floats) to s_out.  counter: one u32 of scratch.
 cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
                                int64_t T, const RowMap& map, int64_t n_total,
                                double* row_losses, double* losses, int* best,
-                               double* alpha_out, cudaStream_t st);
+                               double* alpha_out, const float* s_grid, int64_t K, float* s_out,
+                               unsigned int* counter, cudaStream_t st);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -214,12 +214,6 @@ __global__ void k_unpack(const uint32_t* __restrict__ codes, int64_t N, int64_t 
   }
 }
 
-__global__ void k_copy_selected(const float* __restrict__ s_grid, const int* __restrict__ sel,
-                                int64_t K, float* __restrict__ out) {
-  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (k < K) out[k] = s_grid[static_cast<int64_t>(*sel) * K + k];
-}
-
 unsigned grid_for(int64_t items) {
   const int64_t blocks = ceil_div(items, kQuantThreads);
   return static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(blocks, 148 * 16)));
@@ -263,13 +257,6 @@ cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, 
 cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                           cudaStream_t st) {
   k_unpack<<<grid_for(N * K), kQuantThreads, 0, st>>>(codes, N, K, bits, q);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_copy_selected(const float* s_grid, const int* sel, int64_t K, float* s_out,
-                                 cudaStream_t st) {
-  k_copy_selected<<<static_cast<unsigned>(ceil_div(K, 256)), 256, 0, st>>>(s_grid, sel, K,
-                                                                            s_out);
   return cudaGetLastError();
 }
 

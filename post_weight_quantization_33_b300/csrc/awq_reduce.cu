@@ -12,8 +12,10 @@ namespace {
 
 // row_losses[a][compact row] = sum over token tiles of partials[a][tile][virtual row].
 __global__ void k_row_losses(const float* __restrict__ partials, int n_tiles, int64_t n_pad,
-                             RowMap map, int64_t n_total, double* __restrict__ row_losses) {
+                             RowMap map, int64_t n_total, double* __restrict__ row_losses,
+                             unsigned int* __restrict__ counter) {
   const int a = blockIdx.y;
+  if (a == 0 && blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
   const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (v >= n_pad) return;
   int w = 0;
@@ -27,10 +29,18 @@ __global__ void k_row_losses(const float* __restrict__ partials, int n_tiles, in
 }
 
 // losses[a] = sum_w (sum_n row_losses[a][w, n]) / (N_w * T); one block per a.
+// The last block to finish (counted on *counter, zeroed by k_row_losses)
+// takes the argmin -- first minimum, NaN as +inf -- and copies the chosen
+// scale vector to s_out.
 __global__ void k_grid_losses(const double* __restrict__ row_losses, RowMap map, int64_t n_total,
-                              int64_t T, double* __restrict__ losses) {
+                              int64_t T, double* __restrict__ losses, int* __restrict__ best,
+                              double* __restrict__ alpha_out, const float* __restrict__ s_grid,
+                              int64_t K, float* __restrict__ s_out,
+                              unsigned int* __restrict__ counter) {
   __shared__ double red[256];
+  __shared__ int last, chosen;
   const int a = blockIdx.x;
+  const int n_grid = gridDim.x;
   const double* rl = row_losses + static_cast<int64_t>(a) * n_total;
   double total = 0.0;
   for (int w = 0; w < map.n_w; ++w) {
@@ -46,23 +56,32 @@ __global__ void k_grid_losses(const double* __restrict__ row_losses, RowMap map,
       total += red[0] / (static_cast<double>(map.rows[w]) * static_cast<double>(T));
     __syncthreads();
   }
-  if (threadIdx.x == 0) losses[a] = total;
-}
-
-__global__ void k_argmin(const double* __restrict__ losses, int n_grid, int* __restrict__ best,
-                         double* __restrict__ alpha_out) {
-  if (threadIdx.x != 0) return;
-  int bi = 0;
-  double bv = 0.0;
-  for (int i = 0; i < n_grid; ++i) {
-    const double v = isnan(losses[i]) ? INFINITY : losses[i];
-    if (i == 0 || v < bv) {
-      bi = i;
-      bv = v;
-    }
+  if (threadIdx.x == 0) {
+    losses[a] = total;
+    __threadfence();
+    last = (atomicAdd(counter, 1u) == static_cast<unsigned>(n_grid) - 1u);
   }
-  *best = bi;
-  *alpha_out = static_cast<double>(bi) / static_cast<double>(n_grid);
+  __syncthreads();
+  if (!last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const volatile double* lv = losses;
+    int bi = 0;
+    double bv = 0.0;
+    for (int i = 0; i < n_grid; ++i) {
+      const double v = isnan(lv[i]) ? INFINITY : lv[i];
+      if (i == 0 || v < bv) {
+        bi = i;
+        bv = v;
+      }
+    }
+    *best = bi;
+    *alpha_out = static_cast<double>(bi) / static_cast<double>(n_grid);
+    chosen = bi;
+  }
+  __syncthreads();
+  const float* src = s_grid + static_cast<int64_t>(chosen) * K;
+  for (int64_t k = threadIdx.x; k < K; k += blockDim.x) s_out[k] = src[k];
 }
 
 }  // namespace
@@ -70,11 +89,12 @@ __global__ void k_argmin(const double* __restrict__ losses, int n_grid, int* __r
 cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
                                int64_t T, const RowMap& map, int64_t n_total,
                                double* row_losses, double* losses, int* best,
-                               double* alpha_out, cudaStream_t st) {
+                               double* alpha_out, const float* s_grid, int64_t K, float* s_out,
+                               unsigned int* counter, cudaStream_t st) {
   const dim3 g1(static_cast<unsigned>(ceil_div(n_pad, 256)), static_cast<unsigned>(n_alpha));
-  k_row_losses<<<g1, 256, 0, st>>>(partials, n_tiles, n_pad, map, n_total, row_losses);
-  k_grid_losses<<<n_alpha, 256, 0, st>>>(row_losses, map, n_total, T, losses);
-  k_argmin<<<1, 32, 0, st>>>(losses, n_alpha, best, alpha_out);
+  k_row_losses<<<g1, 256, 0, st>>>(partials, n_tiles, n_pad, map, n_total, row_losses, counter);
+  k_grid_losses<<<n_alpha, 256, 0, st>>>(row_losses, map, n_total, T, losses, best, alpha_out,
+                                         s_grid, K, s_out, counter);
   return cudaGetLastError();
 }
 

@@ -88,9 +88,16 @@ __global__ void __launch_bounds__(kStatsThreads)
 }
 
 __global__ void k_stats_finalize(const unsigned long long* __restrict__ acc, int64_t T,
-                                 int64_t K, double* __restrict__ sX) {
+                                 int64_t K, double* __restrict__ sX,
+                                 unsigned long long* __restrict__ maxmin, int n_grid) {
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (k < K) sX[k] = (static_cast<double>(acc[k]) * 0x1p-24) / static_cast<double>(T);
+  // Starting values of the per-grid-point max/min of the scale kernels
+  // (block 0 has 256 threads >= n_grid).
+  if (maxmin != nullptr && k < n_grid) {
+    maxmin[2 * k] = 0ull;
+    maxmin[2 * k + 1] = ~0ull;
+  }
 }
 
 // u[a][k] = max(sX_k, 1e-4)^(a / n_grid) in fp64; per-grid-point max and min
@@ -172,15 +179,17 @@ cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
 }
 
 cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int64_t K,
-                                  double* sX, cudaStream_t st) {
-  k_stats_finalize<<<static_cast<unsigned>(ceil_div(K, 256)), 256, 0, st>>>(acc, T, K, sX);
+                                  double* sX, cudaStream_t st, unsigned long long* maxmin,
+                                  int n_grid) {
+  k_stats_finalize<<<static_cast<unsigned>(ceil_div(K, 256)), 256, 0, st>>>(acc, T, K, sX,
+                                                                            maxmin, n_grid);
   return cudaGetLastError();
 }
 
 cudaError_t launch_scales(const double* sX, int64_t K, int n_grid, double* u_ws,
-                          unsigned long long* maxmin_ws, float* s, float* r,
-                          cudaStream_t st) {
-  k_init_maxmin<<<1, kMaxGrid, 0, st>>>(maxmin_ws, n_grid);
+                          unsigned long long* maxmin_ws, float* s, float* r, cudaStream_t st,
+                          bool maxmin_ready) {
+  if (!maxmin_ready) k_init_maxmin<<<1, kMaxGrid, 0, st>>>(maxmin_ws, n_grid);
   const dim3 grid(static_cast<unsigned>(ceil_div(K, 256)), static_cast<unsigned>(n_grid));
   k_scale_pow<<<grid, 256, 0, st>>>(sX, K, n_grid, u_ws, maxmin_ws);
   k_scale_norm<<<grid, 256, 0, st>>>(u_ws, K, maxmin_ws, s, r);
