@@ -190,18 +190,32 @@ def blas_threads() -> int:
         return 1
 
 
+def use_all_cores() -> None:
+    """Let the oracle's one library matmul use every host core (the host may
+    start with the BLAS pool limited, e.g. by OMP_NUM_THREADS)."""
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(limits=os.cpu_count() or 1, user_api="blas")
+    except Exception:
+        pass
+
+
 def cpu_baseline(data, wl, target_s: float = 15.0) -> dict:
-    """The oracle as it stands on a bounded row sample (about target_s of CPU work)."""
-    rows = 64
-    t0 = time.perf_counter()
-    oracle_step(data, wl, rows)
-    dt = time.perf_counter() - t0
+    """The oracle as it stands on a bounded row sample (about target_s of CPU work).
+
+    The row count grows until one timed sample takes at least a third of
+    target_s (each step's cost has a part that does not scale with rows)."""
+    use_all_cores()
     max_rows = min(wl.spec(w).rows for c in wl.calls for w in c.ws)
-    rows = int(min(max_rows, max(64, rows * target_s / max(dt, 1e-3))))
-    rows = max(64, rows // 64 * 64)
-    t0 = time.perf_counter()
-    n = oracle_step(data, wl, rows)
-    dt = time.perf_counter() - t0
+    rows = 64
+    while True:
+        t0 = time.perf_counter()
+        n = oracle_step(data, wl, rows)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 3 or rows >= max_rows:
+            break
+        rows = int(min(max_rows, max(2 * rows, rows * target_s / max(dt, 1e-3))))
+        rows = max(64, rows // 64 * 64)
     return {"value": n / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid "
                       f"points ({n} weights searched in {dt:.1f} s; numpy fp64, BLAS threads as "
@@ -212,6 +226,7 @@ def cpu_baseline(data, wl, target_s: float = 15.0) -> dict:
 def run_reference(args, rank: int, world: int) -> None:
     if rank != 0:
         return
+    use_all_cores()
     wl = workloads.WORKLOADS[args.workload]
     data = workloads.generate(args.workload)
     rows = args.reference_rows

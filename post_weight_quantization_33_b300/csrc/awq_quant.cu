@@ -97,55 +97,187 @@ __device__ __forceinline__ uint32_t pack3_bits24(const Quant8& r) {
   return bits;
 }
 
-// Search output (one launch per weight, blockIdx.y = grid point a): the
-// quantization residual in the units of W,
-//   delta[a][row_off + n][k] = fp16( w - ((q - z) * scale) * (1/s_k) ),
-// i.e. W - deq(Q(W diag(s))) diag(s)^-1 row by row.  (q - z) * scale is exact
-// in fp32 (a 5-bit integer times an 11-bit significand); the product with the
-// fp32 reciprocal and the difference are single fp32 roundings, and the only
-// coarse rounding is the final one to fp16, relative to the residual itself.
+// Round half to even without the conversion unit: adding and removing
+// 1.5 * 2^23 leaves rne(t) for |t| <= 2^22 (the sum's ulp is 1, and the
+// addition rounds half to even).  The map is monotone, so for larger |t| the
+// result keeps the side of [-2^22, 2^22] that t is on, which is all the
+// clamps below ever look at.
+__device__ __forceinline__ float rne_small(float t) {
+  return __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
+}
+
+__device__ __forceinline__ void ld_v8f(const float* p, float* v) {
+  uint32_t r[8];
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Packed fp32 pairs (sm_100 f32x2 arithmetic, both lanes rounded to nearest
+// even).  ptxas fuses a packed multiply into a following packed add even with
+// .rn, so packed ops are used here only where no add consumes a product:
+// every "product, then add" of the quantizer stays in scalar intrinsics.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float a, float b) {
+  return static_cast<f32x2>(__float_as_uint(a)) | (static_cast<f32x2>(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ float lo2(f32x2 v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi2(f32x2 v) {
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Three-input min / max (exact, like fminf / fmaxf).
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Search output: the quantization residual of every grid point, in the units
+// of W,
+//   delta[a][row_off + n][k] = fp16( w - ((q - z) * scale) / s_k ),
+// i.e. W - deq(Q(W diag(s))) diag(s)^-1 row by row.  The codes and zero
+// points are those of quantize8 (same fp32 steps, same rounding); only the
+// rounding itself uses rne_small instead of a float-to-int conversion, with
+// the clamp applied to (q - z) directly:
+//   q - z = clamp(rne(w' * rcp), -z, L - z).
+// (q - z) * scale is exact in fp32 (a 4-bit integer times an 11-bit
+// significand); w - that * (1/s_k) is one fused multiply-add, and the one
+// coarse rounding is the final one to fp16, relative to the residual.
+//
+// Work split: a lane owns 16 consecutive channels of two consecutive rows (a
+// group of 128 is 8 lanes, of 64 is 4), loads s and 1/s of a grid point once
+// for both rows, and evaluates every grid point, so W is read and converted
+// to fp32 once.  A warp covers 512 channels of its row pair; the 8 warps of a
+// block take 16 consecutive rows at the same channels, so their 256-bit loads
+// of s and 1/s hit the same L1 lines.  Warps are numbered row panel (64
+// rows), channel chunk, row pair.  Each lane writes one whole 32-byte sector
+// per row and grid point.
+constexpr int kResPanel = 64;
+constexpr int kResPerLane = 16;
+constexpr int kResRowsPerLane = 2;
+
 template <int GROUP>
 __global__ void __launch_bounds__(kQuantThreads)
-    k_quant_residual(const uint4* __restrict__ W, int64_t N, int64_t K, int levels,
+    k_quant_residual(const __half* __restrict__ W, int64_t N, int64_t K, int levels,
                      const float* __restrict__ s_grid, const float* __restrict__ r_grid,
-                     int64_t row_off, int64_t n_pad, uint4* __restrict__ delta) {
-  constexpr int GLANES = GROUP / 8;
-  const int a = blockIdx.y;
-  const int64_t kc = K / 8;
-  const int64_t total = N * kc;
-  const float* s = s_grid + static_cast<int64_t>(a) * K;
-  const float* r = r_grid + static_cast<int64_t>(a) * K;
+                     int n_alpha, int64_t row_off, int64_t n_pad, __half* __restrict__ delta) {
+  constexpr int EPL = kResPerLane, RPT = kResRowsPerLane;
+  constexpr int GLANES = GROUP / EPL;
+  constexpr int SUBS = kResPanel / RPT;
+  const int64_t lanes_per_row = K / EPL;
+  const int64_t kw = (lanes_per_row + 31) / 32;      // warp chunks per row
+  const int64_t panels = (N + kResPanel - 1) / kResPanel;
+  const int64_t total_warps = panels * SUBS * kw;
   const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-       base < total; base += stride) {
-    const int64_t item = base + lane;
-    const bool active = item < total;
-    const int64_t it = active ? item : 0;
-    const int64_t row = it / kc;
-    const int64_t c = it - row * kc;
-    const uint4 wv = active ? ldg_stream(W + it) : make_uint4(0, 0, 0, 0);
-    const Quant8 q = quantize8<GLANES>(wv, s + c * 8, levels);
-    if (active) {
-      const float4 ra = __ldg(reinterpret_cast<const float4*>(r + c * 8));
-      const float4 rb = __ldg(reinterpret_cast<const float4*>(r + c * 8) + 1);
-      const float rv[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-      const float sf = __half2float(q.scale);
-      const uint32_t w32[4] = {wv.x, wv.y, wv.z, wv.w};
-      uint32_t out[4];
+  const float L = static_cast<float>(levels);
+  const int64_t slab = n_pad * K;                     // halves per grid point
+  for (int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       gw < total_warps; gw += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+    const int64_t pn = gw / (SUBS * kw);
+    const int64_t rem = gw - pn * (SUBS * kw);
+    const int64_t j = rem / SUBS;
+    const int64_t row0 = pn * kResPanel + (rem - j * SUBS) * RPT;
+    if (row0 >= N) continue;                          // whole warp: no shuffle mixes rows
+    // Lanes past the end of the row form whole groups (K % GROUP == 0), so
+    // their dummy values never meet real ones in a reduction.
+    const int64_t lc = j * 32 + lane;
+    const bool active = lc < lanes_per_row;
+    const int64_t k0 = (active ? lc : lanes_per_row - 1) * EPL;
+    float w[RPT][EPL];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 h = *reinterpret_cast<const __half2*>(&w32[i]);
-        const float d0 = __fmul_rn(static_cast<float>(static_cast<int>(q.q[2 * i]) - q.zero), sf);
-        const float d1 =
-            __fmul_rn(static_cast<float>(static_cast<int>(q.q[2 * i + 1]) - q.zero), sf);
-        const float e0 = __fsub_rn(__low2float(h), __fmul_rn(d0, rv[2 * i]));
-        const float e1 = __fsub_rn(__high2float(h), __fmul_rn(d1, rv[2 * i + 1]));
-        const __half2 e = __floats2half2_rn(e0, e1);
-        out[i] = *reinterpret_cast<const uint32_t*>(&e);
+    for (int r = 0; r < RPT; ++r) {
+      const int64_t row = min(row0 + r, N - 1);       // a lone last row loads itself twice
+      const uint4* wp = reinterpret_cast<const uint4*>(W + row * K + k0);
+#pragma unroll
+      for (int v = 0; v < EPL / 8; ++v) {
+        const uint4 q = __ldg(wp + v);
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+          w[r][8 * v + 2 * i] = f.x;
+          w[r][8 * v + 2 * i + 1] = f.y;
+        }
       }
-      delta[(static_cast<int64_t>(a) * n_pad + row_off + row) * kc + c] =
-          make_uint4(out[0], out[1], out[2], out[3]);
+    }
+#pragma unroll 1
+    for (int a = 0; a < n_alpha; ++a) {
+      float sv[EPL], rv[EPL];
+      const float* sp = s_grid + static_cast<int64_t>(a) * K + k0;
+      const float* rp = r_grid + static_cast<int64_t>(a) * K + k0;
+#pragma unroll
+      for (int v = 0; v < EPL / 8; ++v) {
+        ld_v8f(sp + 8 * v, sv + 8 * v);
+        ld_v8f(rp + 8 * v, rv + 8 * v);
+      }
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        float ws[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; i += 2) {
+          const f32x2 p = mul2(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+          ws[i] = lo2(p);
+          ws[i + 1] = hi2(p);
+        }
+        float mnA = fminf(ws[0], ws[1]), mxA = fmaxf(ws[0], ws[1]);
+        float mnB = fminf(ws[2], ws[3]), mxB = fmaxf(ws[2], ws[3]);
+#pragma unroll
+        for (int i = 4; i < EPL; i += 4) {
+          mnA = min3f(mnA, ws[i], ws[i + 1]);
+          mxA = max3f(mxA, ws[i], ws[i + 1]);
+          mnB = min3f(mnB, ws[i + 2], ws[i + 3]);
+          mxB = max3f(mxB, ws[i + 2], ws[i + 3]);
+        }
+        float mn = fminf(mnA, mnB), mx = fmaxf(mxA, mxB);
+#pragma unroll
+        for (int off = GLANES / 2; off; off >>= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        }
+        const float step = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-5f), L);
+        const float sf = __half2float(__float2half_rn(step));
+        const float rcp = __frcp_rn(sf);
+        const float z = fminf(fmaxf(rne_small(__fmul_rn(-mn, rcp)), 0.0f), L);
+        const float lo = -z, hi = L - z;
+        const f32x2 nsf = pack2(-sf, -sf);
+        uint32_t o[EPL / 2];
+#pragma unroll
+        for (int i = 0; i < EPL; i += 2) {
+          const float d0 = fminf(fmaxf(rne_small(__fmul_rn(ws[i], rcp)), lo), hi);
+          const float d1 = fminf(fmaxf(rne_small(__fmul_rn(ws[i + 1], rcp)), lo), hi);
+          // w - (d * sf) * (1/s): the product d * sf is exact.
+          const f32x2 e = fma2(mul2(pack2(d0, d1), nsf), pack2(rv[i], rv[i + 1]),
+                               pack2(w[r][i], w[r][i + 1]));
+          const __half2 hv = __floats2half2_rn(lo2(e), hi2(e));
+          o[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        const int64_t row = row0 + r;
+        if (active && row < N) st_v8(delta + a * slab + (row_off + row) * K + k0, o);
+      }
     }
   }
 }
@@ -226,15 +358,16 @@ cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bit
                                   int64_t row_off, int64_t n_pad, __half* delta,
                                   cudaStream_t st) {
   const int levels = (1 << bits) - 1;
-  const dim3 grid(grid_for(N * (K / 8)), static_cast<unsigned>(n_alpha));
-  const uint4* w = reinterpret_cast<const uint4*>(W);
-  uint4* d = reinterpret_cast<uint4*>(delta);
+  const int64_t warps = ceil_div(N, kResPanel) * (kResPanel / kResRowsPerLane) *
+                        ceil_div(K / kResPerLane, 32);
+  const int64_t blocks = ceil_div(warps * 32, kQuantThreads);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(blocks, int64_t(1) << 30));
   if (group == 128)
-    k_quant_residual<128><<<grid, kQuantThreads, 0, st>>>(w, N, K, levels, s_grid, r_grid,
-                                                          row_off, n_pad, d);
+    k_quant_residual<128><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
+                                                          n_alpha, row_off, n_pad, delta);
   else
-    k_quant_residual<64><<<grid, kQuantThreads, 0, st>>>(w, N, K, levels, s_grid, r_grid,
-                                                         row_off, n_pad, d);
+    k_quant_residual<64><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
+                                                         n_alpha, row_off, n_pad, delta);
   return cudaGetLastError();
 }
 
