@@ -181,23 +181,54 @@ def oracle_step(data, wl, rows_per_weight: int):
     return done
 
 
+def _openblas_calls():
+    """(get, set) of the OpenBLAS bundled with numpy, through its public
+    thread-count API, for hosts without threadpoolctl; (None, None) if absent."""
+    import ctypes
+    import glob
+    libdir = os.path.join(os.path.dirname(os.path.dirname(np.__file__)), "numpy.libs")
+    for path in sorted(glob.glob(os.path.join(libdir, "*openblas*.so*"))):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for prefix in ("scipy_openblas", "openblas"):
+            for suffix in ("64_", "_64_", ""):
+                get = getattr(lib, f"{prefix}_get_num_threads{suffix}", None)
+                put = getattr(lib, f"{prefix}_set_num_threads{suffix}", None)
+                if get is not None and put is not None:
+                    get.restype = ctypes.c_int
+                    put.argtypes = [ctypes.c_int]
+                    return get, put
+    return None, None
+
+
 def blas_threads() -> int:
+    """Threads of numpy's BLAS pool (the oracle's one multi-threaded step)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return int(max(n)) if n else 1
+        if n:
+            return int(max(n))
     except Exception:
-        return 1
+        pass
+    get, _ = _openblas_calls()
+    return int(get()) if get is not None else 1
 
 
 def use_all_cores() -> None:
-    """Let the oracle's one library matmul use every host core (the host may
-    start with the BLAS pool limited, e.g. by OMP_NUM_THREADS)."""
+    """Let the oracle's one library matmul use every core this process may run
+    on (the host may start with the BLAS pool limited)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     try:
         from threadpoolctl import threadpool_limits
-        threadpool_limits(limits=os.cpu_count() or 1, user_api="blas")
+        threadpool_limits(limits=cores, user_api="blas")
+        return
     except Exception:
         pass
+    _, put = _openblas_calls()
+    if put is not None:
+        put(cores)
 
 
 def cpu_baseline(data, wl, target_s: float = 15.0) -> dict:
@@ -220,6 +251,61 @@ def cpu_baseline(data, wl, target_s: float = 15.0) -> dict:
             "sample": f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid "
                       f"points ({n} weights searched in {dt:.1f} s; numpy fp64, BLAS threads as "
                       f"in 'cores', elementwise work single-threaded)"}
+
+
+def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
+    """Achieved HBM bandwidth of the two HBM-bound entry points at the
+    largest workload's sizes (X 8192x8192; W 28672x8192, INT4 g128), called
+    through the C ABI with preallocated buffers, L2 flushed between launches.
+    Bytes are the algorithmic ones: 2TK for the statistic; 2NK read +
+    NK/2 codes + 3NK/128 scales and zeros written for quantize + pack."""
+    import ctypes
+    import torch
+    import post_weight_quantization_33_b300 as awq
+    L = awq.lib()
+    stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    out = {}
+
+    def timed(fn):
+        ts = []
+        fn()
+        for i in range(reps):
+            flush.fill_(i)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    T, K = 8192, 8192
+    X = torch.randn(T, K, generator=g, device=dev).half()
+    sX = torch.empty(K, dtype=torch.float64, device=dev)
+    ms = timed(lambda: awq._check(L.awq_stats(X.data_ptr(), T, K, sX.data_ptr(), st)))
+    nbytes = 2 * T * K
+    out["stats"] = {"shape": f"X {T}x{K} fp16", "ms": ms, "bytes": nbytes,
+                    "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
+    del X
+    N, K = 28672, 8192
+    W = (torch.randn(N, K, generator=g, device=dev) * 0.015).half()
+    s = torch.rand(K, generator=g, device=dev) + 0.5
+    codes = torch.empty(N * K // 8, dtype=torch.int32, device=dev)
+    sc = torch.empty(N * K // 128, dtype=torch.float16, device=dev)
+    z = torch.empty(N * K // 128, dtype=torch.uint8, device=dev)
+    cfg = awq.QConfig(4, 128, 1, N_GRID)
+    ms = timed(lambda: awq._check(L.awq_quantize_pack(
+        W.data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg), codes.data_ptr(), sc.data_ptr(),
+        z.data_ptr(), st)))
+    nbytes = 2 * N * K + N * K // 2 + 3 * N * K // 128
+    out["quantize_pack"] = {"shape": f"W {N}x{K} fp16 -> INT4 g128", "ms": ms, "bytes": nbytes,
+                            "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
+    del W
+    return out
 
 
 # --------------------------------------------------------------------------- arms
@@ -385,6 +471,14 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         "clocks": clk,
         "wall_s": t_wall,
     }
+    # The residual pass: W read once, n_grid fp16 residuals written.
+    res_ms = stage_sum["residual"] / args.steps
+    res_bytes = sum(2 * wl.spec(w).rows * wl.spec(w).cols * (1 + N_GRID)
+                    for c in wl.calls for w in c.ws)
+    line["hbm_kernels"] = hbm_kernels(dev, flush, pk["hbm_gbs"])
+    line["hbm_kernels"]["residual"] = {
+        "shape": "this workload, every grid point", "ms": res_ms, "bytes": res_bytes,
+        "gbs": res_bytes / res_ms / 1e6, "frac": res_bytes / res_ms / 1e6 / pk["hbm_gbs"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(data, wl)
     print(json.dumps(line), flush=True)

@@ -14,8 +14,12 @@
 //   z = clamp(rn(-min * rcp), 0, 2^b - 1);  q = clamp(rn(w' * rcp) + z, 0, 2^b - 1)
 // where rn rounds half to even.
 //
-// One thread owns 8 consecutive weights of a row (one 16-byte load); a group
-// of 64 or 128 weights is 8 or 16 adjacent lanes, reduced with shuffles.
+// Both kernels that quantize (the search's residual pass and the final
+// quantize + pack) give a lane 16 consecutive channels of two consecutive
+// rows: a group of 128 channels is 8 lanes, of 64 is 4, reduced with
+// shuffles, and the per-group step, fp16 scale and reciprocal are paid once
+// per 16 weights.  Rounding avoids the float-to-int conversion unit (see
+// rne_small).
 #include <algorithm>
 
 #include "awq_internal.h"
@@ -24,88 +28,10 @@ namespace awq {
 namespace {
 
 constexpr int kQuantThreads = 256;
+constexpr int kPerLane = 16;        // consecutive channels per lane
+constexpr int kRowsPerLane = 2;     // rows per lane
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-struct Quant8 {
-  uint32_t q[8];
-  __half scale;
-  int zero;
-};
-
-// Quantize the thread's 8 weights; every lane of the warp must call this
-// (shuffles), GLANES = group / 8 adjacent lanes form one group.
-template <int GLANES>
-__device__ __forceinline__ Quant8 quantize8(const uint4 wv, const float* __restrict__ s8,
-                                            const int levels) {
-  const float4 sa = __ldg(reinterpret_cast<const float4*>(s8));
-  const float4 sb = __ldg(reinterpret_cast<const float4*>(s8) + 1);
-  const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-  const uint32_t wv32[4] = {wv.x, wv.y, wv.z, wv.w};
-  float w[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2 h = *reinterpret_cast<const __half2*>(&wv32[i]);
-    w[2 * i] = __fmul_rn(__low2float(h), sv[2 * i]);
-    w[2 * i + 1] = __fmul_rn(__high2float(h), sv[2 * i + 1]);
-  }
-  float mn = w[0], mx = w[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    mn = fminf(mn, w[i]);
-    mx = fmaxf(mx, w[i]);
-  }
-#pragma unroll
-  for (int off = GLANES / 2; off; off >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  }
-  const float rng = __fsub_rn(mx, mn);
-  const float step = __fdiv_rn(fmaxf(rng, 1e-5f), static_cast<float>(levels));
-  Quant8 r;
-  r.scale = __float2half_rn(step);
-  const float rcp = __frcp_rn(__half2float(r.scale));
-  int z = __float2int_rn(__fmul_rn(-mn, rcp));
-  z = min(max(z, 0), levels);
-  r.zero = z;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    int q = __float2int_rn(__fmul_rn(w[i], rcp));
-    q = min(max(q, -levels), levels) + z;
-    r.q[i] = static_cast<uint32_t>(min(max(q, 0), levels));
-  }
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack4(const Quant8& r) {
-  uint32_t word = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) word |= r.q[i] << (4 * i);
-  return word;
-}
-
-__device__ __forceinline__ uint32_t pack3_bits24(const Quant8& r) {
-  uint32_t bits = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) bits |= r.q[i] << (3 * i);
-  return bits;
-}
-
-// Round half to even without the conversion unit: adding and removing
-// 1.5 * 2^23 leaves rne(t) for |t| <= 2^22 (the sum's ulp is 1, and the
-// addition rounds half to even).  The map is monotone, so for larger |t| the
-// result keeps the side of [-2^22, 2^22] that t is on, which is all the
-// clamps below ever look at.
-__device__ __forceinline__ float rne_small(float t) {
-  return __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
-}
-
+// ---------------------------------------------------------------- helpers
 __device__ __forceinline__ void ld_v8f(const float* p, float* v) {
   uint32_t r[8];
   asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -116,16 +42,52 @@ __device__ __forceinline__ void ld_v8f(const float* p, float* v) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void ld_v8u(const void* p, uint4* v) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w), "=r"(v[1].x),
+                 "=r"(v[1].y), "=r"(v[1].z), "=r"(v[1].w)
+               : "l"(p));
+}
+
 __device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
 
+// 16 fp16 weights (two raw 16-byte chunks, or 32 bytes of memory) as fp32.
+__device__ __forceinline__ void raw_to_f32(const uint4* raw, float* w) {
+#pragma unroll
+  for (int v = 0; v < 2; ++v) {
+    const uint32_t u[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      w[8 * v + 2 * i] = f.x;
+      w[8 * v + 2 * i + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void load_w16(const __half* p, float* w) {
+  const uint4* wp = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int v = 0; v < 2; ++v) {
+    const uint4 q = __ldg(wp + v);
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      w[8 * v + 2 * i] = f.x;
+      w[8 * v + 2 * i + 1] = f.y;
+    }
+  }
+}
+
 // Packed fp32 pairs (sm_100 f32x2 arithmetic, both lanes rounded to nearest
 // even).  ptxas fuses a packed multiply into a following packed add even with
-// .rn, so packed ops are used here only where no add consumes a product:
-// every "product, then add" of the quantizer stays in scalar intrinsics.
+// .rn, so a packed add never consumes a product directly: in the quantizer
+// the rounding add consumes a clamped value (a min / max sits between).
 typedef unsigned long long f32x2;
 __device__ __forceinline__ f32x2 pack2(float a, float b) {
   return static_cast<f32x2>(__float_as_uint(a)) | (static_cast<f32x2>(__float_as_uint(b)) << 32);
@@ -137,6 +99,11 @@ __device__ __forceinline__ float hi2(f32x2 v) {
 __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
   f32x2 d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
@@ -156,174 +123,363 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
+// Round half to even without the conversion unit: adding and removing
+// 1.5 * 2^23 leaves rne(t) for |t| <= 2^22 (the sum's ulp is 1, and the
+// addition rounds half to even).  The map is monotone, so for larger |t| the
+// result keeps the side of [-2^22, 2^22] that t is on, which is all the
+// clamps below ever look at.
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+__device__ __forceinline__ float rne_small(float t) {
+  return __fsub_rn(__fadd_rn(t, kMagic), kMagic);
+}
+
+// Per-group parameters of the quantizer, from the lane's 16 scaled weights
+// w' = w * s (every lane of the warp calls this; GLANES adjacent lanes form
+// one group).
+//
+// Only one side of the code clamp can ever act (rne is odd-symmetric and
+// fl(x * rcp) is monotone in x): with zu = rne(-min * rcp) <= L, every code
+// rne(w' * rcp) + z is >= 0 and only the upper bound L can be exceeded; with
+// zu > L (z clamped to L, every w' < 0) every code is <= L and only 0 can be
+// undershot.  `low` marks that second case.
+struct GroupQ {
+  float sf;    // float(fp16 scale)
+  float rcp;   // fp32 1 / sf
+  float z;     // zero point (an integer in [0, L])
+  bool low;    // the clamp that can act is the one at 0 (else the one at L)
+  __half scale;
+};
+
+template <int GLANES>
+__device__ __forceinline__ GroupQ group_params(const float* ws, float L) {
+  float mnA = fminf(ws[0], ws[1]), mxA = fmaxf(ws[0], ws[1]);
+  float mnB = fminf(ws[2], ws[3]), mxB = fmaxf(ws[2], ws[3]);
+#pragma unroll
+  for (int i = 4; i < kPerLane; i += 4) {
+    mnA = min3f(mnA, ws[i], ws[i + 1]);
+    mxA = max3f(mxA, ws[i], ws[i + 1]);
+    mnB = min3f(mnB, ws[i + 2], ws[i + 3]);
+    mxB = max3f(mxB, ws[i + 2], ws[i + 3]);
+  }
+  float mn = fminf(mnA, mnB), mx = fmaxf(mxA, mxB);
+#pragma unroll
+  for (int off = GLANES / 2; off; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  }
+  GroupQ g;
+  const float step = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-5f), L);
+  g.scale = __float2half_rn(step);
+  g.sf = __half2float(g.scale);
+  g.rcp = __frcp_rn(g.sf);
+  const float zu = rne_small(__fmul_rn(-mn, g.rcp));
+  g.low = zu > L;
+  g.z = fminf(fmaxf(zu, 0.0f), L);
+  return g;
+}
+
+// The same for the lane's two rows at once: the two rows' reductions,
+// shuffles and per-group arithmetic are interleaved (independent chains).
+template <int GLANES>
+__device__ __forceinline__ void group_params2(const float (&ws)[kRowsPerLane][kPerLane], float L,
+                                              GroupQ (&g)[kRowsPerLane]) {
+  float mn[kRowsPerLane], mx[kRowsPerLane];
+#pragma unroll
+  for (int r = 0; r < kRowsPerLane; ++r) {
+    float mnA = fminf(ws[r][0], ws[r][1]), mxA = fmaxf(ws[r][0], ws[r][1]);
+    float mnB = fminf(ws[r][2], ws[r][3]), mxB = fmaxf(ws[r][2], ws[r][3]);
+#pragma unroll
+    for (int i = 4; i < kPerLane; i += 4) {
+      mnA = min3f(mnA, ws[r][i], ws[r][i + 1]);
+      mxA = max3f(mxA, ws[r][i], ws[r][i + 1]);
+      mnB = min3f(mnB, ws[r][i + 2], ws[r][i + 3]);
+      mxB = max3f(mxB, ws[r][i + 2], ws[r][i + 3]);
+    }
+    mn[r] = fminf(mnA, mnB);
+    mx[r] = fmaxf(mxA, mxB);
+  }
+#pragma unroll
+  for (int off = GLANES / 2; off; off >>= 1) {
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      mn[r] = fminf(mn[r], __shfl_xor_sync(0xFFFFFFFFu, mn[r], off));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], off));
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerLane; ++r) {
+    const float step = __fdiv_rn(fmaxf(__fsub_rn(mx[r], mn[r]), 1e-5f), L);
+    g[r].scale = __float2half_rn(step);
+    g[r].sf = __half2float(g[r].scale);
+    g[r].rcp = __frcp_rn(g[r].sf);
+    const float zu = rne_small(__fmul_rn(-mn[r], g[r].rcp));
+    g[r].low = zu > L;
+    g[r].z = fminf(fmaxf(zu, 0.0f), L);
+  }
+}
+
+// ws[i] = w[i] * s[i], correctly rounded (packed multiplies; no add follows).
+__device__ __forceinline__ void scale16(const float* w, const float* s, float* ws) {
+#pragma unroll
+  for (int i = 0; i < kPerLane; i += 2) {
+    const f32x2 p = mul2(pack2(w[i], w[i + 1]), pack2(s[i], s[i + 1]));
+    ws[i] = lo2(p);
+    ws[i + 1] = hi2(p);
+  }
+}
+
+// Launch geometry shared by both kernels, without integer division:
+// blockIdx.x is a chunk of 32 lanes x kPerLane channels, and the 8 warps of a
+// block take 16 consecutive rows (two per warp) at those channels, so their
+// loads of s share L1 lines; blockIdx.y walks 16-row blocks (grid-stride).
+// Blocks are issued x-fastest, so consecutive blocks cover whole 16-row slabs
+// of W.  Lanes past the end of a row form whole groups (K % GROUP == 0), so
+// their dummy values (they re-read the row's last chunk) never meet real
+// ones in a reduction.
+constexpr int kRowsPerBlock = (kQuantThreads / 32) * kRowsPerLane;
+
+struct Lane {
+  int64_t lc;      // lane chunk along the row (kPerLane channels each)
+  int64_t k0;      // first channel (clamped for lanes past the row's end)
+  bool active;     // lc is inside the row
+};
+
+__device__ __forceinline__ Lane lane_chunk(int64_t K) {
+  const int64_t lanes_per_row = K / kPerLane;
+  Lane l;
+  l.lc = static_cast<int64_t>(blockIdx.x) * 32 + (threadIdx.x & 31);
+  l.active = l.lc < lanes_per_row;
+  l.k0 = (l.active ? l.lc : lanes_per_row - 1) * kPerLane;
+  return l;
+}
+
+// ---------------------------------------------------------------- residual
 // Search output: the quantization residual of every grid point, in the units
 // of W,
 //   delta[a][row_off + n][k] = fp16( w - ((q - z) * scale) / s_k ),
 // i.e. W - deq(Q(W diag(s))) diag(s)^-1 row by row.  The codes and zero
-// points are those of quantize8 (same fp32 steps, same rounding); only the
-// rounding itself uses rne_small instead of a float-to-int conversion, with
-// the clamp applied to (q - z) directly:
-//   q - z = clamp(rne(w' * rcp), -z, L - z).
+// points are those of the final quantizer (same steps, same rounding), with
+// the clamp applied to (q - z) directly:  q - z = clamp(rne(w' * rcp), -z, L - z).
 // (q - z) * scale is exact in fp32 (a 4-bit integer times an 11-bit
 // significand); w - that * (1/s_k) is one fused multiply-add, and the one
 // coarse rounding is the final one to fp16, relative to the residual.
 //
-// Work split: a lane owns 16 consecutive channels of two consecutive rows (a
-// group of 128 is 8 lanes, of 64 is 4), loads s and 1/s of a grid point once
-// for both rows, and evaluates every grid point, so W is read and converted
-// to fp32 once.  A warp covers 512 channels of its row pair; the 8 warps of a
-// block take 16 consecutive rows at the same channels, so their 256-bit loads
-// of s and 1/s hit the same L1 lines.  Warps are numbered row panel (64
-// rows), channel chunk, row pair.  Each lane writes one whole 32-byte sector
-// per row and grid point.
-constexpr int kResPanel = 64;
-constexpr int kResPerLane = 16;
-constexpr int kResRowsPerLane = 2;
-
+// A lane loads s and 1/s of a grid point once for its two rows and evaluates
+// every grid point, so W is read and converted to fp32 once.  The 8 warps of
+// a block take 16 consecutive rows at the same channels, so their 256-bit
+// loads of s and 1/s hit the same L1 lines.  Each lane writes one whole
+// 32-byte sector per row and grid point.
 template <int GROUP>
 __global__ void __launch_bounds__(kQuantThreads)
     k_quant_residual(const __half* __restrict__ W, int64_t N, int64_t K, int levels,
                      const float* __restrict__ s_grid, const float* __restrict__ r_grid,
                      int n_alpha, int64_t row_off, int64_t n_pad, __half* __restrict__ delta) {
-  constexpr int EPL = kResPerLane, RPT = kResRowsPerLane;
-  constexpr int GLANES = GROUP / EPL;
-  constexpr int SUBS = kResPanel / RPT;
-  const int64_t lanes_per_row = K / EPL;
-  const int64_t kw = (lanes_per_row + 31) / 32;      // warp chunks per row
-  const int64_t panels = (N + kResPanel - 1) / kResPanel;
-  const int64_t total_warps = panels * SUBS * kw;
-  const int lane = threadIdx.x & 31;
+  constexpr int GLANES = GROUP / kPerLane;
   const float L = static_cast<float>(levels);
   const int64_t slab = n_pad * K;                     // halves per grid point
-  for (int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       gw < total_warps; gw += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
-    const int64_t pn = gw / (SUBS * kw);
-    const int64_t rem = gw - pn * (SUBS * kw);
-    const int64_t j = rem / SUBS;
-    const int64_t row0 = pn * kResPanel + (rem - j * SUBS) * RPT;
-    if (row0 >= N) continue;                          // whole warp: no shuffle mixes rows
-    // Lanes past the end of the row form whole groups (K % GROUP == 0), so
-    // their dummy values never meet real ones in a reduction.
-    const int64_t lc = j * 32 + lane;
-    const bool active = lc < lanes_per_row;
-    const int64_t k0 = (active ? lc : lanes_per_row - 1) * EPL;
-    float w[RPT][EPL];
+  const Lane lw = lane_chunk(K);
+  for (int64_t row0 = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + (threadIdx.x >> 5)) *
+                      kRowsPerLane;
+       row0 < N; row0 += static_cast<int64_t>(gridDim.y) * kRowsPerBlock) {
+    float w[kRowsPerLane][kPerLane];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-      const int64_t row = min(row0 + r, N - 1);       // a lone last row loads itself twice
-      const uint4* wp = reinterpret_cast<const uint4*>(W + row * K + k0);
-#pragma unroll
-      for (int v = 0; v < EPL / 8; ++v) {
-        const uint4 q = __ldg(wp + v);
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
-          w[r][8 * v + 2 * i] = f.x;
-          w[r][8 * v + 2 * i + 1] = f.y;
-        }
-      }
-    }
+    for (int r = 0; r < kRowsPerLane; ++r)   // a lone last row loads itself twice
+      load_w16(W + min(row0 + r, N - 1) * K + lw.k0, w[r]);
 #pragma unroll 1
     for (int a = 0; a < n_alpha; ++a) {
-      float sv[EPL], rv[EPL];
-      const float* sp = s_grid + static_cast<int64_t>(a) * K + k0;
-      const float* rp = r_grid + static_cast<int64_t>(a) * K + k0;
+      float sv[kPerLane], rv[kPerLane];
+      const float* sp = s_grid + static_cast<int64_t>(a) * K + lw.k0;
+      const float* rp = r_grid + static_cast<int64_t>(a) * K + lw.k0;
+      ld_v8f(sp, sv);
+      ld_v8f(sp + 8, sv + 8);
+      ld_v8f(rp, rv);
+      ld_v8f(rp + 8, rv + 8);
+      float ws[kRowsPerLane][kPerLane];
 #pragma unroll
-      for (int v = 0; v < EPL / 8; ++v) {
-        ld_v8f(sp + 8 * v, sv + 8 * v);
-        ld_v8f(rp + 8 * v, rv + 8 * v);
-      }
+      for (int r = 0; r < kRowsPerLane; ++r) scale16(w[r], sv, ws[r]);
+      GroupQ gq[kRowsPerLane];
+      group_params2<GLANES>(ws, L, gq);
+      // rare: some group of the warp is all negative (both clamp sides needed)
+      const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
 #pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        float ws[EPL];
+      for (int r = 0; r < kRowsPerLane; ++r) {
+        const GroupQ& g = gq[r];
+        const float lo = -g.z, hi = L - g.z;
+        const f32x2 nsf = pack2(-g.sf, -g.sf);
+        // d = clamp(rne(w' * rcp), -z, L - z): the bounds are integers, so
+        // the clamp may come before the rounding adds.
+        const f32x2 rcp2 = pack2(g.rcp, g.rcp);
+        const f32x2 magic2 = pack2(kMagic, kMagic), nmagic2 = pack2(-kMagic, -kMagic);
+        float d[kPerLane];
 #pragma unroll
-        for (int i = 0; i < EPL; i += 2) {
-          const f32x2 p = mul2(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
-          ws[i] = lo2(p);
-          ws[i + 1] = hi2(p);
+        for (int i = 0; i < kPerLane; i += 2) {
+          const f32x2 t = mul2(pack2(ws[r][i], ws[r][i + 1]), rcp2);
+          float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
+          if (low) {
+            t0 = fmaxf(t0, lo);
+            t1 = fmaxf(t1, lo);
+          }
+          const f32x2 m = add2(add2(pack2(t0, t1), magic2), nmagic2);
+          d[i] = lo2(m);
+          d[i + 1] = hi2(m);
         }
-        float mnA = fminf(ws[0], ws[1]), mxA = fmaxf(ws[0], ws[1]);
-        float mnB = fminf(ws[2], ws[3]), mxB = fmaxf(ws[2], ws[3]);
+        uint32_t o[kPerLane / 2];
 #pragma unroll
-        for (int i = 4; i < EPL; i += 4) {
-          mnA = min3f(mnA, ws[i], ws[i + 1]);
-          mxA = max3f(mxA, ws[i], ws[i + 1]);
-          mnB = min3f(mnB, ws[i + 2], ws[i + 3]);
-          mxB = max3f(mxB, ws[i + 2], ws[i + 3]);
-        }
-        float mn = fminf(mnA, mnB), mx = fmaxf(mxA, mxB);
-#pragma unroll
-        for (int off = GLANES / 2; off; off >>= 1) {
-          mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        }
-        const float step = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-5f), L);
-        const float sf = __half2float(__float2half_rn(step));
-        const float rcp = __frcp_rn(sf);
-        const float z = fminf(fmaxf(rne_small(__fmul_rn(-mn, rcp)), 0.0f), L);
-        const float lo = -z, hi = L - z;
-        const f32x2 nsf = pack2(-sf, -sf);
-        uint32_t o[EPL / 2];
-#pragma unroll
-        for (int i = 0; i < EPL; i += 2) {
-          const float d0 = fminf(fmaxf(rne_small(__fmul_rn(ws[i], rcp)), lo), hi);
-          const float d1 = fminf(fmaxf(rne_small(__fmul_rn(ws[i + 1], rcp)), lo), hi);
+        for (int i = 0; i < kPerLane; i += 2) {
           // w - (d * sf) * (1/s): the product d * sf is exact.
-          const f32x2 e = fma2(mul2(pack2(d0, d1), nsf), pack2(rv[i], rv[i + 1]),
+          const f32x2 e = fma2(mul2(pack2(d[i], d[i + 1]), nsf), pack2(rv[i], rv[i + 1]),
                                pack2(w[r][i], w[r][i + 1]));
           const __half2 hv = __floats2half2_rn(lo2(e), hi2(e));
           o[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
         }
         const int64_t row = row0 + r;
-        if (active && row < N) st_v8(delta + a * slab + (row_off + row) * K + k0, o);
+        if (lw.active && row < N) st_v8(delta + a * slab + (row_off + row) * K + lw.k0, o);
       }
     }
   }
 }
 
+// ---------------------------------------------------------------- final
 // Result layout: INT4 codes [N][K/8] (code 8j+m in nibble m of word j);
 // INT3 codes [N][3K/32] (bit stream, code k in bits [3k, 3k+3));
 // scales fp16 [N][K/group]; zeros u8 [N][K/group].
-template <int BITS, int GROUP>
+//
+// The code is taken in the rounding constant's binade: m = rn(w' * rcp) +
+// 1.5 * 2^23 is clamped to [M - z, M + L - z], and the integer code is the
+// difference of the bit patterns of m and M - z (consecutive integers in
+// [2^23, 2^24) have consecutive patterns).  codes8: the code words are
+// 8-byte aligned (INT4 only), so a lane stores its two words at once.
+template <int BITS, int GROUP, bool A32>
 __global__ void __launch_bounds__(kQuantThreads)
-    k_quant_final(const uint4* __restrict__ W, int64_t N, int64_t K, const float* __restrict__ s_base,
-                  const int* __restrict__ sel, uint32_t* __restrict__ codes,
-                  __half* __restrict__ scales, uint8_t* __restrict__ zeros) {
-  constexpr int GLANES = GROUP / 8;
+    k_quant_final(const __half* __restrict__ W, int64_t N, int64_t K,
+                  const float* __restrict__ s_base, const int* __restrict__ sel,
+                  uint32_t* __restrict__ codes, __half* __restrict__ scales,
+                  uint8_t* __restrict__ zeros, bool codes8) {
+  constexpr int GLANES = GROUP / kPerLane;
   constexpr int LEVELS = (1 << BITS) - 1;
-  const int64_t kc = K / 8;
-  const int64_t total = N * kc;
+  const float L = static_cast<float>(LEVELS);
   const int64_t groups = K / GROUP;
+  const int64_t words = BITS == 4 ? K / 8 : 3 * K / 32;
   const float* s = s_base + (sel ? static_cast<int64_t>(*sel) * K : 0);
   const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-       base < total; base += stride) {
-    const int64_t item = base + lane;
-    const bool active = item < total;
-    const int64_t it = active ? item : 0;
-    const int64_t row = it / kc;
-    const int64_t c = it - row * kc;
-    const uint4 wv = active ? ldg_stream(W + it) : make_uint4(0, 0, 0, 0);
-    const Quant8 r = quantize8<GLANES>(wv, s + c * 8, LEVELS);
-    if (BITS == 4) {
-      if (active) codes[it] = pack4(r);
-    } else {
-      // Four threads hold 4 x 24 bits = 3 words; thread j of the quad writes
-      // word j from its own bits and those of thread j+1.
-      const uint32_t own = pack3_bits24(r);
-      const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, own, 1);
-      const int j = static_cast<int>(c & 3);
-      if (active && j < 3) {
-        const uint32_t word = (own >> (8 * j)) | (next << (24 - 8 * j));
-        codes[row * (3 * K / 32) + (c >> 2) * 3 + j] = word;
+  const Lane lw = lane_chunk(K);
+  for (int64_t row0 = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + (threadIdx.x >> 5)) *
+                      kRowsPerLane;
+       row0 < N; row0 += static_cast<int64_t>(gridDim.y) * kRowsPerBlock) {
+    // Both rows' weights, then s: with A32 (W and s 32-byte aligned) one
+    // 256-bit load per 32 bytes, so a warp's request covers whole lines.
+    uint4 raw[kRowsPerLane][2];
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {   // a lone last row loads itself twice
+      const __half* src = W + min(row0 + r, N - 1) * K + lw.k0;
+      if (A32) {
+        ld_v8u(src, raw[r]);
+      } else {
+        raw[r][0] = __ldg(reinterpret_cast<const uint4*>(src));
+        raw[r][1] = __ldg(reinterpret_cast<const uint4*>(src) + 1);
       }
     }
-    if (active && (lane % GLANES) == 0) {
-      const int64_t g = (c * 8) / GROUP;
-      scales[row * groups + g] = r.scale;
-      zeros[row * groups + g] = static_cast<uint8_t>(r.zero);
+    float sv[kPerLane];
+    if (A32) {
+      ld_v8f(s + lw.k0, sv);
+      ld_v8f(s + lw.k0 + 8, sv + 8);
+    } else {
+#pragma unroll
+      for (int v = 0; v < kPerLane / 4; ++v) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(s + lw.k0) + v);
+        sv[4 * v] = f.x;
+        sv[4 * v + 1] = f.y;
+        sv[4 * v + 2] = f.z;
+        sv[4 * v + 3] = f.w;
+      }
+    }
+    float ws[kRowsPerLane][kPerLane];
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      float w[kPerLane];
+      raw_to_f32(raw[r], w);
+      scale16(w, sv, ws[r]);
+    }
+    GroupQ gq[kRowsPerLane];
+    group_params2<GLANES>(ws, L, gq);
+    // rare: some group of the warp is all negative (both clamp sides needed)
+    const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      const int64_t row = row0 + r;
+      const GroupQ& g = gq[r];
+      const uint32_t base = __float_as_uint(__fsub_rn(kMagic, g.z));   // bits of M - z
+      // b[i] = bit pattern of M + clamp(rne(w' * rcp), -z, L - z); code = b[i] - base.
+      // The bounds are integers, so clamping before the rounding add is the
+      // same as clamping after it.
+      const float lo = -g.z, hi = L - g.z;
+      const f32x2 rcp2 = pack2(g.rcp, g.rcp), magic2 = pack2(kMagic, kMagic);
+      uint32_t b[kPerLane];
+#pragma unroll
+      for (int i = 0; i < kPerLane; i += 2) {
+        const f32x2 t = mul2(pack2(ws[r][i], ws[r][i + 1]), rcp2);
+        float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
+        if (low) {
+          t0 = fmaxf(t0, lo);
+          t1 = fmaxf(t1, lo);
+        }
+        const f32x2 m = add2(pack2(t0, t1), magic2);
+        b[i] = static_cast<uint32_t>(m);
+        b[i + 1] = static_cast<uint32_t>(m >> 32);
+      }
+      const bool store = lw.active && row < N;
+      uint32_t* crow = codes + row * words;
+      // Packing by multiply-add on the FMA pipe: sum_i code_i * 2^(bits*i) =
+      // sum_i b_i * 2^(bits*i) - base * sum_i 2^(bits*i) (mod 2^32), exact
+      // because the true packed value fits in 32 bits.
+      if (BITS == 4) {
+        uint32_t c0 = b[7], c1 = b[15];
+#pragma unroll
+        for (int i = 6; i >= 0; --i) {
+          c0 = c0 * 16u + b[i];
+          c1 = c1 * 16u + b[8 + i];
+        }
+        c0 -= base * 0x11111111u;
+        c1 -= base * 0x11111111u;
+        if (store) {
+          uint32_t* dst = crow + 2 * lw.lc;
+          if (codes8) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(c0, c1);
+          } else {
+            dst[0] = c0;
+            dst[1] = c1;
+          }
+        }
+      } else {
+        // 16 codes = 48 bits: codes 0..10 in lo32 (code 10 keeps its low 2
+        // bits there), code 10's top bit and codes 11..15 in hi16.  An
+        // even/odd lane pair holds 96 bits = 3 words (K % 32 == 0, so pairs
+        // are never split by the row's end).
+        uint32_t lo32 = b[10];
+#pragma unroll
+        for (int i = 9; i >= 0; --i) lo32 = lo32 * 8u + b[i];
+        lo32 -= base * 0x49249249u;                     // sum_{i<=10} 8^i mod 2^32
+        uint32_t hi16 = b[15];
+#pragma unroll
+        for (int i = 14; i >= 11; --i) hi16 = hi16 * 8u + b[i];
+        hi16 = (hi16 - base * 0x00001249u) * 2u + ((b[10] - base) >> 2);
+        const uint32_t next_lo = __shfl_down_sync(0xFFFFFFFFu, lo32, 1);
+        if (store) {
+          uint32_t* dst = crow + (lw.lc >> 1) * 3;
+          if ((lane & 1) == 0) {
+            dst[0] = lo32;
+            dst[1] = hi16 | (next_lo << 16);
+          } else {
+            // this lane's bits 16..47: the pair's word 2
+            dst[2] = (lo32 >> 16) | (hi16 << 16);
+          }
+        }
+      }
+      if (store && (lane % GLANES) == 0) {
+        const int64_t gi = row * groups + lw.k0 / GROUP;
+        scales[gi] = g.scale;
+        zeros[gi] = static_cast<uint8_t>(__float2uint_rn(g.z));
+      }
     }
   }
 }
@@ -346,9 +502,26 @@ __global__ void k_unpack(const uint32_t* __restrict__ codes, int64_t N, int64_t 
   }
 }
 
-unsigned grid_for(int64_t items) {
-  const int64_t blocks = ceil_div(items, kQuantThreads);
-  return static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(blocks, 148 * 16)));
+dim3 quant_grid(int64_t N, int64_t K) {
+  const int64_t gx = ceil_div(K / kPerLane, 32);
+  const int64_t gy = std::min<int64_t>(ceil_div(N, kRowsPerBlock), 65535);
+  return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(std::max<int64_t>(gy, 1)));
+}
+
+template <int BITS, int GROUP>
+cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, const int* sel,
+                         uint32_t* codes, __half* scales, uint8_t* zeros, cudaStream_t st) {
+  const bool c8 = (reinterpret_cast<uintptr_t>(codes) % 8) == 0;
+  const bool a32 = (reinterpret_cast<uintptr_t>(W) % 32) == 0 &&
+                   (reinterpret_cast<uintptr_t>(s) % 32) == 0;
+  const dim3 grid = quant_grid(N, K);
+  if (a32)
+    k_quant_final<BITS, GROUP, true><<<grid, kQuantThreads, 0, st>>>(W, N, K, s, sel, codes,
+                                                                     scales, zeros, c8);
+  else
+    k_quant_final<BITS, GROUP, false><<<grid, kQuantThreads, 0, st>>>(W, N, K, s, sel, codes,
+                                                                      scales, zeros, c8);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -358,10 +531,7 @@ cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bit
                                   int64_t row_off, int64_t n_pad, __half* delta,
                                   cudaStream_t st) {
   const int levels = (1 << bits) - 1;
-  const int64_t warps = ceil_div(N, kResPanel) * (kResPanel / kResRowsPerLane) *
-                        ceil_div(K / kResPerLane, 32);
-  const int64_t blocks = ceil_div(warps * 32, kQuantThreads);
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(blocks, int64_t(1) << 30));
+  const dim3 grid = quant_grid(N, K);
   if (group == 128)
     k_quant_residual<128><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
                                                           n_alpha, row_off, n_pad, delta);
@@ -374,22 +544,20 @@ cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bit
 cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, int group,
                                const float* s, const int* sel, uint32_t* codes,
                                __half* scales, uint8_t* zeros, cudaStream_t st) {
-  const unsigned grid = grid_for(N * (K / 8));
-  const uint4* w = reinterpret_cast<const uint4*>(W);
   if (bits == 4 && group == 128)
-    k_quant_final<4, 128><<<grid, kQuantThreads, 0, st>>>(w, N, K, s, sel, codes, scales, zeros);
-  else if (bits == 4 && group == 64)
-    k_quant_final<4, 64><<<grid, kQuantThreads, 0, st>>>(w, N, K, s, sel, codes, scales, zeros);
-  else if (bits == 3 && group == 128)
-    k_quant_final<3, 128><<<grid, kQuantThreads, 0, st>>>(w, N, K, s, sel, codes, scales, zeros);
-  else
-    k_quant_final<3, 64><<<grid, kQuantThreads, 0, st>>>(w, N, K, s, sel, codes, scales, zeros);
-  return cudaGetLastError();
+    return launch_final<4, 128>(W, N, K, s, sel, codes, scales, zeros, st);
+  if (bits == 4 && group == 64)
+    return launch_final<4, 64>(W, N, K, s, sel, codes, scales, zeros, st);
+  if (bits == 3 && group == 128)
+    return launch_final<3, 128>(W, N, K, s, sel, codes, scales, zeros, st);
+  return launch_final<3, 64>(W, N, K, s, sel, codes, scales, zeros, st);
 }
 
 cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                           cudaStream_t st) {
-  k_unpack<<<grid_for(N * K), kQuantThreads, 0, st>>>(codes, N, K, bits, q);
+  const int64_t blocks = ceil_div(N * K, kQuantThreads);
+  k_unpack<<<static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(blocks, 148 * 16))),
+             kQuantThreads, 0, st>>>(codes, N, K, bits, q);
   return cudaGetLastError();
 }
 

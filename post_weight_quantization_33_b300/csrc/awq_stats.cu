@@ -11,6 +11,7 @@
 // single correctly rounded fp64 division.
 #include <algorithm>
 
+#include "awq_async.cuh"
 #include "awq_internal.h"
 
 namespace awq {
@@ -18,71 +19,114 @@ namespace {
 
 constexpr int kStatsThreads = 256;   // 8 warps; a warp covers 256 channels
 
-// |h| of an fp16 bit pattern, in units of 2^-24, exactly.
-__device__ __forceinline__ unsigned long long abs_half_units(uint32_t h) {
-  const uint32_t b = h & 0x7FFFu;
-  const uint32_t e = b >> 10;
-  const uint32_t m = b & 0x3FFu;
-  const uint32_t mant = e ? (m | 0x400u) : m;
-  const uint32_t sh = e ? e - 1u : 0u;
-  return static_cast<unsigned long long>(mant) << sh;
+// Exact sums on the FMA pipe.  For an fp16 value x, u = |x| * 2^24 is an
+// integer below 2^40.  One fma against C = 1.5 * 2^43 rounds u to a multiple
+// of 2^20 (the ulp of [2^43, 2^44)); the two parts
+//   hi = (round(u) - C) / 2^20   (an integer <= 2^20)
+//   lo = u - round(u)            (an integer, |lo| <= 2^19)
+// are exact in fp32, and so are their sums over 16 tokens (|hi sum| <= 2^24,
+// |lo sum| <= 2^23).  Every 16 tokens the two fp32 sums are converted to
+// integers and added to 64-bit totals: the result is the exact integer sum,
+// independent of order.
+constexpr float kSplitC = 13194139533312.0f;   // 1.5 * 2^43
+constexpr int kFlushTokens = 16;
+constexpr int kStatStages = 4;                                   // steps of 4 tokens
+constexpr int kStatSmem = (kStatsThreads / 32) * kStatStages * 4 * 32 * 16;   // 64 KB
+static_assert(kStatSmem >= 8 * 8 * 33 * 8, "the ring also holds the cross-warp sums");
+
+__device__ __forceinline__ void add_half_exact(float v, float& hi, float& lo) {
+  const float r = __fmaf_rn(v, 16777216.0f, kSplitC);        // round(u) + C
+  const float fh = __fsub_rn(r, kSplitC);                     // round(u)
+  lo = __fadd_rn(lo, __fmaf_rn(v, 16777216.0f, -fh));         // u - round(u), exact
+  hi = __fmaf_rn(fh, 0x1p-20f, hi);                           // round(u) / 2^20, exact
 }
 
-__device__ __forceinline__ void add_chunk(unsigned long long (&acc)[8], const uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ void add_chunk(float (&hi)[8], float (&lo)[8], const uint4 v) {
+  const uint32_t w[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu,
+                         v.w & 0x7FFF7FFFu};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    acc[2 * i] += abs_half_units(w[i] & 0xFFFFu);
-    acc[2 * i + 1] += abs_half_units(w[i] >> 16);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    add_half_exact(f.x, hi[2 * i], lo[2 * i]);
+    add_half_exact(f.y, hi[2 * i + 1], lo[2 * i + 1]);
   }
-}
-
-__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
 }
 
 // Block (x, y): channel chunks [32*x, 32*x + 32) (8 channels each), tokens
-// [y*rows, (y+1)*rows).  Warp w walks tokens w, w+8, ...; the 8 warps are
-// then summed in shared memory and added to acc with one 64-bit atomic per
-// channel (integer addition: the result does not depend on the order).
+// [y*rows, (y+1)*rows).  Warp w walks tokens w, w+8, ... four at a time
+// (a step); every 16 of its tokens (and at the end) the fp32 part sums are
+// flushed to 64-bit totals.  Loads go through a per-warp ring of
+// kStatStages steps in shared memory filled with cp.async (token q of lane l
+// at [stage][q][l]: conflict-free; each lane reads back only its own
+// copies), so kStatStages - 1 steps of loads are in flight without holding
+// registers.  The 8 warps are then summed in shared memory and added to acc
+// with one 64-bit atomic per channel (integer addition: the result does not
+// depend on the order).
 __global__ void __launch_bounds__(kStatsThreads)
     k_stats_accumulate(const uint4* __restrict__ X, int64_t T, int64_t kchunks,
                        int64_t rows_per_block, unsigned long long* __restrict__ acc) {
-  __shared__ unsigned long long red[8][8][33];
+  extern __shared__ uint4 ring_smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t chunk = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const bool live = chunk < kchunks;
   const int64_t t0 = static_cast<int64_t>(blockIdx.y) * rows_per_block;
   const int64_t t1 = min(T, t0 + rows_per_block);
-  unsigned long long s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (chunk < kchunks) {
-    int64_t t = t0 + warp;
-    for (; t + 24 < t1; t += 32) {
-      const uint4 v0 = ldg_stream(X + t * kchunks + chunk);
-      const uint4 v1 = ldg_stream(X + (t + 8) * kchunks + chunk);
-      const uint4 v2 = ldg_stream(X + (t + 16) * kchunks + chunk);
-      const uint4 v3 = ldg_stream(X + (t + 24) * kchunks + chunk);
-      add_chunk(s, v0);
-      add_chunk(s, v1);
-      add_chunk(s, v2);
-      add_chunk(s, v3);
-    }
-    for (; t < t1; t += 8) add_chunk(s, ldg_stream(X + t * kchunks + chunk));
-  }
+  uint4* ring = ring_smem + warp * (kStatStages * 4 * 32);
+  const uint32_t ring_u32 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+  const int64_t steps = t1 > t0 + warp ? (t1 - t0 - warp + 31) / 32 : 0;
+  auto issue = [&](int64_t step) {
+    if (step < steps && live) {
+      const int st = static_cast<int>(step % kStatStages);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) red[warp][j][lane] = s[j];
+      for (int q = 0; q < 4; ++q) {
+        const int64_t t = t0 + warp + 32 * step + 8 * q;
+        const bool in = t < t1;
+        cp_async16(ring_u32 + ((st * 4 + q) * 32 + lane) * 16, in ? X + t * kchunks + chunk : X,
+                   in ? 16 : 0);
+      }
+    }
+    cp_async_commit();   // possibly empty: one group per step
+  };
+  long long tot[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float hi[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float lo[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kStatStages - 1; ++i) issue(i);
+  int since_flush = 0;
+  for (int64_t step = 0; step < steps; ++step) {
+    issue(step + kStatStages - 1);
+    cp_async_wait<kStatStages - 1>();
+    if (live) {
+      const int st = static_cast<int>(step % kStatStages);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) add_chunk(hi, lo, ring[(st * 4 + q) * 32 + lane]);
+    }
+    since_flush += 4;
+    if (since_flush == kFlushTokens || step + 1 == steps) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        tot[j] += (static_cast<long long>(__float2int_rn(hi[j])) << 20) +
+                  static_cast<long long>(__float2int_rn(lo[j]));
+        hi[j] = 0.f;
+        lo[j] = 0.f;
+      }
+      since_flush = 0;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();   // the ring is reused for the cross-warp sum
+  auto red = reinterpret_cast<unsigned long long(*)[8][33]>(ring_smem);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[warp][j][lane] = static_cast<unsigned long long>(tot[j]);
   __syncthreads();
-  if (warp == 0 && chunk < kchunks) {
+  if (warp == 0 && live) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      unsigned long long tot = 0;
+      unsigned long long sum = 0;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) tot += red[w][j][lane];
-      if (tot) atomicAdd(acc + chunk * 8 + j, tot);
+      for (int w = 0; w < 8; ++w) sum += red[w][j][lane];
+      if (sum) atomicAdd(acc + chunk * 8 + j, sum);
     }
   }
 }
@@ -165,16 +209,20 @@ cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
                                     unsigned long long* acc, cudaStream_t st) {
   const int64_t kchunks = K / 8;
   const int64_t gx = ceil_div(kchunks, 32);
-  // Enough row slices for ~8 blocks per SM (148 SMs), at least 32 rows each.
-  int64_t gy = ceil_div(148 * 8, gx);
+  // About three resident blocks per SM (148 SMs; 64 KB of ring each) in one
+  // wave; token slices a multiple of 32 rows (8 warps x 4 tokens per step).
+  int64_t gy = std::max<int64_t>(1, ceil_div(148 * 3, gx));
   int64_t rows = ceil_div(T, gy);
-  rows = std::max<int64_t>(32, ceil_div(rows, 8) * 8);
+  rows = std::max<int64_t>(32, ceil_div(rows, 32) * 32);
   gy = ceil_div(T, rows);
   cudaError_t e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long) * K, st);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_stats_accumulate, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kStatSmem);
+  if (e != cudaSuccess) return e;
   k_stats_accumulate<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
-                       kStatsThreads, 0, st>>>(reinterpret_cast<const uint4*>(X), T, kchunks,
-                                               rows, acc);
+                       kStatsThreads, kStatSmem, st>>>(reinterpret_cast<const uint4*>(X), T,
+                                                       kchunks, rows, acc);
   return cudaGetLastError();
 }
 
