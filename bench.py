@@ -460,7 +460,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["tflops"],
                      "unit": "TFLOP/s", "frac": achieved / pk["tflops"],
                      "traffic": profiled_traffic(),
-                     "kernel": "k_gemm<true> (tcgen05 error GEMM), fp16 operands, f32 accumulate",
+                     "kernel": "k_gemm_err_pair (tcgen05 cta_group::2 error GEMM), fp16 operands, f32 accumulate",
                      "peak_source": f"{pk['source']} bf16 burst (dense fp16 taken equal)",
                      "launch_ms": gemm_avg_ms},
         "step_roofline": {"ideal_ms": ideal_s * 1e3, "frac": ideal_s * 1e3 / (total_ms / args.steps)},

@@ -360,6 +360,8 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
     n_pad += ceil_div(Ws[i].N, kTileM) * kTileM;
     n_total += Ws[i].N;
   }
+  const int64_t n_used = n_pad;                 // rows of the last weight's tiles
+  n_pad = ceil_div(n_pad, kPairRows) * kPairRows;   // whole pair tiles for the error GEMM
   const int G = cfg->n_grid;
   const int64_t groups = K / cfg->group_size;
   const int64_t n_tiles = ceil_div(T, kTileN);
@@ -457,6 +459,11 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
                                sizeof(__half) * n_pad * K, 0, sizeof(__half) * pad_rows * K, G,
                                s),
              "residual padding reset");
+  }
+  if (n_pad > n_used) {
+    AWQ_CUDA(cudaMemset2DAsync(delta + n_used * K, sizeof(__half) * n_pad * K, 0,
+                               sizeof(__half) * (n_pad - n_used) * K, G, s),
+             "residual tail reset");
   }
   // Optional stage boundaries (awq_set_stage_timing): events on this stream.
   if (g_stage_timing.load()) {

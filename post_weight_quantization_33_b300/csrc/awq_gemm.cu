@@ -17,6 +17,7 @@
 //
 // The same kernel with a row-major fp32 store in the epilogue computes the
 // reference output Y = W X^T.
+#include <algorithm>
 #include <mutex>
 
 #include "awq_internal.h"
@@ -266,6 +267,253 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair error GEMM
+// The error GEMM proper.  A cluster of two CTAs (one per SM) owns a pair tile
+// of 256 residual rows x 256 tokens; the even CTA issues
+// tcgen05.mma.cta_group::2 (M 256, N 256, K 16), which reads A from both
+// CTAs' shared memories (128 rows each) and B likewise (128 tokens each) and
+// leaves each CTA's 128 rows x 256 tokens in its own TMEM.  Per SM and K step
+// of 64 this moves 32 KB from L2 into shared memory for 4.2 MFLOP (a single
+// CTA with M 128 needs 48 KB), and 6 stages fit instead of 4.
+//
+//   warp 4 (both CTAs)  TMA producer: own 128 residual rows and own 128
+//                       tokens of X into its stage; completion is counted on
+//                       the even CTA's `full` barrier;
+//   warp 5              TMEM owner in both CTAs (pair allocation of 512
+//                       columns: two 256-column accumulators); in the even CTA
+//                       lane 0 issues the MMAs and commits to `empty` (both
+//                       CTAs: their stages are free) and `tfull` (both CTAs:
+//                       the accumulator is ready);
+//   warps 0-3 (both)    epilogue as in k_gemm, then one arrival per thread on
+//                       the even CTA's `tempty` (256 arrivals free it).
+//
+// Teardown: each producer waits until every stage it filled was released
+// (so no MMA still reads its shared memory and no commit still targets its
+// barriers), then both CTAs meet at a cluster barrier before TMEM is freed and
+// either CTA exits.
+constexpr int PM = 128;                 // rows per CTA
+constexpr int PN = 256;                 // tokens per pair tile
+constexpr int PSTAGES = 6;
+constexpr uint32_t PA_BYTES = PM * BK * 2;        // 16 KB
+constexpr uint32_t PB_BYTES = (PN / 2) * BK * 2;  // 16 KB (this CTA's half of the tokens)
+constexpr uint32_t P_OFF_A = 0;
+constexpr uint32_t P_OFF_B = P_OFF_A + PSTAGES * PA_BYTES;
+constexpr uint32_t P_OFF_BAR = P_OFF_B + PSTAGES * PB_BYTES;
+constexpr uint32_t P_NUM_BARS = 2 * PSTAGES + 5;   // full, empty, tfull x2, tempty x2, drain
+constexpr uint32_t P_OFF_MISC = P_OFF_BAR + P_NUM_BARS * 8;
+constexpr uint32_t P_SMEM_BYTES = P_OFF_MISC + 16 + 1024;
+static_assert(P_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(P_OFF_B % 1024 == 0 && PA_BYTES % 1024 == 0 && PB_BYTES % 1024 == 0,
+              "swizzle atoms");
+constexpr uint32_t kIdescPair = idesc_f16_f32(2 * PM, PN);
+constexpr uint32_t kPairTmemCols = 512;
+
+struct PairArgs {
+  int num_mp;        // pair tiles along residual rows (256 rows each)
+  int num_n_tiles;   // token tiles (256 tokens each)
+  int num_alpha;     // grid points
+  int k_blocks;      // K / 64
+  int64_t n_pad;     // rows of the residual and partials layout (multiple of 256)
+  float* partials;   // [alpha][n_tiles][n_pad]
+  int* status;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_err_pair(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, const PairArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + P_OFF_BAR;
+  const uint32_t bar_empty = bar_full + 8 * PSTAGES;
+  const uint32_t bar_tfull = bar_empty + 8 * PSTAGES;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P_OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P_OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 2 * kEpilogueThreads);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), kPairTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers are initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = p.num_mp * p.num_n_tiles * p.num_alpha;
+  auto decode = [&](int tile, int& a, int& nt, int& mp) {
+    const int per_alpha = p.num_mp * p.num_n_tiles;
+    a = tile / per_alpha;
+    const int rem = tile - a * per_alpha;
+    nt = rem / p.num_mp;
+    mp = rem - nt * p.num_mp;
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total_tiles && ok; tile += num_pairs) {
+        int a, nt, mp;
+        decode(tile, a, nt, mp);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status,
+                                 kDevTimeoutEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = bar_full + 8 * stage;
+          if (leader) mbar_arrive_expect_tx(fb_local, 2 * (PA_BYTES + PB_BYTES));
+          const uint32_t fb = map_shared(fb_local, 0);
+          tma_load_3d_pair(sbase + P_OFF_A + stage * PA_BYTES, &tmap_a, fb, kb * BK,
+                           mp * 2 * PM + static_cast<int>(rank) * PM, a);
+          tma_load_2d_pair(sbase + P_OFF_B + stage * PB_BYTES, &tmap_b, fb, kb * BK,
+                           nt * PN + static_cast<int>(rank) * (PN / 2));
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Tail: wait until every stage this CTA filled has been released by the
+      // MMAs (a stage never filled passes at once).
+      for (int i = 0; i < PSTAGES; ++i) {
+        mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, nullptr, p.status, kDevTimeoutDrain,
+                          ok ? kWaitLimitNs : kDrainLimitNs);
+        if (++stage == PSTAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true, issued = false;
+      int it = 0;
+      for (int tile = pair; tile < total_tiles && ok; tile += num_pairs, ++it) {
+        const uint32_t acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status,
+                               kDevTimeoutTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * PN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status,
+                                 kDevTimeoutFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + P_OFF_A + stage * PA_BYTES;
+          const uint32_t b_addr = sbase + P_OFF_B + stage * PB_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            umma_f16_pair(d_tmem, smem_desc_sw128(a_addr + 32 * k),
+                          smem_desc_sw128(b_addr + 32 * k), kIdescPair, (kb | k) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit_pair(bar_empty + 8 * stage, 0x3);
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair(bar_tfull + 8 * acc, 0x3);
+      }
+      if (!ok && issued) {
+        // Wait for the MMAs in flight before TMEM or either CTA's stages go away.
+        umma_commit_pair(bar_drain, 0x1);
+        mbar_wait_bounded(bar_drain, 0, nullptr, p.status, kDevTimeoutDrain, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp;               // TMEM lane quarter (warps 0-3)
+    const int row = q * 32 + lane;    // row within this CTA's 128
+    const uint32_t tempty_leader = map_shared(bar_tempty, 0);
+    int it = 0;
+    for (int tile = pair; tile < total_tiles; tile += num_pairs, ++it) {
+      int a, nt, mp;
+      decode(tile, a, nt, mp);
+      const uint32_t acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      // tcgen05.ld is warp-collective: decide together and reconverge.
+      const bool ready = __all_sync(0xFFFFFFFFu,
+                                    mbar_wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag,
+                                                      p.status, kDevTimeoutTmemFull));
+      if (!ready) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PN;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < PN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float e0 = __uint_as_float(v[j]);
+          const float e1 = __uint_as_float(v[j + 1]);
+          sum0 = fmaf(e0, e0, sum0);
+          sum1 = fmaf(e1, e1, sum1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(tempty_leader + 8 * acc);
+      p.partials[(static_cast<int64_t>(a) * p.num_n_tiles + nt) * p.n_pad +
+                 static_cast<int64_t>(mp) * 2 * PM + static_cast<int64_t>(rank) * PM + row] =
+          sum0 + sum1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Error path only: give copies already issued time to land before the
+    // pair's shared memory is released.
+    const unsigned long long t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  cluster_sync();   // neither CTA leaves while the other may still touch it
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kPairTmemCols);
+  }
+}
+
 __global__ void k_wait_selftest(unsigned long long limit_ns, int* status) {
   __shared__ __align__(8) uint64_t bar_storage;
   const uint32_t bar = smem_u32(&bar_storage);
@@ -359,33 +607,55 @@ cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, i
 cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
                               int64_t n_pad, int n_alpha, float* partials, int* status,
                               cudaStream_t st) {
-  CUtensorMap ta, tb;
-  // A 3-D map even for one grid point keeps the kernel's coordinates uniform.
+  if (n_pad % (2 * PM) != 0) return cudaErrorInvalidValue;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
   {
+    // Residual [alpha][n_pad][K]: box 64 x 128 (this CTA's rows of a pair tile).
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(n_pad),
                                 static_cast<cuuint64_t>(n_alpha)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
                                    static_cast<cuuint64_t>(K) * 2 * static_cast<cuuint64_t>(n_pad)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BM), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(PM), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (fn(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(delta), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  if (!make_tmap_f16(&tb, X, 1, T, K, BN)) return cudaErrorInvalidValue;
-  GemmArgs a{};
-  a.num_m_tiles = static_cast<int>(n_pad / BM);
-  a.num_n_tiles = static_cast<int>(ceil_div(T, BN));
+  // X [T][K]: box 64 x 128 (this CTA's half of a 256-token tile; tokens past
+  // T read as zeros).
+  if (!make_tmap_f16(&tb, X, 1, T, K, PN / 2)) return cudaErrorInvalidValue;
+  PairArgs a{};
+  a.num_mp = static_cast<int>(n_pad / (2 * PM));
+  a.num_n_tiles = static_cast<int>(ceil_div(T, PN));
   a.num_alpha = n_alpha;
   a.k_blocks = static_cast<int>(K / BK);
-  a.T = T;
   a.n_pad = n_pad;
   a.partials = partials;
   a.status = status;
-  return launch<true>(ta, tb, a, st);
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_err_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(P_SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  // One pair per co-resident cluster slot (persistent), at most one per tile.
+  const int64_t tiles = static_cast<int64_t>(a.num_mp) * a.num_n_tiles * a.num_alpha;
+  int clusters = sm_count() / 2;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm_err_pair, &cfg) == cudaSuccess &&
+        max_clusters > 0)
+      clusters = std::min(clusters, max_clusters);
+    else
+      cudaGetLastError();
+  }
+  const int pairs = static_cast<int>(std::min<int64_t>(clusters, tiles));
+  k_gemm_err_pair<<<2 * pairs, kThreads, P_SMEM_BYTES, st>>>(ta, tb, a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st) {

@@ -24,10 +24,12 @@ enum DeviceError : int {
 constexpr int kMaxWeights = 16;
 constexpr int kMaxGrid = 64;
 
-// ---- error GEMM geometry (one CTA tile = 128 weight rows x 256 tokens)
+// ---- GEMM geometry (one CTA tile = 128 weight rows x 256 tokens; the error
+// GEMM runs on CTA pairs, so its row space is padded to 256-row pair tiles)
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kTileK = 64;
+constexpr int kPairRows = 2 * kTileM;
 
 // Map from the padded "virtual row" space used by the error GEMM (every
 // weight's rows start on a multiple of kTileM) to the compact row order of
@@ -75,7 +77,8 @@ cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits,
 cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, int64_t T,
                                   int64_t K, float* y, int* status, cudaStream_t st);
 // partials[a][n_tile][n_pad] = sum over the tile's tokens of (delta[a] X^T)^2
-// for every grid point a (delta: fp16 [n_alpha][n_pad][K]).
+// for every grid point a (delta: fp16 [n_alpha][n_pad][K], n_pad a multiple
+// of kPairRows).
 cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
                               int64_t n_pad, int n_alpha, float* partials, int* status,
                               cudaStream_t st);
