@@ -126,7 +126,9 @@ awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stre
 /* Scale vectors for every grid point ("AWQ explained": s = sX^alpha).
  *   sX : device fp64 [K], K >= 1.
  *   s  : device fp32 [n_grid][K], written; row i uses alpha = i / n_grid.
- * Allocates n_grid*K*8 bytes of stream-ordered scratch. */
+ * x^alpha is formed in fp64 from one log and one exp per channel (relative
+ * error below 2^-47 before the fp32 rounding).  Allocates 16 bytes of
+ * stream-ordered scratch. */
 awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s, void* stream);
 
 /* Scale, group-quantize and pack one weight ("AWQ Explained", multigrid.ai,

@@ -258,14 +258,10 @@ awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s_out, voi
   auto cleanup = [&] {
     if (ws) cudaFreeAsync(ws, s);
   };
-  Carver c;
-  const size_t o_u = c.take<double>(int64_t(n_grid) * K);
-  const size_t o_mm = c.take<unsigned long long>(2 * n_grid);
-  AWQ_CUDA(pool_alloc(&ws, c.off, s), "scratch allocation");
-  char* b = static_cast<char*>(ws);
-  AWQ_CUDA(launch_scales(sX, K, n_grid, reinterpret_cast<double*>(b + o_u),
-                         reinterpret_cast<unsigned long long*>(b + o_mm), s_out, nullptr, s),
-           "scale kernels");
+  AWQ_CUDA(pool_alloc(&ws, 2 * sizeof(unsigned long long), s), "scratch allocation");
+  auto* range = static_cast<unsigned long long*>(ws);
+  AWQ_CUDA(launch_sx_range(sX, K, range, s), "scale range kernel");
+  AWQ_CUDA(launch_scales(sX, K, n_grid, range, s_out, nullptr, s), "scale kernel");
   AWQ_CUDA(cudaFreeAsync(ws, s), "scratch release");
   return ok();
 }
@@ -417,12 +413,11 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   Carver wc;
   const size_t o_acc = wc.take<unsigned long long>(K);
   const size_t o_sx = wc.take<double>(K);
-  const size_t o_u = wc.take<double>(int64_t(G) * K);
-  const size_t o_mm = wc.take<unsigned long long>(2 * G);
+  const size_t o_rng = wc.take<unsigned long long>(3);   // scale range [2], loss counter
   const size_t o_r = wc.take<float>(int64_t(G) * K);
   const size_t o_d = wc.take<__half>(int64_t(G) * n_pad * K);
   const size_t o_pt = wc.take<float>(int64_t(G) * n_tiles * n_pad);
-  const size_t o_cnt = wc.take<unsigned int>(1);
+  const size_t o_cs = wc.take<double>(int64_t(G) * loss_chunks(n_pad) * n_w);
 
   AWQ_CUDA(pool_alloc(&r->block, rc.off, s), "result allocation");
   AWQ_CUDA(pool_alloc(&ws, wc.off, s), "scratch allocation");
@@ -442,12 +437,12 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   }
   auto* acc = reinterpret_cast<unsigned long long*>(wb + o_acc);
   auto* sx_ws = reinterpret_cast<double*>(wb + o_sx);
-  auto* u_ws = reinterpret_cast<double*>(wb + o_u);
-  auto* mm_ws = reinterpret_cast<unsigned long long*>(wb + o_mm);
+  auto* range = reinterpret_cast<unsigned long long*>(wb + o_rng);
   auto* r_ws = reinterpret_cast<float*>(wb + o_r);
   auto* delta = reinterpret_cast<__half*>(wb + o_d);
   auto* partials = reinterpret_cast<float*>(wb + o_pt);
-  auto* counter = reinterpret_cast<unsigned int*>(wb + o_cnt);
+  auto* chunk_sums = reinterpret_cast<double*>(wb + o_cs);
+  auto* counter = reinterpret_cast<unsigned int*>(range + 2);
   const __half* Xh = static_cast<const __half*>(X);
 
   AWQ_CUDA(cudaMemsetAsync(r->status, 0, sizeof(int), s), "status reset");
@@ -475,19 +470,23 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
     return r->timed ? cudaEventRecord(r->ev[e], s) : cudaSuccess;
   };
   AWQ_CUDA(mark(AWQ_STAGE_STATS), "event record");
-  // 1. channel statistic
+  // 1. channel statistic (and the range of max(sX, 1e-4) for the scales)
   const double* sxp = sX;
+  AWQ_CUDA(cudaMemsetAsync(range, 0, 3 * sizeof(unsigned long long), s), "range reset");
   if (sxp == nullptr) {
     AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, s), "stats kernel");
-    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s, mm_ws, G), "stats finalize kernel");
+    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s, range), "stats finalize kernel");
     r->launches += 2;
     sxp = sx_ws;
   }
   AWQ_CUDA(mark(AWQ_STAGE_SCALES), "event record");
   // 2. scales (and their fp32 reciprocals) for every grid point
-  AWQ_CUDA(launch_scales(sxp, K, G, u_ws, mm_ws, r->s_grid, r_ws, s, sX == nullptr),
-           "scale kernels");
-  r->launches += (sX == nullptr) ? 2 : 3;
+  if (sX != nullptr) {
+    AWQ_CUDA(launch_sx_range(sX, K, range, s), "scale range kernel");
+    r->launches += 1;
+  }
+  AWQ_CUDA(launch_scales(sxp, K, G, range, r->s_grid, r_ws, s), "scale kernel");
+  r->launches += 1;
   AWQ_CUDA(mark(AWQ_STAGE_RESIDUAL), "event record");
   // 3. quantize every weight at every grid point; keep the fp16 residual
   for (int i = 0; i < n_w; ++i) {
@@ -504,10 +503,10 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   AWQ_CUDA(mark(AWQ_STAGE_LOSS), "event record");
   // 5. losses and argmin
   AWQ_CUDA(launch_loss_reduce(partials, G, static_cast<int>(n_tiles), n_pad, T, map, n_total,
-                              r->row_losses, r->losses, r->best, r->alpha, r->s_grid, K, r->s,
-                              counter, s),
+                              chunk_sums, r->row_losses, r->losses, r->best, r->alpha,
+                              r->s_grid, K, r->s, counter, s),
            "loss reduction");
-  r->launches += 2;
+  r->launches += 1;
   AWQ_CUDA(mark(AWQ_STAGE_FINAL), "event record");
   // 6. final quantization at the chosen grid point (index read on the device)
   for (int i = 0; i < n_w; ++i) {

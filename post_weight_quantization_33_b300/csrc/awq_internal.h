@@ -44,17 +44,17 @@ struct RowMap {
 // ---- statistics and scales (awq_stats.cu)
 cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
                                     unsigned long long* acc, cudaStream_t st);
-// maxmin (nullable): also write the starting values of launch_scales'
-// max/min words for n_grid grid points.
+// range (nullable, 2 words zeroed by the caller): also the range of
+// max(sX, 1e-4) over the channels, for launch_scales.
 cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int64_t K,
                                   double* sX, cudaStream_t st,
-                                  unsigned long long* maxmin = nullptr, int n_grid = 0);
-// u_ws: [n_grid][K] fp64 scratch; maxmin_ws: [2*n_grid] u64 scratch, which
-// this launcher initialises unless maxmin_ready (done by launch_stats_finalize).
-// r (nullable): fp32 1/s [n_grid][K].
-cudaError_t launch_scales(const double* sX, int64_t K, int n_grid, double* u_ws,
-                          unsigned long long* maxmin_ws, float* s, float* r, cudaStream_t st,
-                          bool maxmin_ready = false);
+                                  unsigned long long* range = nullptr);
+// The same range for a caller-given sX (zeroes `range` first).
+cudaError_t launch_sx_range(const double* sX, int64_t K, unsigned long long* range,
+                            cudaStream_t st);
+// s: fp32 [n_grid][K]; r (nullable): fp32 1/s [n_grid][K].
+cudaError_t launch_scales(const double* sX, int64_t K, int n_grid,
+                          const unsigned long long* range, float* s, float* r, cudaStream_t st);
 
 // ---- group quantizer (awq_quant.cu)
 // Search output: delta[a][row_off + n][k] = fp16(w - (q - z) * scale / s_k)
@@ -87,10 +87,14 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st);
 
 // ---- loss reduction (awq_reduce.cu)
-// Also copies s_grid[best] (K floats) to s_out.  counter: one u32 of scratch.
+// Number of 256-row chunks of the padded row space (chunk_sums holds
+// n_alpha * loss_chunks(n_pad) * n_w doubles of scratch).
+int64_t loss_chunks(int64_t n_pad);
+// Also copies s_grid[best] (K floats) to s_out.  counter: one u32 of scratch,
+// zeroed by the caller before the launch.
 cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
                                int64_t T, const RowMap& map, int64_t n_total,
-                               double* row_losses, double* losses, int* best,
+                               double* chunk_sums, double* row_losses, double* losses, int* best,
                                double* alpha_out, const float* s_grid, int64_t K, float* s_out,
                                unsigned int* counter, cudaStream_t st);
 

@@ -10,69 +10,89 @@
 namespace awq {
 namespace {
 
-// row_losses[a][compact row] = sum over token tiles of partials[a][tile][virtual row].
-__global__ void k_row_losses(const float* __restrict__ partials, int n_tiles, int64_t n_pad,
-                             RowMap map, int64_t n_total, double* __restrict__ row_losses,
-                             unsigned int* __restrict__ counter) {
+constexpr int kLossRows = 256;   // rows per block (a chunk)
+
+// Block (c, a): rows [256c, 256c + 256) of the padded row space, grid point
+// a.  Per row: the sum over token tiles of partials[a][tile][row], in tile
+// order, written to row_losses; per weight present in the chunk: the sum of
+// its rows by a fixed tree, written to chunk_sums[a][c][w].  The last block
+// to finish (counted on *counter, zeroed by the caller) adds the chunks of
+// every grid point in chunk order, divides by N_w * T, sums the weights, takes
+// the argmin -- first minimum, NaN as +inf -- and copies the chosen scale
+// vector to s_out.  Every sum has a fixed order: the result is deterministic.
+__global__ void __launch_bounds__(kLossRows)
+    k_losses(const float* __restrict__ partials, int n_tiles, int64_t n_pad, RowMap map,
+             int64_t n_total, int64_t T, double* __restrict__ chunk_sums,
+             double* __restrict__ row_losses, double* __restrict__ losses,
+             int* __restrict__ best, double* __restrict__ alpha_out,
+             const float* __restrict__ s_grid, int64_t K, float* __restrict__ s_out,
+             unsigned int* __restrict__ counter) {
+  __shared__ double red[kLossRows];
+  __shared__ int last, chosen;
+  const int c = blockIdx.x;
   const int a = blockIdx.y;
-  if (a == 0 && blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
-  const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (v >= n_pad) return;
+  const int n_chunks = gridDim.x;
+  const int n_grid = gridDim.y;
+  const int64_t v = static_cast<int64_t>(c) * kLossRows + threadIdx.x;   // padded row
   int w = 0;
   while (w + 1 < map.n_w && v >= map.pad_off[w + 1]) ++w;
   const int64_t n = v - map.pad_off[w];
-  if (n >= map.rows[w]) return;   // padding row
-  double s = 0.0;
-  for (int t = 0; t < n_tiles; ++t)
-    s += static_cast<double>(partials[(static_cast<int64_t>(a) * n_tiles + t) * n_pad + v]);
-  row_losses[static_cast<int64_t>(a) * n_total + map.cum[w] + n] = s;
-}
-
-// losses[a] = sum_w (sum_n row_losses[a][w, n]) / (N_w * T); one block per a.
-// The last block to finish (counted on *counter, zeroed by k_row_losses)
-// takes the argmin -- first minimum, NaN as +inf -- and copies the chosen
-// scale vector to s_out.
-__global__ void k_grid_losses(const double* __restrict__ row_losses, RowMap map, int64_t n_total,
-                              int64_t T, double* __restrict__ losses, int* __restrict__ best,
-                              double* __restrict__ alpha_out, const float* __restrict__ s_grid,
-                              int64_t K, float* __restrict__ s_out,
-                              unsigned int* __restrict__ counter) {
-  __shared__ double red[256];
-  __shared__ int last, chosen;
-  const int a = blockIdx.x;
-  const int n_grid = gridDim.x;
-  const double* rl = row_losses + static_cast<int64_t>(a) * n_total;
-  double total = 0.0;
-  for (int w = 0; w < map.n_w; ++w) {
-    double s = 0.0;
-    for (int64_t n = threadIdx.x; n < map.rows[w]; n += blockDim.x) s += rl[map.cum[w] + n];
-    red[threadIdx.x] = s;
+  const bool real = v < n_pad && n < map.rows[w];
+  double row = 0.0;
+  if (real) {
+    const float* pa = partials + static_cast<int64_t>(a) * n_tiles * n_pad + v;
+    for (int t = 0; t < n_tiles; ++t) row += static_cast<double>(pa[static_cast<int64_t>(t) * n_pad]);
+    row_losses[static_cast<int64_t>(a) * n_total + map.cum[w] + n] = row;
+  }
+  // Per-weight chunk sums (a chunk of 256 rows meets at most a few weights).
+  const int64_t v0 = static_cast<int64_t>(c) * kLossRows;
+  double* cs = chunk_sums + (static_cast<int64_t>(a) * n_chunks + c) * map.n_w;
+  for (int wi = 0; wi < map.n_w; ++wi) {
+    const int64_t lo = map.pad_off[wi];
+    const int64_t hi = lo + map.rows[wi];
+    if (hi <= v0 || lo >= v0 + kLossRows) {   // block-uniform: weight absent from the chunk
+      if (threadIdx.x == 0) cs[wi] = 0.0;
+      continue;
+    }
+    red[threadIdx.x] = (real && w == wi) ? row : 0.0;
     __syncthreads();
-    for (int off = blockDim.x / 2; off; off >>= 1) {
+    for (int off = kLossRows / 2; off; off >>= 1) {
       if (threadIdx.x < off) red[threadIdx.x] += red[threadIdx.x + off];
       __syncthreads();
     }
-    if (threadIdx.x == 0)
-      total += red[0] / (static_cast<double>(map.rows[w]) * static_cast<double>(T));
+    if (threadIdx.x == 0) cs[wi] = red[0];
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    losses[a] = total;
     __threadfence();
-    last = (atomicAdd(counter, 1u) == static_cast<unsigned>(n_grid) - 1u);
+    last = (atomicAdd(counter, 1u) == static_cast<unsigned>(n_chunks * n_grid) - 1u);
   }
   __syncthreads();
   if (!last) return;
+  __threadfence();
+  // Final reduction: thread i handles grid point i (n_grid <= 64 <= 256).
+  const volatile double* vcs = chunk_sums;
+  if (threadIdx.x < n_grid) {
+    const int ga = threadIdx.x;
+    double total = 0.0;
+    for (int wi = 0; wi < map.n_w; ++wi) {
+      double sw = 0.0;
+      for (int ci = 0; ci < n_chunks; ++ci)
+        sw += vcs[(static_cast<int64_t>(ga) * n_chunks + ci) * map.n_w + wi];
+      total += sw / (static_cast<double>(map.rows[wi]) * static_cast<double>(T));
+    }
+    losses[ga] = total;
+    red[ga] = total;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const volatile double* lv = losses;
     int bi = 0;
     double bv = 0.0;
     for (int i = 0; i < n_grid; ++i) {
-      const double v = isnan(lv[i]) ? INFINITY : lv[i];
-      if (i == 0 || v < bv) {
+      const double x = isnan(red[i]) ? INFINITY : red[i];
+      if (i == 0 || x < bv) {
         bi = i;
-        bv = v;
+        bv = x;
       }
     }
     *best = bi;
@@ -86,15 +106,17 @@ __global__ void k_grid_losses(const double* __restrict__ row_losses, RowMap map,
 
 }  // namespace
 
+int64_t loss_chunks(int64_t n_pad) { return ceil_div(n_pad, kLossRows); }
+
 cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
                                int64_t T, const RowMap& map, int64_t n_total,
-                               double* row_losses, double* losses, int* best,
+                               double* chunk_sums, double* row_losses, double* losses, int* best,
                                double* alpha_out, const float* s_grid, int64_t K, float* s_out,
                                unsigned int* counter, cudaStream_t st) {
-  const dim3 g1(static_cast<unsigned>(ceil_div(n_pad, 256)), static_cast<unsigned>(n_alpha));
-  k_row_losses<<<g1, 256, 0, st>>>(partials, n_tiles, n_pad, map, n_total, row_losses, counter);
-  k_grid_losses<<<n_alpha, 256, 0, st>>>(row_losses, map, n_total, T, losses, best, alpha_out,
-                                         s_grid, K, s_out, counter);
+  const dim3 grid(static_cast<unsigned>(loss_chunks(n_pad)), static_cast<unsigned>(n_alpha));
+  k_losses<<<grid, kLossRows, 0, st>>>(partials, n_tiles, n_pad, map, n_total, T, chunk_sums,
+                                       row_losses, losses, best, alpha_out, s_grid, K, s_out,
+                                       counter);
   return cudaGetLastError();
 }
 

@@ -273,7 +273,7 @@ def test_stage_timing_and_launch_count():
         ms = r.stage_ms()
         assert set(ms) == set(awq.STAGES) and all(v >= 0 for v in ms.values())
         assert ms["error_gemm"] > 0
-        assert r.kernel_launches == 9   # 2 stats, 2 scales, 1 residual, 1 GEMM, 2 loss, 1 final
+        assert r.kernel_launches == 7   # 2 stats, 1 scales, 1 residual, 1 GEMM, 1 loss, 1 final
         r.free()
     finally:
         awq.set_stage_timing(False)
