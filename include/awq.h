@@ -34,11 +34,16 @@
  *    (never a trap), see awq_result_check and awq_reference_output.
  *
  * Quantizer (fp32, every operation correctly rounded, none fused), per group
- * of `group_size` consecutive input channels of one output row:
- *   w' = w * s_k;  rng = max w' - min w';  step = max(rng, 1e-5) / (2^b - 1);
+ * of `group_size` consecutive input channels of one output row (group_size
+ * -1: the whole row is one group):
+ *   w' = w * s_k;
+ *   asymmetric (zero_point 1): step = max(max w' - min w', 1e-5) / (2^b - 1),
+ *     zero = clamp(rne(-min w' * rcp), 0, 2^b - 1);
+ *   symmetric (zero_point 0): step = max(max |w'|, 1e-5) / (2^(b-1) - 1),
+ *     zero = 2^(b-1);
  *   scale = fp16_rne(step);  rcp = 1 / float(scale);
- *   zero = clamp(rne(-min w' * rcp), 0, 2^b - 1);
  *   code = clamp(rne(w' * rcp) + zero, 0, 2^b - 1);   rne = half to even.
+ * Dequantization is (code - zero) * scale in both forms.
  * Scale vector: u_k = max(sX_k, 1e-4)^alpha (fp64),
  *   s_k = fp32(u_k / sqrt(max_k u * min_k u)),  alpha_i = i / n_grid.
  * Loss: ||W X^T - deq(Q(W diag(s))) diag(s)^-1 X^T||_F^2 / (N T), summed over
@@ -80,8 +85,9 @@ typedef enum awq_status {
 
 /* Quantizer configuration ("AWQ Explained", multigrid.ai, "How the scale is
  * chosen": bits, group_size, zero_point).  Supported: bits 3 or 4,
- * group_size 64 or 128, zero_point 1, n_grid 1..AWQ_MAX_GRID (20 is the
- * default grid alpha = 0, 0.05, ..., 0.95). */
+ * group_size 64, 128 or -1 (one group per output row; K must then be a
+ * multiple of 64), zero_point 1 (asymmetric) or 0 (symmetric), n_grid
+ * 1..AWQ_MAX_GRID (20 is the default grid alpha = 0, 0.05, ..., 0.95). */
 typedef struct awq_qconfig {
   int bits;
   int group_size;
@@ -133,12 +139,13 @@ awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s, void* s
 
 /* Scale, group-quantize and pack one weight ("AWQ Explained", multigrid.ai,
  * "Scaling instead of mixed precision"; realpython glossary: 3/4-bit codes in
- * groups).  One pass over W; allocates nothing.
+ * groups).  One pass over W; allocates nothing, except N*8 bytes of
+ * stream-ordered scratch for group_size -1 (a row min / max pre-pass).
  *   W      : device fp16 [N][K]; N >= 0 (N = 0 is a no-op), K % group == 0.
  *   s      : device fp32 [K] (the per-input-channel scale).
  *   codes  : device uint32 [awq_packed_words(N, K, bits)], written.
- *   scales : device fp16 [N][K/group], written.
- *   zeros  : device uint8 [N][K/group], written. */
+ *   scales : device fp16 [N][K/group] ([N][1] for group_size -1), written.
+ *   zeros  : device uint8 [N][K/group] ([N][1] for group_size -1), written. */
 awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s,
                              const awq_qconfig* cfg, uint32_t* codes, void* scales,
                              uint8_t* zeros, void* stream);
@@ -147,6 +154,23 @@ awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s
  *   codes : device uint32 [awq_packed_words(N, K, bits)];  q : device uint8 [N][K]. */
 awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                             void* stream);
+
+/* Deploy step: fold diag(s)^-1 into the operation that produces the
+ * layer's input ("AWQ Explained", multigrid.ai, "Scaling instead of mixed
+ * precision": the inverse scale folds offline into the preceding LayerNorm /
+ * RMSNorm weight or preceding linear layer, so what ships is the quantized
+ * matrix and a modified norm).
+ *   V    : device fp16 [rows][cols] row-major, 2-byte aligned.  rows = K of
+ *          the quantized layer; cols = 1 for a vector (a norm weight or a
+ *          bias), or the preceding linear layer's input width (its weight is
+ *          [K][cols]: output row k feeds input channel k).
+ *   s    : device fp32 [rows] (the scale the search chose, awq_result_s).
+ *   out  : device fp16 [rows][cols], written:
+ *          out[i][j] = fp16_rne(fp32(V[i][j]) / s[i]) (correctly rounded fp32
+ *          division).  May be V itself (in place).
+ * rows, cols >= 1.  One HBM pass; allocates nothing. */
+awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float* s, void* out,
+                          void* stream);
 
 /* Layer output before quantization, Y = W X^T ("AWQ Explained", multigrid.ai,
  * "How the scale is chosen": the W x term), on tcgen05 tensor cores.
@@ -196,8 +220,9 @@ const double* awq_result_row_losses(const awq_result* r); /* device fp64 [n_grid
                                                               sum_t error^2 per output row,
                                                               weights concatenated in order */
 const uint32_t* awq_result_codes(const awq_result* r, int i);  /* device packed codes of W_i */
-const void* awq_result_scales(const awq_result* r, int i);     /* device fp16 [N_i][K/group] */
-const uint8_t* awq_result_zeros(const awq_result* r, int i);   /* device uint8 [N_i][K/group] */
+const void* awq_result_scales(const awq_result* r, int i);     /* device fp16 [N_i][K/group],
+                                                                  [N_i][1] for group -1 */
+const uint8_t* awq_result_zeros(const awq_result* r, int i);   /* device uint8, same shape */
 
 /* Number of kernels the search enqueued (host value, valid on return). */
 int awq_result_kernel_launches(const awq_result* r);

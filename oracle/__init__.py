@@ -8,6 +8,7 @@ from .awq_oracle import (  # noqa: F401
     channel_magnitude,
     dequantize_scaled,
     first_argmin,
+    fold_inverse_scale,
     layer_loss,
     output_error_rows,
     pack_codes,

@@ -25,6 +25,10 @@ it follows.  Pages (by title):
   glossary): 3- or 4-bit packing in groups, commonly 128.
 * [AI360] "AWQ" (ai360xpert.com), section "How It Works", step 4: the scaled
   weights are quantized with plain round-to-nearest.
+* [MG-FOLD] "AWQ Explained" (multigrid.ai), "Scaling instead of mixed
+  precision": diag(s)^-1 is folded offline into the operation that produces
+  the layer's input (the preceding LayerNorm / RMSNorm weight, or a preceding
+  linear layer), so what ships is the quantized matrix and a modified norm.
 
 Readings where the pages are silent (each also listed in the design doc):
 
@@ -48,6 +52,18 @@ Readings where the pages are silent (each also listed in the design doc):
 6. Packing: INT4 row n, word j holds codes 8j..8j+7 in nibbles 0..7 (code 8j
    in bits 0-3).  INT3 row n is a little-endian bit stream, code k in bits
    [3k, 3k+3), 32 codes per 3 uint32 words.
+7. Folding: V'[k] = fp16(fp32(V[k]) / s_k) for a norm weight or bias; for a
+   preceding linear layer [K][M] (its output row k feeds input channel k)
+   every entry of row k is divided by s_k.  One correctly rounded fp32
+   division, then round-to-nearest-even to fp16.
+8. Symmetric quantizer (zero_point false; AI360 "The Idea": quantization
+   groups weights and scales them by their maximum value):
+   step = max(max|w'|, 1e-5) / (2^(b-1) - 1), scale = fp16_rne(step),
+   rcp = fp32(1 / scale), the zero point is the fixed mid-code 2^(b-1), and
+   q = clamp(rne(w' * rcp) + 2^(b-1), 0, 2^b - 1) -- the same stored layout
+   and dequantization (q - z) * scale.
+9. group_size -1 (the AwqConfig knob in [MG] "How the scale is chosen"):
+   one group spans an output row's K channels.
 
 Parity pins for every function here live in ``tests/test_oracle_pins.py``.
 """
@@ -99,14 +115,19 @@ def scale_vector(sX: np.ndarray, alpha: float) -> np.ndarray:
 # [MG] "the grid step is the group's range divided by the number of levels";
 # [AI360] step 4 round-to-nearest; [MG] AwqConfig zero_point = true).
 # --------------------------------------------------------------------------
-def quantize_groups(W: np.ndarray, s: np.ndarray, bits: int, group: int):
+def quantize_groups(W: np.ndarray, s: np.ndarray, bits: int, group: int,
+                    zero_point: bool = True):
     """Return (codes uint8 [N,K], scales fp16 [N,K/group], zeros uint8 [N,K/group]).
 
+    ``group`` = -1 makes one group of each output row (reading 9).
+    ``zero_point`` False is the symmetric form of reading 8.
     All arithmetic is fp32 (numpy evaluates each operation separately and
-    rounds it; nothing is fused), following reading 3 step by step.
+    rounds it; nothing is fused), following readings 3 and 8 step by step.
     """
     W = np.asarray(W, np.float16)
     N, K = W.shape
+    if group == -1:
+        group = K
     if K % group:
         raise ValueError("K must be a multiple of the group size")
     levels = np.float32((1 << bits) - 1)
@@ -115,12 +136,19 @@ def quantize_groups(W: np.ndarray, s: np.ndarray, bits: int, group: int):
     g = w_scaled.reshape(N, K // group, group)
     mn = g.min(axis=2)
     mx = g.max(axis=2)
-    rng = mx - mn                                                  # fp32
-    step32 = np.maximum(rng, RANGE_FLOOR) / levels                 # fp32 divide
+    if zero_point:
+        rng = mx - mn                                              # fp32
+        step32 = np.maximum(rng, RANGE_FLOOR) / levels             # fp32 divide
+    else:
+        amax = np.maximum(-mn, mx)                                 # max |w'|
+        step32 = np.maximum(amax, RANGE_FLOOR) / np.float32((1 << (bits - 1)) - 1)
     scale16 = step32.astype(np.float16)                            # fp16 RNE
     sf = scale16.astype(np.float32)
     rcp = np.float32(1.0) / sf                                     # fp32 reciprocal
-    zero = np.clip(np.rint(-mn * rcp), 0, levels)                  # integer zero point
+    if zero_point:
+        zero = np.clip(np.rint(-mn * rcp), 0, levels)              # integer zero point
+    else:
+        zero = np.full(mn.shape, np.float32(1 << (bits - 1)))      # fixed mid-code
     q = np.rint(g * rcp[:, :, None]) + zero[:, :, None]
     q = np.clip(q, 0, levels)
     return (q.reshape(N, K).astype(np.uint8), scale16,
@@ -234,7 +262,8 @@ def first_argmin(losses: Sequence[float]) -> int:
 
 def search(X: np.ndarray, Ws: Sequence[np.ndarray], bits: int = 4, group: int = 128,
            n_grid: int = 20, sX: Optional[np.ndarray] = None,
-           rows: Optional[Sequence[Optional[np.ndarray]]] = None) -> Dict:
+           rows: Optional[Sequence[Optional[np.ndarray]]] = None,
+           zero_point: bool = True) -> Dict:
     """The full search for the weights ``Ws`` sharing activations ``X``.
 
     ``rows`` (optional, one entry per weight) restricts the loss to a subset of
@@ -258,6 +287,7 @@ def search(X: np.ndarray, Ws: Sequence[np.ndarray], bits: int = 4, group: int = 
         sel.append(np.asarray(W, np.float16) if r is None
                    else np.asarray(W, np.float16)[np.asarray(r)])
     X64 = X.astype(np.float64)
+    grp = K if group == -1 else group
     Yref = [w.astype(np.float64) @ X64.T for w in sel]
     s_grid = np.stack([scale_vector(sX, a) for a in alphas])
     row_losses = [np.zeros((n_grid, w.shape[0])) for w in sel]
@@ -266,8 +296,8 @@ def search(X: np.ndarray, Ws: Sequence[np.ndarray], bits: int = 4, group: int = 
         s = s_grid[i]
         total = 0.0
         for wi, w in enumerate(sel):
-            c, sc, z = quantize_groups(w, s, bits, group)
-            rl = output_error_rows(w, X, s, c, sc, z, group, Y=Yref[wi])
+            c, sc, z = quantize_groups(w, s, bits, group, zero_point)
+            rl = output_error_rows(w, X, s, c, sc, z, grp, Y=Yref[wi])
             row_losses[wi][i] = rl
             total += rl.sum() / (w.shape[0] * T)
         losses[i] = total
@@ -275,7 +305,7 @@ def search(X: np.ndarray, Ws: Sequence[np.ndarray], bits: int = 4, group: int = 
     s_best = s_grid[best]
     codes, scales, zeros, packed = [], [], [], []
     for w in sel:
-        c, sc, z = quantize_groups(w, s_best, bits, group)
+        c, sc, z = quantize_groups(w, s_best, bits, group, zero_point)
         codes.append(c)
         scales.append(sc)
         zeros.append(z)
@@ -283,3 +313,18 @@ def search(X: np.ndarray, Ws: Sequence[np.ndarray], bits: int = 4, group: int = 
     return dict(sX=sX, alphas=alphas, s_grid=s_grid, row_losses=row_losses,
                 losses=losses, best=best, alpha=float(alphas[best]), s=s_best,
                 codes=codes, scales=scales, zeros=zeros, packed=packed)
+
+
+# --------------------------------------------------------------------------
+# Step 7: deploy ([MG-FOLD]; reading 7): fold diag(s)^-1 into the producer
+# of the layer's input.
+# --------------------------------------------------------------------------
+def fold_inverse_scale(V: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """V / s along the first axis: a vector [K] (norm weight or bias) or a
+    preceding linear layer [K, M]; fp32 division, fp16 result."""
+    V = np.asarray(V, np.float16)
+    s32 = np.asarray(s, np.float32)
+    if V.shape[0] != s32.shape[0]:
+        raise ValueError("V's first axis must match s")
+    d = s32 if V.ndim == 1 else s32.reshape((-1,) + (1,) * (V.ndim - 1))
+    return (V.astype(np.float32) / d).astype(np.float16)

@@ -13,6 +13,7 @@ Functions mirror the C entry points:
 ``quantize_pack(W, s, bits, g)``  packed codes, fp16 scales, u8 zeros  (awq_quantize_pack)
 ``unpack_codes(codes, N, K, b)``  codes as uint8 [N, K]                (awq_unpack_codes)
 ``reference_output(W, X)``        Y = W X^T in fp32                    (awq_reference_output)
+``fold_scale(V, s)``              V / s along rows (deploy step)       (awq_fold_scale)
 ``search(X, Ws, ...)``            the full per-layer search            (awq_search_layer)
 """
 from __future__ import annotations
@@ -25,8 +26,8 @@ import numpy as np
 import torch
 
 __all__ = [
-    "AwqError", "lib", "library_path", "stats", "stats_noalloc", "scales", "quantize_pack", "unpack_codes",
-    "reference_output", "search", "search_host", "SearchResult", "packed_words",
+    "AwqError", "lib", "library_path", "groups_per_row", "stats", "stats_noalloc", "scales", "quantize_pack", "unpack_codes",
+    "reference_output", "fold_scale", "search", "search_host", "SearchResult", "packed_words",
     "release_cached_memory", "selftest_bounded_wait", "set_stage_timing", "STAGES",
     "EXPORTED_SYMBOLS",
 ]
@@ -46,7 +47,7 @@ EXPORTED_SYMBOLS = (
     "awq_result_s", "awq_result_s_grid", "awq_result_row_losses", "awq_result_codes",
     "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
     "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
-    "awq_result_stage_ms", "awq_stats_noalloc",
+    "awq_result_stage_ms", "awq_stats_noalloc", "awq_fold_scale",
 )
 
 # Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
         "awq_quantize_pack": (st, [vp, i64, i64, vp, ctypes.POINTER(QConfig), vp, vp, vp, vp]),
         "awq_unpack_codes": (st, [vp, i64, i64, i32, vp, vp]),
         "awq_reference_output": (st, [vp, i64, vp, i64, i64, vp, vp, vp]),
+        "awq_fold_scale": (st, [vp, i64, i64, vp, vp, vp]),
         "awq_search_layer": (st, [vp, i64, i64, vp, ctypes.POINTER(Weight), i32,
                                   ctypes.POINTER(QConfig), vp, ctypes.POINTER(vp)]),
         "awq_result_check": (st, [vp]),
@@ -148,8 +150,13 @@ def _require(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
-def _cfg(bits: int, group: int, n_grid: int = 20) -> QConfig:
-    return QConfig(bits, group, 1, n_grid)
+def _cfg(bits: int, group: int, n_grid: int = 20, zero_point: bool = True) -> QConfig:
+    return QConfig(bits, group, 1 if zero_point else 0, n_grid)
+
+
+def groups_per_row(K: int, group: int) -> int:
+    """Quantization groups in a row of K channels (group -1: the whole row)."""
+    return 1 if group == -1 else K // group
 
 
 def packed_words(N: int, K: int, bits: int) -> int:
@@ -186,7 +193,8 @@ def scales(sX: torch.Tensor, n_grid: int = 20) -> torch.Tensor:
     return s
 
 
-def quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: int = 128):
+def quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: int = 128,
+                  zero_point: bool = True):
     """(codes int32 [words] holding the uint32 bit patterns, scales fp16 [N, K/g], zeros u8)."""
     _require(W, "W", torch.float16, 2)
     _require(s, "s", torch.float32, 1)
@@ -195,9 +203,10 @@ def quantize_pack(W: torch.Tensor, s: torch.Tensor, bits: int = 4, group: int = 
     if words < 0:
         raise ValueError(f"cannot pack K={K} at {bits} bits")
     codes = torch.empty(max(words, 1), dtype=torch.int32, device=W.device)[:words]
-    sc = torch.empty((N, K // group), dtype=torch.float16, device=W.device)
-    z = torch.empty((N, K // group), dtype=torch.uint8, device=W.device)
-    cfg = _cfg(bits, group)
+    G = groups_per_row(K, group)
+    sc = torch.empty((N, G), dtype=torch.float16, device=W.device)
+    z = torch.empty((N, G), dtype=torch.uint8, device=W.device)
+    cfg = _cfg(bits, group, 20, zero_point)
     _check(lib().awq_quantize_pack(W.data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg),
                                    codes.data_ptr(), sc.data_ptr(), z.data_ptr(), _stream()))
     return codes, sc, z
@@ -224,6 +233,22 @@ def reference_output(W: torch.Tensor, X: torch.Tensor, check: bool = True) -> to
     if check and int(status.item()) != 0:
         raise AwqError(AWQ_ERR_TIMEOUT, f"bounded device wait expired (code {int(status.item())})")
     return Y
+
+
+def fold_scale(V: torch.Tensor, s: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """fp16 V / s along the first axis (a norm weight or bias [K], or a
+    preceding linear layer's weight [K, M]); `out` may be V (in place)."""
+    if V.dtype != torch.float16 or V.dim() not in (1, 2) or not V.is_cuda or not V.is_contiguous():
+        raise ValueError("V must be a contiguous CUDA fp16 tensor [K] or [K, M]")
+    _require(s, "s", torch.float32, 1)
+    rows = V.shape[0]
+    cols = 1 if V.dim() == 1 else V.shape[1]
+    if out is None:
+        out = torch.empty_like(V)
+    elif out.shape != V.shape or out.dtype != torch.float16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp16 tensor shaped like V")
+    _check(lib().awq_fold_scale(V.data_ptr(), rows, cols, s.data_ptr(), out.data_ptr(), _stream()))
+    return out
 
 
 class _DevArray:
@@ -302,11 +327,13 @@ class SearchResult:
 
     def scales(self, i: int = 0) -> torch.Tensor:
         return _alias(lib().awq_result_scales(self._handle(), i),
-                      (self.Ns[i], self.K // self.group), "<f2", self.device).clone()
+                      (self.Ns[i], groups_per_row(self.K, self.group)), "<f2",
+                      self.device).clone()
 
     def zeros(self, i: int = 0) -> torch.Tensor:
         return _alias(lib().awq_result_zeros(self._handle(), i),
-                      (self.Ns[i], self.K // self.group), "|u1", self.device).clone()
+                      (self.Ns[i], groups_per_row(self.K, self.group)), "|u1",
+                      self.device).clone()
 
     @property
     def kernel_launches(self) -> int:
@@ -335,8 +362,10 @@ class SearchResult:
 
 
 def search(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: int = 128,
-           n_grid: int = 20, sX: Optional[torch.Tensor] = None) -> SearchResult:
-    """Run awq_search_layer for the weights ``Ws`` sharing activations ``X``."""
+           n_grid: int = 20, sX: Optional[torch.Tensor] = None,
+           zero_point: bool = True) -> SearchResult:
+    """Run awq_search_layer for the weights ``Ws`` sharing activations ``X``
+    (group -1: one group per output row; zero_point False: symmetric)."""
     _require(X, "X", torch.float16, 2)
     T, K = X.shape
     arr = (Weight * len(Ws))()
@@ -350,7 +379,7 @@ def search(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: in
     if sX is not None:
         _require(sX, "sX", torch.float64, 1)
         sxp = sX.data_ptr()
-    cfg = _cfg(bits, group, n_grid)
+    cfg = _cfg(bits, group, n_grid, zero_point)
     out = ctypes.c_void_p()
     _check(lib().awq_search_layer(X.data_ptr(), T, K, sxp, arr, len(Ws), ctypes.byref(cfg),
                                   _stream(), ctypes.byref(out)))
@@ -358,14 +387,14 @@ def search(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: in
 
 
 def search_host(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: int = 128,
-                n_grid: int = 20, device="cuda") -> dict:
+                n_grid: int = 20, device="cuda", zero_point: bool = True) -> dict:
     """Search with host (CPU, ideally pinned) inputs; returns host outputs.
 
     Copies X and the weights to the device, runs ``search`` and copies the
     results back (codes, scales, zeros per weight, s, losses, alpha)."""
     Xd = X.to(device, non_blocking=True)
     Wd = [W.to(device, non_blocking=True) for W in Ws]
-    r = search(Xd, Wd, bits, group, n_grid)
+    r = search(Xd, Wd, bits, group, n_grid, zero_point=zero_point)
     try:
         out = {
             "codes": [r.codes(i).to("cpu", non_blocking=True) for i in range(len(Ws))],

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -74,14 +75,27 @@ awq_status check_dev(const void* p, const char* name, uintptr_t align) {
   return AWQ_OK;
 }
 
+// K must be a multiple of the group size, and of 64 for one group per row
+// (the quantizer's 16-channel lanes and the GEMM's 64-channel K step).
+bool k_fits(int64_t K, const awq_qconfig* cfg) {
+  const int64_t g = cfg->group_size == -1 ? 64 : cfg->group_size;
+  return K >= 1 && K % g == 0;
+}
+
+int64_t groups_per_row(int64_t K, const awq_qconfig* cfg) {
+  return cfg->group_size == -1 ? 1 : K / cfg->group_size;
+}
+
 awq_status check_cfg(const awq_qconfig* cfg) {
   if (cfg == nullptr) return fail(AWQ_ERR_INVALID, "cfg is NULL");
   if (cfg->bits != 3 && cfg->bits != 4)
     return fail(AWQ_ERR_UNSUPPORTED, "bits=%d (supported: 3, 4)", cfg->bits);
-  if (cfg->group_size != 64 && cfg->group_size != 128)
-    return fail(AWQ_ERR_UNSUPPORTED, "group_size=%d (supported: 64, 128)", cfg->group_size);
-  if (cfg->zero_point != 1)
-    return fail(AWQ_ERR_UNSUPPORTED, "zero_point=%d (supported: 1, asymmetric)", cfg->zero_point);
+  if (cfg->group_size != 64 && cfg->group_size != 128 && cfg->group_size != -1)
+    return fail(AWQ_ERR_UNSUPPORTED, "group_size=%d (supported: 64, 128, -1 = per row)",
+                cfg->group_size);
+  if (cfg->zero_point != 0 && cfg->zero_point != 1)
+    return fail(AWQ_ERR_UNSUPPORTED, "zero_point=%d (supported: 1 asymmetric, 0 symmetric)",
+                cfg->zero_point);
   if (cfg->n_grid < 1 || cfg->n_grid > kMaxGrid)
     return fail(AWQ_ERR_INVALID, "n_grid=%d (1..%d)", cfg->n_grid, kMaxGrid);
   return AWQ_OK;
@@ -272,8 +286,9 @@ awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s
   awq_status st;
   if ((st = check_cfg(cfg)) != AWQ_OK) return st;
   if (N < 0) return fail(AWQ_ERR_INVALID, "N=%lld", static_cast<long long>(N));
-  if (K < 1 || K % cfg->group_size || K > (int64_t(1) << 31))
-    return fail(AWQ_ERR_INVALID, "K=%lld (must be a positive multiple of group_size=%d)",
+  if (!k_fits(K, cfg) || K > (int64_t(1) << 31))
+    return fail(AWQ_ERR_INVALID,
+                "K=%lld (must be a positive multiple of group_size=%d; of 64 for -1)",
                 static_cast<long long>(K), cfg->group_size);
   if (N == 0) return ok();
   if ((st = check_dev(W, "W", 16)) != AWQ_OK) return st;
@@ -282,10 +297,20 @@ awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s
   if ((st = check_dev(scales, "scales", 2)) != AWQ_OK) return st;
   if ((st = check_dev(zeros, "zeros", 1)) != AWQ_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto cleanup = [] {};
+  void* ws = nullptr;   // per-row min / max, for one group per row only
+  auto cleanup = [&] {
+    if (ws) cudaFreeAsync(ws, s);
+  };
+  if (cfg->group_size == -1)
+    AWQ_CUDA(pool_alloc(&ws, sizeof(float2) * N, s), "scratch allocation");
   AWQ_CUDA(launch_quant_final(static_cast<const __half*>(W), N, K, cfg->bits, cfg->group_size,
-                              s_vec, nullptr, codes, static_cast<__half*>(scales), zeros, s),
+                              cfg->zero_point, s_vec, nullptr, codes,
+                              static_cast<__half*>(scales), zeros, static_cast<float2*>(ws), s),
            "quantize kernel");
+  if (ws) {
+    AWQ_CUDA(cudaFreeAsync(ws, s), "scratch release");
+    ws = nullptr;
+  }
   return ok();
 }
 
@@ -301,6 +326,23 @@ awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bit
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto cleanup = [] {};
   AWQ_CUDA(launch_unpack(codes, N, K, bits, q, s), "unpack kernel");
+  return ok();
+}
+
+awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float* s_vec,
+                          void* out, void* stream) {
+  if (rows < 1 || cols < 1 || rows > (int64_t(1) << 40) / cols)
+    return fail(AWQ_ERR_INVALID, "rows=%lld cols=%lld (both >= 1)", static_cast<long long>(rows),
+                static_cast<long long>(cols));
+  awq_status st;
+  if ((st = check_dev(V, "V", 2)) != AWQ_OK) return st;
+  if ((st = check_dev(s_vec, "s", 4)) != AWQ_OK) return st;
+  if ((st = check_dev(out, "out", 2)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto cleanup = [] {};
+  AWQ_CUDA(launch_fold(static_cast<const __half*>(V), rows, cols, s_vec,
+                       static_cast<__half*>(out), s),
+           "fold kernel");
   return ok();
 }
 
@@ -333,8 +375,9 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   awq_status st;
   if ((st = check_cfg(cfg)) != AWQ_OK) return st;
   if (T < 1) return fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
-  if (K < 1 || K % cfg->group_size)
-    return fail(AWQ_ERR_INVALID, "K=%lld (must be a positive multiple of group_size=%d)",
+  if (!k_fits(K, cfg))
+    return fail(AWQ_ERR_INVALID,
+                "K=%lld (must be a positive multiple of group_size=%d; of 64 for -1)",
                 static_cast<long long>(K), cfg->group_size);
   if (Ws == nullptr || n_w < 1 || n_w > kMaxWeights)
     return fail(AWQ_ERR_INVALID, "n_w=%d (1..%d) with a non-NULL Ws", n_w, kMaxWeights);
@@ -359,7 +402,7 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   const int64_t n_used = n_pad;                 // rows of the last weight's tiles
   n_pad = ceil_div(n_pad, kPairRows) * kPairRows;   // whole pair tiles for the error GEMM
   const int G = cfg->n_grid;
-  const int64_t groups = K / cfg->group_size;
+  const int64_t groups = groups_per_row(K, cfg);
   const int64_t n_tiles = ceil_div(T, kTileN);
   if (K > (int64_t(1) << 30) || T > (int64_t(1) << 30) || n_pad > (int64_t(1) << 30) ||
       (n_pad / kTileM) * n_tiles * G > (int64_t(1) << 30))
@@ -418,6 +461,9 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   const size_t o_d = wc.take<__half>(int64_t(G) * n_pad * K);
   const size_t o_pt = wc.take<float>(int64_t(G) * n_tiles * n_pad);
   const size_t o_cs = wc.take<double>(int64_t(G) * loss_chunks(n_pad) * n_w);
+  int64_t max_rows = 0;
+  for (int i = 0; i < n_w; ++i) max_rows = std::max<int64_t>(max_rows, Ws[i].N);
+  const size_t o_mmr = wc.take<float2>(cfg->group_size == -1 ? int64_t(G) * max_rows : 1);
 
   AWQ_CUDA(pool_alloc(&r->block, rc.off, s), "result allocation");
   AWQ_CUDA(pool_alloc(&ws, wc.off, s), "scratch allocation");
@@ -442,6 +488,7 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   auto* delta = reinterpret_cast<__half*>(wb + o_d);
   auto* partials = reinterpret_cast<float*>(wb + o_pt);
   auto* chunk_sums = reinterpret_cast<double*>(wb + o_cs);
+  auto* rowmm = reinterpret_cast<float2*>(wb + o_mmr);   // per-row min / max (group -1)
   auto* counter = reinterpret_cast<unsigned int*>(range + 2);
   const __half* Xh = static_cast<const __half*>(X);
 
@@ -491,10 +538,10 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   // 3. quantize every weight at every grid point; keep the fp16 residual
   for (int i = 0; i < n_w; ++i) {
     AWQ_CUDA(launch_quant_residual(static_cast<const __half*>(Ws[i].W), Ws[i].N, K, cfg->bits,
-                                   cfg->group_size, r->s_grid, r_ws, G, map.pad_off[i], n_pad,
-                                   delta, s),
+                                   cfg->group_size, cfg->zero_point, r->s_grid, r_ws, G,
+                                   map.pad_off[i], n_pad, delta, rowmm, s),
              "quantize kernel (residual)");
-    r->launches += 1;
+    r->launches += cfg->group_size == -1 ? 2 : 1;
   }
   AWQ_CUDA(mark(AWQ_STAGE_ERROR_GEMM), "event record");
   // 4. error GEMM for every grid point: per-row sums of (residual X^T)^2
@@ -511,10 +558,10 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   // 6. final quantization at the chosen grid point (index read on the device)
   for (int i = 0; i < n_w; ++i) {
     AWQ_CUDA(launch_quant_final(static_cast<const __half*>(Ws[i].W), Ws[i].N, K, cfg->bits,
-                                cfg->group_size, r->s_grid, r->best, r->codes[i], r->scales[i],
-                                r->zeros[i], s),
+                                cfg->group_size, cfg->zero_point, r->s_grid, r->best,
+                                r->codes[i], r->scales[i], r->zeros[i], rowmm, s),
              "quantize kernel (final)");
-    r->launches += 1;
+    r->launches += cfg->group_size == -1 ? 2 : 1;
   }
   AWQ_CUDA(mark(AWQ_NUM_STAGES), "event record");
   // 7. small outputs to pinned host memory

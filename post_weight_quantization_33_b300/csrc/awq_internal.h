@@ -57,18 +57,22 @@ cudaError_t launch_scales(const double* sX, int64_t K, int n_grid,
                           const unsigned long long* range, float* s, float* r, cudaStream_t st);
 
 // ---- group quantizer (awq_quant.cu)
+// group: 64, 128, or -1 (one group per row); zero_point 1 (asymmetric) or 0
+// (symmetric).  rowmm: scratch of n_alpha * N float2 (residual) or N float2
+// (final), used only when group is -1.
 // Search output: delta[a][row_off + n][k] = fp16(w - (q - z) * scale / s_k)
 // for every grid point a, rows of weight i placed at row_off in a row space
 // of n_pad rows.
 cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bits, int group,
-                                  const float* s_grid, const float* r_grid, int n_alpha,
-                                  int64_t row_off, int64_t n_pad, __half* delta,
-                                  cudaStream_t st);
-// Result layout: packed codes, fp16 scales [N][K/group], u8 zeros [N][K/group].
-// The scale vector is s + (*sel) * K when sel is non-null, else s.
+                                  int zero_point, const float* s_grid, const float* r_grid,
+                                  int n_alpha, int64_t row_off, int64_t n_pad, __half* delta,
+                                  float2* rowmm, cudaStream_t st);
+// Result layout: packed codes, fp16 scales [N][K/group], u8 zeros [N][K/group]
+// (one per row for group -1).  The scale vector is s + (*sel) * K when sel is
+// non-null, else s.
 cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, int group,
-                               const float* s, const int* sel, uint32_t* codes,
-                               __half* scales, uint8_t* zeros, cudaStream_t st);
+                               int zero_point, const float* s, const int* sel, uint32_t* codes,
+                               __half* scales, uint8_t* zeros, float2* rowmm, cudaStream_t st);
 cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                           cudaStream_t st);
 
@@ -85,6 +89,12 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
 // Self-test of the bounded wait: one CTA waits on an mbarrier nothing
 // arrives at; *status receives kDevTimeoutSelfTest after ~limit_ns.
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st);
+
+// ---- deploy (awq_fold.cu)
+// out[i][j] = fp16(fp32(V[i][j]) / s[i]) for V fp16 [rows][cols] (cols = 1:
+// a vector); out may alias V.
+cudaError_t launch_fold(const __half* V, int64_t rows, int64_t cols, const float* s, __half* out,
+                        cudaStream_t st);
 
 // ---- loss reduction (awq_reduce.cu)
 // Number of 256-row chunks of the padded row space (chunk_sums holds

@@ -21,6 +21,7 @@
 // per 16 weights.  Rounding avoids the float-to-int conversion unit (see
 // rne_small).
 #include <algorithm>
+#include <type_traits>
 
 #include "awq_internal.h"
 
@@ -133,15 +134,24 @@ __device__ __forceinline__ float rne_small(float t) {
   return __fsub_rn(__fadd_rn(t, kMagic), kMagic);
 }
 
-// Per-group parameters of the quantizer, from the lane's 16 scaled weights
-// w' = w * s (every lane of the warp calls this; GLANES adjacent lanes form
-// one group).
+// Per-group parameters of the quantizer for the lane's two rows, from the
+// lane's 16 scaled weights w' = w * s of each row.  GROUP 64 or 128: GLANES =
+// GROUP / 16 adjacent lanes form one group and reduce min / max by shuffles
+// (every lane of the warp calls this); the two rows' reductions, shuffles and
+// arithmetic are interleaved (independent chains).  GROUP 0 (one group per
+// row): the row's min / max come precomputed in `rowmm` (k_row_minmax).
+//
+// Asymmetric (zero_point): step = max(max - min, 1e-5) / L, z = clamp(rne(-min
+// * rcp), 0, L).  Symmetric: step = max(max |w'|, 1e-5) / ((L - 1) / 2) and
+// z = (L + 1) / 2, the mid-code.
 //
 // Only one side of the code clamp can ever act (rne is odd-symmetric and
-// fl(x * rcp) is monotone in x): with zu = rne(-min * rcp) <= L, every code
-// rne(w' * rcp) + z is >= 0 and only the upper bound L can be exceeded; with
-// zu > L (z clamped to L, every w' < 0) every code is <= L and only 0 can be
-// undershot.  `low` marks that second case.
+// fl(x * rcp) is monotone in x): asymmetric with zu = rne(-min * rcp) <= L,
+// every code rne(w' * rcp) + z is >= 0 and only the upper bound L can be
+// exceeded; with zu > L (z clamped to L, every w' < 0) every code is <= L and
+// only 0 can be undershot (`low` marks that case).  Symmetric: |w' * rcp| <=
+// (L - 1) / 2 within the fp16 rounding of the step, so no clamp acts; the
+// upper one is kept.
 struct GroupQ {
   float sf;    // float(fp16 scale)
   float rcp;   // fp32 1 / sf
@@ -150,71 +160,60 @@ struct GroupQ {
   __half scale;
 };
 
-template <int GLANES>
-__device__ __forceinline__ GroupQ group_params(const float* ws, float L) {
-  float mnA = fminf(ws[0], ws[1]), mxA = fmaxf(ws[0], ws[1]);
-  float mnB = fminf(ws[2], ws[3]), mxB = fmaxf(ws[2], ws[3]);
-#pragma unroll
-  for (int i = 4; i < kPerLane; i += 4) {
-    mnA = min3f(mnA, ws[i], ws[i + 1]);
-    mxA = max3f(mxA, ws[i], ws[i + 1]);
-    mnB = min3f(mnB, ws[i + 2], ws[i + 3]);
-    mxB = max3f(mxB, ws[i + 2], ws[i + 3]);
-  }
-  float mn = fminf(mnA, mnB), mx = fmaxf(mxA, mxB);
-#pragma unroll
-  for (int off = GLANES / 2; off; off >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  }
-  GroupQ g;
-  const float step = __fdiv_rn(fmaxf(__fsub_rn(mx, mn), 1e-5f), L);
-  g.scale = __float2half_rn(step);
-  g.sf = __half2float(g.scale);
-  g.rcp = __frcp_rn(g.sf);
-  const float zu = rne_small(__fmul_rn(-mn, g.rcp));
-  g.low = zu > L;
-  g.z = fminf(fmaxf(zu, 0.0f), L);
-  return g;
-}
-
-// The same for the lane's two rows at once: the two rows' reductions,
-// shuffles and per-group arithmetic are interleaved (independent chains).
-template <int GLANES>
+template <int GROUP, bool SYM>
 __device__ __forceinline__ void group_params2(const float (&ws)[kRowsPerLane][kPerLane], float L,
-                                              GroupQ (&g)[kRowsPerLane]) {
+                                              const float2* rowmm, GroupQ (&g)[kRowsPerLane]) {
   float mn[kRowsPerLane], mx[kRowsPerLane];
-#pragma unroll
-  for (int r = 0; r < kRowsPerLane; ++r) {
-    float mnA = fminf(ws[r][0], ws[r][1]), mxA = fmaxf(ws[r][0], ws[r][1]);
-    float mnB = fminf(ws[r][2], ws[r][3]), mxB = fmaxf(ws[r][2], ws[r][3]);
-#pragma unroll
-    for (int i = 4; i < kPerLane; i += 4) {
-      mnA = min3f(mnA, ws[r][i], ws[r][i + 1]);
-      mxA = max3f(mxA, ws[r][i], ws[r][i + 1]);
-      mnB = min3f(mnB, ws[r][i + 2], ws[r][i + 3]);
-      mxB = max3f(mxB, ws[r][i + 2], ws[r][i + 3]);
-    }
-    mn[r] = fminf(mnA, mnB);
-    mx[r] = fmaxf(mxA, mxB);
-  }
-#pragma unroll
-  for (int off = GLANES / 2; off; off >>= 1) {
+  if constexpr (GROUP == 0) {
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r) {
-      mn[r] = fminf(mn[r], __shfl_xor_sync(0xFFFFFFFFu, mn[r], off));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], off));
+      mn[r] = rowmm[r].x;
+      mx[r] = rowmm[r].y;
+    }
+  } else {
+    constexpr int GLANES = GROUP / kPerLane;
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      float mnA = fminf(ws[r][0], ws[r][1]), mxA = fmaxf(ws[r][0], ws[r][1]);
+      float mnB = fminf(ws[r][2], ws[r][3]), mxB = fmaxf(ws[r][2], ws[r][3]);
+#pragma unroll
+      for (int i = 4; i < kPerLane; i += 4) {
+        mnA = min3f(mnA, ws[r][i], ws[r][i + 1]);
+        mxA = max3f(mxA, ws[r][i], ws[r][i + 1]);
+        mnB = min3f(mnB, ws[r][i + 2], ws[r][i + 3]);
+        mxB = max3f(mxB, ws[r][i + 2], ws[r][i + 3]);
+      }
+      mn[r] = fminf(mnA, mnB);
+      mx[r] = fmaxf(mxA, mxB);
+    }
+#pragma unroll
+    for (int off = GLANES / 2; off; off >>= 1) {
+#pragma unroll
+      for (int r = 0; r < kRowsPerLane; ++r) {
+        mn[r] = fminf(mn[r], __shfl_xor_sync(0xFFFFFFFFu, mn[r], off));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], off));
+      }
     }
   }
 #pragma unroll
   for (int r = 0; r < kRowsPerLane; ++r) {
-    const float step = __fdiv_rn(fmaxf(__fsub_rn(mx[r], mn[r]), 1e-5f), L);
-    g[r].scale = __float2half_rn(step);
-    g[r].sf = __half2float(g[r].scale);
-    g[r].rcp = __frcp_rn(g[r].sf);
-    const float zu = rne_small(__fmul_rn(-mn[r], g[r].rcp));
-    g[r].low = zu > L;
-    g[r].z = fminf(fmaxf(zu, 0.0f), L);
+    if constexpr (SYM) {
+      const float half_levels = 0.5f * (L - 1.0f);   // 7 or 3, exact
+      const float step = __fdiv_rn(fmaxf(fmaxf(-mn[r], mx[r]), 1e-5f), half_levels);
+      g[r].scale = __float2half_rn(step);
+      g[r].sf = __half2float(g[r].scale);
+      g[r].rcp = __frcp_rn(g[r].sf);
+      g[r].low = false;
+      g[r].z = 0.5f * (L + 1.0f);                      // 8 or 4, exact
+    } else {
+      const float step = __fdiv_rn(fmaxf(__fsub_rn(mx[r], mn[r]), 1e-5f), L);
+      g[r].scale = __float2half_rn(step);
+      g[r].sf = __half2float(g[r].scale);
+      g[r].rcp = __frcp_rn(g[r].sf);
+      const float zu = rne_small(__fmul_rn(-mn[r], g[r].rcp));
+      g[r].low = zu > L;
+      g[r].z = fminf(fmaxf(zu, 0.0f), L);
+    }
   }
 }
 
@@ -269,12 +268,12 @@ __device__ __forceinline__ Lane lane_chunk(int64_t K) {
 // a block take 16 consecutive rows at the same channels, so their 256-bit
 // loads of s and 1/s hit the same L1 lines.  Each lane writes one whole
 // 32-byte sector per row and grid point.
-template <int GROUP>
+template <int GROUP, bool SYM>
 __global__ void __launch_bounds__(kQuantThreads)
     k_quant_residual(const __half* __restrict__ W, int64_t N, int64_t K, int levels,
                      const float* __restrict__ s_grid, const float* __restrict__ r_grid,
-                     int n_alpha, int64_t row_off, int64_t n_pad, __half* __restrict__ delta) {
-  constexpr int GLANES = GROUP / kPerLane;
+                     int n_alpha, int64_t row_off, int64_t n_pad, __half* __restrict__ delta,
+                     const float2* __restrict__ rowmm) {
   const float L = static_cast<float>(levels);
   const int64_t slab = n_pad * K;                     // halves per grid point
   const Lane lw = lane_chunk(K);
@@ -297,8 +296,14 @@ __global__ void __launch_bounds__(kQuantThreads)
       float ws[kRowsPerLane][kPerLane];
 #pragma unroll
       for (int r = 0; r < kRowsPerLane; ++r) scale16(w[r], sv, ws[r]);
+      float2 mm[kRowsPerLane];
+      if constexpr (GROUP == 0) {   // per-row groups: min / max of this grid point's rows
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r)
+          mm[r] = rowmm[static_cast<int64_t>(a) * N + min(row0 + r, N - 1)];
+      }
       GroupQ gq[kRowsPerLane];
-      group_params2<GLANES>(ws, L, gq);
+      group_params2<GROUP, SYM>(ws, L, mm, gq);
       // rare: some group of the warp is all negative (both clamp sides needed)
       const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
 #pragma unroll
@@ -349,16 +354,15 @@ __global__ void __launch_bounds__(kQuantThreads)
 // difference of the bit patterns of m and M - z (consecutive integers in
 // [2^23, 2^24) have consecutive patterns).  codes8: the code words are
 // 8-byte aligned (INT4 only), so a lane stores its two words at once.
-template <int BITS, int GROUP, bool A32>
+template <int BITS, int GROUP, bool SYM, bool A32>
 __global__ void __launch_bounds__(kQuantThreads)
     k_quant_final(const __half* __restrict__ W, int64_t N, int64_t K,
                   const float* __restrict__ s_base, const int* __restrict__ sel,
                   uint32_t* __restrict__ codes, __half* __restrict__ scales,
-                  uint8_t* __restrict__ zeros, bool codes8) {
-  constexpr int GLANES = GROUP / kPerLane;
+                  uint8_t* __restrict__ zeros, bool codes8, const float2* __restrict__ rowmm) {
   constexpr int LEVELS = (1 << BITS) - 1;
   const float L = static_cast<float>(LEVELS);
-  const int64_t groups = K / GROUP;
+  const int64_t groups = GROUP == 0 ? 1 : K / (GROUP == 0 ? 1 : GROUP);
   const int64_t words = BITS == 4 ? K / 8 : 3 * K / 32;
   const float* s = s_base + (sel ? static_cast<int64_t>(*sel) * K : 0);
   const int lane = threadIdx.x & 31;
@@ -400,8 +404,13 @@ __global__ void __launch_bounds__(kQuantThreads)
       raw_to_f32(raw[r], w);
       scale16(w, sv, ws[r]);
     }
+    float2 mm[kRowsPerLane];
+    if constexpr (GROUP == 0) {   // per-row groups: precomputed min / max
+#pragma unroll
+      for (int r = 0; r < kRowsPerLane; ++r) mm[r] = rowmm[min(row0 + r, N - 1)];
+    }
     GroupQ gq[kRowsPerLane];
-    group_params2<GLANES>(ws, L, gq);
+    group_params2<GROUP, SYM>(ws, L, mm, gq);
     // rare: some group of the warp is all negative (both clamp sides needed)
     const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
 #pragma unroll
@@ -475,11 +484,72 @@ __global__ void __launch_bounds__(kQuantThreads)
           }
         }
       }
-      if (store && (lane % GLANES) == 0) {
-        const int64_t gi = row * groups + lw.k0 / GROUP;
+      bool group_lead;
+      int64_t gi;
+      if constexpr (GROUP == 0) {
+        group_lead = lw.lc == 0;
+        gi = row;
+      } else {
+        group_lead = (lane % (GROUP / kPerLane)) == 0;
+        gi = row * groups + lw.k0 / GROUP;
+      }
+      if (store && group_lead) {
         scales[gi] = g.scale;
         zeros[gi] = static_cast<uint8_t>(__float2uint_rn(g.z));
       }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- per-row groups
+// group_size -1: the min / max of w' = w * s over each row's K channels,
+// rowmm[a][n] = {min, max} for grid point a -- or, with `sel`, for the one
+// grid point *sel, stored at a = 0.  Block = one row (grid-stride over rows);
+// 16-byte loads of W and s.  Min and max are exact, so the order of the
+// reduction does not matter.
+__global__ void __launch_bounds__(256)
+    k_row_minmax(const __half* __restrict__ W, int64_t N, int64_t K,
+                 const float* __restrict__ s_grid, const int* __restrict__ sel, int n_alpha,
+                 float2* __restrict__ rowmm) {
+  __shared__ float smn[8], smx[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const uint4* wr = reinterpret_cast<const uint4*>(W + row * K);
+    for (int a = 0; a < n_alpha; ++a) {
+      const float* s = s_grid + static_cast<int64_t>(sel ? *sel : a) * K;
+      float mn = INFINITY, mx = -INFINITY;
+      for (int64_t c = threadIdx.x; c < K / 8; c += blockDim.x) {
+        const uint4 q = __ldg(wr + c);
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(s + 8 * c));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(s + 8 * c) + 1);
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+          const float w0 = __fmul_rn(f.x, sv[2 * i]), w1 = __fmul_rn(f.y, sv[2 * i + 1]);
+          mn = min3f(mn, w0, w1);
+          mx = max3f(mx, w0, w1);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+      }
+      if (lane == 0) {
+        smn[warp] = mn;
+        smx[warp] = mx;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w) {
+          mn = fminf(mn, smn[w]);
+          mx = fmaxf(mx, smx[w]);
+        }
+        rowmm[static_cast<int64_t>(a) * N + row] = make_float2(mn, mx);
+      }
+      __syncthreads();
     }
   }
 }
@@ -508,49 +578,91 @@ dim3 quant_grid(int64_t N, int64_t K) {
   return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(std::max<int64_t>(gy, 1)));
 }
 
-template <int BITS, int GROUP>
+template <int BITS, int GROUP, bool SYM>
 cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, const int* sel,
-                         uint32_t* codes, __half* scales, uint8_t* zeros, cudaStream_t st) {
+                         uint32_t* codes, __half* scales, uint8_t* zeros, const float2* rowmm,
+                         cudaStream_t st) {
   const bool c8 = (reinterpret_cast<uintptr_t>(codes) % 8) == 0;
   const bool a32 = (reinterpret_cast<uintptr_t>(W) % 32) == 0 &&
                    (reinterpret_cast<uintptr_t>(s) % 32) == 0;
   const dim3 grid = quant_grid(N, K);
   if (a32)
-    k_quant_final<BITS, GROUP, true><<<grid, kQuantThreads, 0, st>>>(W, N, K, s, sel, codes,
-                                                                     scales, zeros, c8);
+    k_quant_final<BITS, GROUP, SYM, true><<<grid, kQuantThreads, 0, st>>>(
+        W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
   else
-    k_quant_final<BITS, GROUP, false><<<grid, kQuantThreads, 0, st>>>(W, N, K, s, sel, codes,
-                                                                      scales, zeros, c8);
+    k_quant_final<BITS, GROUP, SYM, false><<<grid, kQuantThreads, 0, st>>>(
+        W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
   return cudaGetLastError();
+}
+
+template <int BITS, bool SYM>
+cudaError_t launch_final_g(int group, const __half* W, int64_t N, int64_t K, const float* s,
+                           const int* sel, uint32_t* codes, __half* scales, uint8_t* zeros,
+                           const float2* rowmm, cudaStream_t st) {
+  if (group == 128)
+    return launch_final<BITS, 128, SYM>(W, N, K, s, sel, codes, scales, zeros, rowmm, st);
+  if (group == 64)
+    return launch_final<BITS, 64, SYM>(W, N, K, s, sel, codes, scales, zeros, rowmm, st);
+  return launch_final<BITS, 0, SYM>(W, N, K, s, sel, codes, scales, zeros, rowmm, st);
+}
+
+cudaError_t launch_row_minmax(const __half* W, int64_t N, int64_t K, const float* s_grid,
+                              const int* sel, int n_alpha, float2* rowmm, cudaStream_t st) {
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(N, 148 * 8));
+  k_row_minmax<<<grid, 256, 0, st>>>(W, N, K, s_grid, sel, n_alpha, rowmm);
+  return cudaGetLastError();
+}
+
+template <int GROUP, bool SYM>
+void launch_residual_t(dim3 grid, cudaStream_t st, const __half* W, int64_t N, int64_t K,
+                       int levels, const float* s_grid, const float* r_grid, int n_alpha,
+                       int64_t row_off, int64_t n_pad, __half* delta, const float2* rowmm) {
+  k_quant_residual<GROUP, SYM><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
+                                                               n_alpha, row_off, n_pad, delta,
+                                                               rowmm);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bits, int group,
-                                  const float* s_grid, const float* r_grid, int n_alpha,
-                                  int64_t row_off, int64_t n_pad, __half* delta,
-                                  cudaStream_t st) {
+                                  int zero_point, const float* s_grid, const float* r_grid,
+                                  int n_alpha, int64_t row_off, int64_t n_pad, __half* delta,
+                                  float2* rowmm, cudaStream_t st) {
   const int levels = (1 << bits) - 1;
   const dim3 grid = quant_grid(N, K);
-  if (group == 128)
-    k_quant_residual<128><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
-                                                          n_alpha, row_off, n_pad, delta);
-  else
-    k_quant_residual<64><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
-                                                         n_alpha, row_off, n_pad, delta);
+  const bool sym = zero_point == 0;
+  if (group == -1) {
+    cudaError_t e = launch_row_minmax(W, N, K, s_grid, nullptr, n_alpha, rowmm, st);
+    if (e != cudaSuccess) return e;
+  }
+  auto go = [&](auto g, auto y) {
+    launch_residual_t<decltype(g)::value, decltype(y)::value>(
+        grid, st, W, N, K, levels, s_grid, r_grid, n_alpha, row_off, n_pad, delta, rowmm);
+  };
+  using I128 = std::integral_constant<int, 128>;
+  using I64 = std::integral_constant<int, 64>;
+  using I0 = std::integral_constant<int, 0>;
+  using T = std::true_type;
+  using F = std::false_type;
+  if (group == 128) sym ? go(I128{}, T{}) : go(I128{}, F{});
+  else if (group == 64) sym ? go(I64{}, T{}) : go(I64{}, F{});
+  else sym ? go(I0{}, T{}) : go(I0{}, F{});
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, int group,
-                               const float* s, const int* sel, uint32_t* codes,
-                               __half* scales, uint8_t* zeros, cudaStream_t st) {
-  if (bits == 4 && group == 128)
-    return launch_final<4, 128>(W, N, K, s, sel, codes, scales, zeros, st);
-  if (bits == 4 && group == 64)
-    return launch_final<4, 64>(W, N, K, s, sel, codes, scales, zeros, st);
-  if (bits == 3 && group == 128)
-    return launch_final<3, 128>(W, N, K, s, sel, codes, scales, zeros, st);
-  return launch_final<3, 64>(W, N, K, s, sel, codes, scales, zeros, st);
+                               int zero_point, const float* s, const int* sel, uint32_t* codes,
+                               __half* scales, uint8_t* zeros, float2* rowmm, cudaStream_t st) {
+  if (group == -1) {
+    cudaError_t e = launch_row_minmax(W, N, K, s, sel, 1, rowmm, st);
+    if (e != cudaSuccess) return e;
+  }
+  const bool sym = zero_point == 0;
+  if (bits == 4)
+    return sym ? launch_final_g<4, true>(group, W, N, K, s, sel, codes, scales, zeros, rowmm, st)
+               : launch_final_g<4, false>(group, W, N, K, s, sel, codes, scales, zeros, rowmm, st);
+  return sym ? launch_final_g<3, true>(group, W, N, K, s, sel, codes, scales, zeros, rowmm, st)
+             : launch_final_g<3, false>(group, W, N, K, s, sel, codes, scales, zeros, rowmm, st);
 }
 
 cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,

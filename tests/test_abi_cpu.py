@@ -76,13 +76,22 @@ def test_invalid_arguments_rejected_before_launch(L):
     assert L.awq_scales(None, 64, 65, None, None) == INVALID
     assert L.awq_quantize_pack(None, 4, 256, None, _cfg(bits=5), None, None, None, None) == UNSUPPORTED
     assert L.awq_quantize_pack(None, 4, 256, None, _cfg(group=32), None, None, None, None) == UNSUPPORTED
-    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(zp=0), None, None, None, None) == UNSUPPORTED
+    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(zp=2), None, None, None, None) == UNSUPPORTED
+    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(group=-2), None, None, None, None) == UNSUPPORTED
+    # one group per row needs K % 64 == 0; symmetric and per-row are accepted
+    assert L.awq_quantize_pack(None, 4, 96, None, _cfg(group=-1), None, None, None, None) == INVALID
+    assert L.awq_quantize_pack(None, 4, 256, None, _cfg(group=-1, zp=0), None, None, None,
+                               None) == INVALID        # NULL W: reaches the pointer checks
     assert L.awq_quantize_pack(None, 4, 200, None, _cfg(), None, None, None, None) == INVALID
     assert L.awq_quantize_pack(None, 4, 256, None, None, None, None, None, None) == INVALID
     # N = 0 is a valid no-op and touches no pointer.
     assert L.awq_quantize_pack(None, 0, 256, None, _cfg(), None, None, None, None) == 0
     assert L.awq_unpack_codes(None, 2, 100, 4, None, None) == INVALID
     assert L.awq_reference_output(None, 4, None, 4, 100, None, None, None) == INVALID
+    assert L.awq_fold_scale(None, 0, 8, None, None, None) == INVALID
+    assert L.awq_fold_scale(None, 8, 0, None, None, None) == INVALID
+    assert L.awq_fold_scale(None, 8, 8, None, None, None) == INVALID
+    assert b"V" in L.awq_last_error()
     out = ctypes.c_void_p()
     w = (awq.Weight * 1)()
     assert L.awq_search_layer(None, 16, 256, None, w, 1, _cfg(), None, None) == INVALID
@@ -102,6 +111,9 @@ def test_host_pointer_rejected(L):
     buf = (ctypes.c_char * 4096)()
     sx = (ctypes.c_double * 64)()
     st = L.awq_stats(ctypes.addressof(buf), 16, 64, ctypes.addressof(sx), None)
+    assert st == awq.AWQ_ERR_INVALID
+    st = L.awq_fold_scale(ctypes.addressof(buf), 64, 1, ctypes.addressof(sx),
+                          ctypes.addressof(buf), None)
     assert st == awq.AWQ_ERR_INVALID
 
 

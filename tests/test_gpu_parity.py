@@ -91,15 +91,19 @@ def test_scales_match_oracle(K):
 # --------------------------------------------------------------------------
 # Quantize + pack: bit-exact.
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("bits,group", [(4, 128), (4, 64), (3, 128), (3, 64)])
+@pytest.mark.parametrize("zp", [True, False], ids=["asym", "sym"])
+@pytest.mark.parametrize("bits,group", [(4, 128), (4, 64), (3, 128), (3, 64), (4, -1), (3, -1)])
 @pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (300, 1024), (129, 4096)])
-def test_quantize_pack_bit_exact(bits, group, N, K):
-    rng = workloads.weight_rng(N * 31 + K + bits * 7 + group)
+def test_quantize_pack_bit_exact(bits, group, N, K, zp):
+    rng = workloads.weight_rng(N * 31 + K + bits * 7 + group + 3 * zp)
     W = (rng.standard_t(4, (N, K)) * 0.02).astype(np.float16)
-    W[0, :group] = 0                                   # a constant (all-zero) group
+    W[0, :(K if group == -1 else group)] = 0          # a constant (all-zero) group
+    if N > 2:
+        W[1, :64] = np.abs(W[1, :64]) + np.float16(0.01)    # an all-positive stretch
+        W[2] = -np.abs(W[2]) - np.float16(0.01)             # an all-negative row
     s = np.exp(rng.uniform(-1.5, 1.5, K)).astype(np.float32)
-    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group)
-    oc, osc, oz = O.quantize_groups(W, s, bits, group)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group, zero_point=zp)
+    oc, osc, oz = O.quantize_groups(W, s, bits, group, zero_point=zp)
     assert np.array_equal(words_u32(codes).reshape(N, -1), O.pack_codes(oc, bits))
     assert np.array_equal(host(sc).view(np.uint16), osc.view(np.uint16))
     assert np.array_equal(host(z), oz)
@@ -119,6 +123,55 @@ def test_unpack_roundtrip(bits):
     packed = O.pack_codes(q, bits).reshape(-1).view(np.int32)
     got = host(awq.unpack_codes(cuda(packed), 37, 512, bits))
     assert np.array_equal(got, q)
+
+
+# --------------------------------------------------------------------------
+# Deploy: fold diag(s)^-1 into the producer of the layer's input: bit-exact.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(1,), (4096,), (11008,), (64, 256), (300, 13), (7, 8200)])
+def test_fold_bit_exact(shape):
+    rng = workloads.weight_rng(sum(shape) + len(shape))
+    V = (rng.standard_normal(shape) * rng.uniform(0.01, 10)).astype(np.float16)
+    s = np.exp(rng.uniform(-4, 4, shape[0])).astype(np.float32)
+    got = host(awq.fold_scale(cuda(V), cuda(s)))
+    assert np.array_equal(got.view(np.uint16), O.fold_inverse_scale(V, s).view(np.uint16))
+
+
+def test_fold_in_place_and_misaligned():
+    rng = workloads.weight_rng(5150)
+    V = rng.standard_normal((33, 24)).astype(np.float16)
+    s = np.exp(rng.uniform(-2, 2, 33)).astype(np.float32)
+    want = O.fold_inverse_scale(V, s)
+    t = cuda(V)
+    awq.fold_scale(t, cuda(s), out=t)                    # in place
+    assert np.array_equal(host(t).view(np.uint16), want.view(np.uint16))
+    # a 2-byte offset view: not 16-byte aligned, takes the scalar path
+    flat = cuda(np.concatenate([np.zeros(1, np.float16), V.reshape(-1)]))
+    Vm = flat[1:].view(33, 24)
+    got = host(awq.fold_scale(Vm, cuda(s)))
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+def test_fold_after_search_keeps_layer_output():
+    """A norm weight folded with the chosen s, the quantized layer at that s:
+    deq(Q(W diag(s))) applied to the folded activations approximates W x,
+    and equals the search's own error path (W - deq/s) x within rounding."""
+    t = workloads.generate("tiny")
+    W, X = t["W"], t["X"]
+    res = awq.search(cuda(X), [cuda(W)], 4, 128, 20)
+    res.check()
+    s = host(res.s())
+    gamma = workloads.weight_rng(7).uniform(0.5, 1.5, W.shape[1]).astype(np.float16)
+    g2 = host(awq.fold_scale(cuda(gamma), cuda(s)))
+    assert np.array_equal(g2.view(np.uint16), O.fold_inverse_scale(gamma, s).view(np.uint16))
+    codes = O.unpack_codes(words_u32(res.codes()).reshape(W.shape[0], -1), 4, W.shape[1])
+    deq = O.dequantize_scaled(codes, host(res.scales()), host(res.zeros()), 128)
+    x = X.astype(np.float64)
+    y_ref = W.astype(np.float64) @ (gamma.astype(np.float64) * x).T
+    y_dep = deq @ (g2.astype(np.float64) * x).T
+    rel = np.linalg.norm(y_dep - y_ref) / np.linalg.norm(y_ref)
+    assert rel < 0.2            # INT4 g128: a few percent of the output norm
+    res.free()
 
 
 # --------------------------------------------------------------------------
@@ -151,10 +204,10 @@ def _argmin_ok(gpu_best, oracle_losses):
     return close and gpu_best in (order[0], order[1])
 
 
-def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=2e-3):
-    res = awq.search(cuda(X), [cuda(W) for W in Ws], bits, group, n_grid)
+def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=2e-3, zero_point=True):
+    res = awq.search(cuda(X), [cuda(W) for W in Ws], bits, group, n_grid, zero_point=zero_point)
     res.check()
-    ref = O.search(X, Ws, bits, group, n_grid)
+    ref = O.search(X, Ws, bits, group, n_grid, zero_point=zero_point)
     losses = res.losses
     np.testing.assert_allclose(losses, ref["losses"], rtol=LOSS_RTOL, atol=0)
     assert _argmin_ok(res.best, ref["losses"]), (res.best, ref["losses"])
@@ -172,7 +225,7 @@ def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=2e-3):
                                    atol=1e-12 * max(1.0, float(ref["row_losses"][i].max())))
         off += n
         # codes at the GPU's alpha, bit-exact against the oracle quantizer fed the GPU's s
-        oc, osc, oz = O.quantize_groups(W, s_best, bits, group)
+        oc, osc, oz = O.quantize_groups(W, s_best, bits, group, zero_point)
         assert np.array_equal(words_u32(res.codes(i)).reshape(n, -1), O.pack_codes(oc, bits))
         assert np.array_equal(host(res.scales(i)).view(np.uint16), osc.view(np.uint16))
         assert np.array_equal(host(res.zeros(i)), oz)
@@ -193,6 +246,27 @@ def test_search_tiny_workload():
     t = workloads.generate("tiny")
     ref = _compare_search(t["X"], [t["W"]], 4, 128)
     assert ref["best"] > 0
+
+
+@pytest.mark.parametrize("bits,group,zp", [(4, 128, False), (4, -1, True), (4, -1, False),
+                                          (3, 64, False), (3, -1, True)],
+                         ids=lambda v: str(v))
+def test_search_quantizer_modes_tiny(bits, group, zp):
+    """The AwqConfig knobs beyond the default: symmetric (zero_point false)
+    and one group per output row (group_size -1)."""
+    t = workloads.generate("tiny")
+    _compare_search(t["X"], [t["W"]], bits, group, zero_point=zp)
+
+
+def test_search_per_row_two_weights_ragged():
+    Ws = []
+    X = None
+    for j, n in enumerate((130, 60)):
+        W, X0 = workloads.random_layer(n, 256, 77, seed=300 + j, outliers=(3, 200), factor=30.0)
+        Ws.append(W)
+        X = X0 if X is None else X
+    _compare_search(X, Ws, 4, -1, zero_point=False)
+    _compare_search(X, Ws, 3, -1, zero_point=True)
 
 
 @pytest.mark.parametrize("case", [
@@ -252,6 +326,23 @@ def test_search_given_sx_and_small_grid():
     res.check()
     ref = O.search(X, [W], 4, 128, n_grid=5, sX=sX)
     np.testing.assert_allclose(res.losses, ref["losses"], rtol=LOSS_RTOL)
+    res.free()
+
+
+def test_search_weight_magnitude_ablation():
+    """Weight-magnitude saliency (the pages' ablation): the statistic entry
+    point applied to W gives the mean |W| of each input channel, which the
+    search takes in place of the activation statistic."""
+    t = workloads.generate("tiny")
+    W, X = cuda(t["W"]), cuda(t["X"])
+    sxw = awq.stats(W)
+    want_sx = O.channel_magnitude(t["W"])
+    assert np.array_equal(host(sxw), want_sx)
+    res = awq.search(X, [W], 4, 128, 20, sX=sxw)
+    res.check()
+    ref = O.search(t["X"], [t["W"]], 4, 128, 20, sX=want_sx)
+    np.testing.assert_allclose(res.losses, ref["losses"], rtol=LOSS_RTOL, atol=0)
+    assert _argmin_ok(res.best, ref["losses"])
     res.free()
 
 

@@ -37,6 +37,16 @@ def test_quantizer_hand_examples(case):
     assert int(zeros[0, 0]) == case["zero"]
 
 
+@pytest.mark.parametrize("case", golden()["quantizer_symmetric"], ids=lambda c: c["name"])
+def test_symmetric_quantizer_hand_examples(case):
+    w = np.array(case["w"], np.float16)[None, :]
+    codes, sc, z = O.quantize_groups(w, np.array(case["s"], np.float32), case["bits"],
+                                     case["group"], zero_point=False)
+    assert codes[0].tolist() == case["codes"]
+    assert int(sc.view(np.uint16)[0, 0]) == case["scale_fp16_bits"]
+    assert int(z[0, 0]) == case["zero"]
+
+
 @pytest.mark.parametrize("case", golden()["packing"], ids=lambda c: c["name"])
 def test_packing_hand_examples(case):
     codes = np.array([case["codes"]], np.uint8)
@@ -69,6 +79,12 @@ def test_loss_hand_examples(case):
 # --------------------------------------------------------------------------
 # Statistic and scale: closed forms
 # --------------------------------------------------------------------------
+@pytest.mark.parametrize("case", golden()["fold"], ids=lambda c: c["name"])
+def test_fold_hand_examples(case):
+    out = O.fold_inverse_scale(np.array(case["V"], np.float16), np.array(case["s"], np.float32))
+    assert out.view(np.uint16).tolist() == case["out_fp16_bits"]
+
+
 def test_statistic_constant_columns_and_order_independence():
     rng = workloads.weight_rng(1)
     c = rng.standard_normal(16).astype(np.float16)
@@ -367,6 +383,114 @@ def test_activation_aware_scaling_helps_on_tiny_workload():
     res = O.search(t["X"], [t["W"]], 4, 128, n_grid=20)
     assert res["best"] > 0
     assert res["losses"][res["best"]] < 0.9 * res["losses"][0]
+
+
+def test_weight_magnitude_saliency_does_worse():
+    """The pages' ablation (AWQ explained, "Salient weights are
+    activation-aware"; AWQ Explained, multigrid.ai, "Why the activations
+    pick, not the weights"): picking the scale by weight magnitude does worse
+    than by activation magnitude.  With s built from the mean |W| of each
+    input channel, the best loss on the tiny workload (whose salient channels
+    come from the activations) stays above the activation-aware best."""
+    t = workloads.generate("tiny")
+    act = O.search(t["X"], [t["W"]], 4, 128, n_grid=20)
+    wmag = O.search(t["X"], [t["W"]], 4, 128, n_grid=20,
+                    sX=O.channel_magnitude(t["W"]))
+    assert wmag["losses"].min() > 1.05 * act["losses"].min()
+
+
+def test_fold_keeps_the_layer_output():
+    """AWQ Explained (multigrid.ai), "Scaling instead of mixed precision": with
+    diag(s)^-1 folded into the producer of x, the scaled layer W diag(s)
+    computes the same output.  With power-of-two s every step is exact, so
+    the identity holds bit for bit in fp64, for a norm weight and for a
+    preceding linear layer."""
+    rng = workloads.weight_rng(91)
+    K, M, N = 64, 48, 16
+    s = (2.0 ** rng.integers(-3, 4, K)).astype(np.float32)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16).astype(np.float64)
+    gamma = rng.uniform(0.5, 2.0, K).astype(np.float16)
+    h = rng.standard_normal(K)
+    y = W @ (gamma.astype(np.float64) * h)
+    g2 = O.fold_inverse_scale(gamma, s).astype(np.float64)
+    assert np.array_equal((W * s.astype(np.float64)) @ (g2 * h), y)
+    P = (rng.standard_normal((K, M)) * 0.1).astype(np.float16)
+    u = rng.standard_normal(M)
+    y2 = W @ (P.astype(np.float64) @ u)
+    P2 = O.fold_inverse_scale(P, s).astype(np.float64)
+    np.testing.assert_allclose((W * s.astype(np.float64)) @ (P2 @ u), y2, rtol=1e-12, atol=1e-15)
+
+
+def test_fold_rounds_once_to_fp16():
+    rng = workloads.weight_rng(92)
+    V = rng.standard_normal((37, 5)).astype(np.float16)
+    s = np.exp(rng.uniform(-2, 2, 37)).astype(np.float32)
+    out = O.fold_inverse_scale(V, s)
+    exact = V.astype(np.float64) / s.astype(np.float64)[:, None]
+    # within half an fp16 ulp (plus the fp32 rounding before it)
+    ulp = np.spacing(np.abs(out).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= 0.5 * ulp + np.abs(exact) * 2.0 ** -24)
+    with pytest.raises(ValueError):
+        O.fold_inverse_scale(V, s[:-1])
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_symmetric_alpha_zero_is_plain_absmax_rtn(bits):
+    """alpha = 0 (s == 1), zero_point false: a separately written symmetric
+    round-to-nearest by the group's maximum magnitude, loop by loop."""
+    rng = workloads.weight_rng(70 + bits)
+    W = (rng.standard_t(4, (6, 256)) * 0.02).astype(np.float16)
+    codes, sc, z = O.quantize_groups(W, np.ones(256, np.float32), bits, 64, zero_point=False)
+    half = 1 << (bits - 1)
+    for n in range(6):
+        for g in range(4):
+            blk = W[n, 64 * g:64 * g + 64].astype(np.float32)
+            amax = max(float(np.max(np.abs(blk))), 1e-5)
+            step = np.float16(np.float32(amax) / np.float32(half - 1))
+            r = np.float32(1) / np.float32(step)
+            assert sc[n, g] == step and z[n, g] == half
+            for j in range(64):
+                q = int(np.rint(np.float32(blk[j] * r))) + half
+                assert codes[n, 64 * g + j] == min(max(q, 0), 2 * half - 1)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_symmetric_codes_nearest_level(bits):
+    rng = workloads.weight_rng(80 + bits)
+    W = (rng.standard_normal((5, 128)) * 0.05).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, 128)).astype(np.float32)
+    codes, sc, z = O.quantize_groups(W, s, bits, 128, zero_point=False)
+    assert codes.max() <= (1 << bits) - 1 and np.all(z == 1 << (bits - 1))
+    ws = W.astype(np.float32) * s
+    levels = (np.arange(1 << bits)[None, :] - (1 << (bits - 1))) * sc.astype(np.float64)
+    for n in range(5):
+        d = np.abs(ws[n][:, None].astype(np.float64) - levels[n][None, :])
+        best = d.min(axis=1)
+        got = d[np.arange(128), codes[n]]
+        assert np.all(got <= best + 1e-6 * sc[n, 0])
+
+
+def test_per_row_group_is_one_group_of_k():
+    rng = workloads.weight_rng(88)
+    W = (rng.standard_normal((9, 512)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, 512)).astype(np.float32)
+    for zp in (True, False):
+        a = O.quantize_groups(W, s, 4, -1, zero_point=zp)
+        b = O.quantize_groups(W, s, 4, 512, zero_point=zp)
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+        assert a[1].shape == (9, 1)
+
+
+@pytest.mark.parametrize("k", [-2, 3])
+def test_symmetric_homogeneity_power_of_two(k):
+    rng = workloads.weight_rng(89)
+    W = (rng.standard_normal((4, 256)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, 256)).astype(np.float32)
+    c1, s1, z1 = O.quantize_groups(W, s, 4, 128, zero_point=False)
+    c2, s2, z2 = O.quantize_groups(W, s * np.float32(2.0 ** k), 4, 128, zero_point=False)
+    assert np.array_equal(c1, c2) and np.array_equal(z1, z2)
+    assert np.array_equal(s2.astype(np.float64), s1.astype(np.float64) * 2.0 ** k)
 
 
 @pytest.mark.parametrize("bits", [3, 4])
