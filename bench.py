@@ -452,16 +452,21 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     achieved = flops_per_launch / (gemm_avg_ms / 1e3) / 1e12
     ideal_s = max(wl.gemm_flops(N_GRID) / (pk["tflops"] * 1e12),
                   algorithmic_bytes(wl) / (pk["hbm_gbs"] * 1e9))
+    # The GEMM runs inside the step: the burst peak for a short timed region,
+    # the sustained (power-capped, seconds-long) peak for a long one.
+    long_run = total_ms > 2000.0
+    gemm_peak = pk["tflops_sustained"] if long_run else pk["tflops"]
+    peak_kind = "sustained" if long_run else "burst"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic", "config": config_for(args.workload),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / pk["tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": gemm_peak,
+                     "unit": "TFLOP/s", "frac": achieved / gemm_peak,
                      "traffic": profiled_traffic(),
                      "kernel": "k_gemm_err_pair (tcgen05 cta_group::2 error GEMM), fp16 operands, f32 accumulate",
-                     "peak_source": f"{pk['source']} bf16 burst (dense fp16 taken equal)",
+                     "peak_source": f"{pk['source']} bf16 {peak_kind} (dense fp16 taken equal)",
                      "launch_ms": gemm_avg_ms},
         "step_roofline": {"ideal_ms": ideal_s * 1e3, "frac": ideal_s * 1e3 / (total_ms / args.steps)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
