@@ -304,6 +304,18 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     nbytes = 2 * N * K + N * K // 2 + 3 * N * K // 128
     out["quantize_pack"] = {"shape": f"W {N}x{K} fp16 -> INT4 g128", "ms": ms, "bytes": nbytes,
                             "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
+    # The packed layer consumed at decode: W4A16 product for one token, and a
+    # cuBLAS fp16 GEMV on the dense weight of the same shape for context.
+    x = torch.randn(1, K, generator=g, device=dev).half()
+    y = torch.empty(1, N, dtype=torch.float32, device=dev)
+    ms = timed(lambda: awq._check(L.awq_w4a16_matvec(
+        codes.data_ptr(), sc.data_ptr(), z.data_ptr(), N, K, ctypes.byref(cfg), x.data_ptr(), 1,
+        y.data_ptr(), st)))
+    nbytes = N * K // 2 + 3 * N * K // 128 + 2 * K + 4 * N
+    dense_ms = timed(lambda: torch.matmul(x, W.t()))
+    out["w4a16_matvec"] = {"shape": f"W {N}x{K} INT4 g128, 1 token", "ms": ms, "bytes": nbytes,
+                           "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs,
+                           "fp16_cublas_gemv_ms": dense_ms, "speedup_vs_fp16": dense_ms / ms}
     del W
     return out
 

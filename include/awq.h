@@ -172,6 +172,28 @@ awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bit
 awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float* s, void* out,
                           void* stream);
 
+/* W4A16 decode product with a packed layer ("AWQ explained",
+ * "Why weight-only quantization fits decoding": at small batch each token
+ * reads every weight once, so 4-bit weights with 16-bit activations cut the
+ * dominant traffic about four times).
+ *   codes  : device uint32 [N][K/8], INT4 codes as written by the search or
+ *            awq_quantize_pack (cfg->bits must be 4, else AWQ_ERR_UNSUPPORTED).
+ *   scales : device fp16 [N][K/group] ([N][1] for group_size -1).
+ *   zeros  : device uint8, same shape.
+ *   cfg    : the configuration the codes were made with (bits, group_size;
+ *            zero_point and n_grid are not used).
+ *   x      : device fp16 [M][K], 1 <= M <= 8, 16-byte aligned: activations
+ *            with diag(s)^-1 already folded into their producer
+ *            (awq_fold_scale).
+ *   y      : device fp32 [M][N], written:
+ *            y[m][n] = sum_g scale[n][g] * sum_{k in g} (code - zero) * x[m][k],
+ *            all sums in fp32.
+ * K % 8 == 0 and K % group == 0 (K % 64 for group_size -1).  Allocates
+ * nothing. */
+awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uint8_t* zeros,
+                            int64_t N, int64_t K, const awq_qconfig* cfg, const void* x, int M,
+                            float* y, void* stream);
+
 /* Layer output before quantization, Y = W X^T ("AWQ Explained", multigrid.ai,
  * "How the scale is chosen": the W x term), on tcgen05 tensor cores.
  *   W : device fp16 [N][K];  X : device fp16 [T][K];  K % 64 == 0.

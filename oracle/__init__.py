@@ -17,4 +17,5 @@ from .awq_oracle import (  # noqa: F401
     scale_vector,
     search,
     unpack_codes,
+    w4a16_matvec,
 )

@@ -25,6 +25,10 @@ it follows.  Pages (by title):
   glossary): 3- or 4-bit packing in groups, commonly 128.
 * [AI360] "AWQ" (ai360xpert.com), section "How It Works", step 4: the scaled
   weights are quantized with plain round-to-nearest.
+* [AWQX-DEC] "AWQ explained" (hungho77.github.io), "Why weight-only
+  quantization fits decoding": at small batch the weights dominate the
+  memory traffic; 4-bit weights with 16-bit activations (W4A16) cut it about
+  four times.
 * [MG-FOLD] "AWQ Explained" (multigrid.ai), "Scaling instead of mixed
   precision": diag(s)^-1 is folded offline into the operation that produces
   the layer's input (the preceding LayerNorm / RMSNorm weight, or a preceding
@@ -160,6 +164,8 @@ def dequantize_scaled(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
     """deq(Q(W')) in the scaled units of W': (q - z) * scale, fp64."""
     codes = np.asarray(codes)
     N, K = codes.shape
+    if group == -1:
+        group = K
     q = codes.astype(np.float64).reshape(N, K // group, group)
     z = np.asarray(zeros).astype(np.float64)[:, :, None]
     sf = np.asarray(scales, np.float16).astype(np.float64)[:, :, None]
@@ -328,3 +334,16 @@ def fold_inverse_scale(V: np.ndarray, s: np.ndarray) -> np.ndarray:
         raise ValueError("V's first axis must match s")
     d = s32 if V.ndim == 1 else s32.reshape((-1,) + (1,) * (V.ndim - 1))
     return (V.astype(np.float32) / d).astype(np.float16)
+
+
+# --------------------------------------------------------------------------
+# Step 8: consuming the packed layer ([AWQX-DEC]): the W4A16 product.
+# --------------------------------------------------------------------------
+def w4a16_matvec(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray, group: int,
+                 x: np.ndarray) -> np.ndarray:
+    """y[m, n] = sum_k (q[n, k] - z[n, g(k)]) * scale[n, g(k)] * x[m, k] in fp64.
+
+    ``codes`` are unpacked [N, K]; ``x`` is fp16 [M, K] (the activations with
+    diag(s)^-1 already folded into their producer)."""
+    deq = dequantize_scaled(codes, scales, zeros, group)
+    return np.asarray(x, np.float16).astype(np.float64) @ deq.T

@@ -14,6 +14,7 @@ Functions mirror the C entry points:
 ``unpack_codes(codes, N, K, b)``  codes as uint8 [N, K]                (awq_unpack_codes)
 ``reference_output(W, X)``        Y = W X^T in fp32                    (awq_reference_output)
 ``fold_scale(V, s)``              V / s along rows (deploy step)       (awq_fold_scale)
+``w4a16_matvec(codes, sc, z, x)`` y = deq(Q) x for 1..8 tokens         (awq_w4a16_matvec)
 ``search(X, Ws, ...)``            the full per-layer search            (awq_search_layer)
 """
 from __future__ import annotations
@@ -27,7 +28,7 @@ import torch
 
 __all__ = [
     "AwqError", "lib", "library_path", "groups_per_row", "stats", "stats_noalloc", "scales", "quantize_pack", "unpack_codes",
-    "reference_output", "fold_scale", "search", "search_host", "SearchResult", "packed_words",
+    "reference_output", "fold_scale", "w4a16_matvec", "search", "search_host", "SearchResult", "packed_words",
     "release_cached_memory", "selftest_bounded_wait", "set_stage_timing", "STAGES",
     "EXPORTED_SYMBOLS",
 ]
@@ -47,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "awq_result_s", "awq_result_s_grid", "awq_result_row_losses", "awq_result_codes",
     "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
     "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
-    "awq_result_stage_ms", "awq_stats_noalloc", "awq_fold_scale",
+    "awq_result_stage_ms", "awq_stats_noalloc", "awq_fold_scale", "awq_w4a16_matvec",
 )
 
 # Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
         "awq_unpack_codes": (st, [vp, i64, i64, i32, vp, vp]),
         "awq_reference_output": (st, [vp, i64, vp, i64, i64, vp, vp, vp]),
         "awq_fold_scale": (st, [vp, i64, i64, vp, vp, vp]),
+        "awq_w4a16_matvec": (st, [vp, vp, vp, i64, i64, ctypes.POINTER(QConfig), vp, i32, vp,
+                                  vp]),
         "awq_search_layer": (st, [vp, i64, i64, vp, ctypes.POINTER(Weight), i32,
                                   ctypes.POINTER(QConfig), vp, ctypes.POINTER(vp)]),
         "awq_result_check": (st, [vp]),
@@ -249,6 +252,21 @@ def fold_scale(V: torch.Tensor, s: torch.Tensor, out: Optional[torch.Tensor] = N
         raise ValueError("out must be a contiguous fp16 tensor shaped like V")
     _check(lib().awq_fold_scale(V.data_ptr(), rows, cols, s.data_ptr(), out.data_ptr(), _stream()))
     return out
+
+
+def w4a16_matvec(codes: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, N: int, K: int,
+                 x: torch.Tensor, group: int = 128) -> torch.Tensor:
+    """y [M, N] fp32 = deq(INT4 codes) x^T for x fp16 [M, K], 1 <= M <= 8."""
+    _require(codes, "codes", torch.int32, 1)
+    _require(x, "x", torch.float16, 2)
+    if x.shape[1] != K:
+        raise ValueError(f"x has K={x.shape[1]}, expected {K}")
+    M = x.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    cfg = _cfg(4, group)
+    _check(lib().awq_w4a16_matvec(codes.data_ptr(), scales.data_ptr(), zeros.data_ptr(), N, K,
+                                  ctypes.byref(cfg), x.data_ptr(), M, y.data_ptr(), _stream()))
+    return y
 
 
 class _DevArray:

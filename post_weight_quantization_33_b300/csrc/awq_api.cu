@@ -329,6 +329,30 @@ awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bit
   return ok();
 }
 
+awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uint8_t* zeros,
+                            int64_t N, int64_t K, const awq_qconfig* cfg, const void* x, int M,
+                            float* y, void* stream) {
+  awq_status st;
+  if ((st = check_cfg(cfg)) != AWQ_OK) return st;
+  if (cfg->bits != 4)
+    return fail(AWQ_ERR_UNSUPPORTED, "bits=%d (the W4A16 product takes INT4 codes)", cfg->bits);
+  if (N < 1 || N > (int64_t(1) << 31) || !k_fits(K, cfg) || K % 8 || K > (int64_t(1) << 31))
+    return fail(AWQ_ERR_INVALID, "N=%lld K=%lld (N >= 1; K a multiple of 8 and of the group)",
+                static_cast<long long>(N), static_cast<long long>(K));
+  if (M < 1 || M > 8) return fail(AWQ_ERR_INVALID, "M=%d (1..8)", M);
+  if ((st = check_dev(codes, "codes", 4)) != AWQ_OK) return st;
+  if ((st = check_dev(scales, "scales", 2)) != AWQ_OK) return st;
+  if ((st = check_dev(zeros, "zeros", 1)) != AWQ_OK) return st;
+  if ((st = check_dev(x, "x", 16)) != AWQ_OK) return st;
+  if ((st = check_dev(y, "y", 4)) != AWQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto cleanup = [] {};
+  AWQ_CUDA(launch_w4_matvec(codes, static_cast<const __half*>(scales), zeros, N, K,
+                            cfg->group_size, static_cast<const __half*>(x), M, y, s),
+           "W4A16 product kernel");
+  return ok();
+}
+
 awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float* s_vec,
                           void* out, void* stream) {
   if (rows < 1 || cols < 1 || rows > (int64_t(1) << 40) / cols)

@@ -96,6 +96,13 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaS
 cudaError_t launch_fold(const __half* V, int64_t rows, int64_t cols, const float* s, __half* out,
                         cudaStream_t st);
 
+// ---- W4A16 product (awq_matvec.cu)
+// y[m][n] = sum_k (code - zero) * scale * x[m][k], fp32 [M][N], 1 <= M <= 8,
+// INT4 codes [N][K/8], group 64, 128 or -1.
+cudaError_t launch_w4_matvec(const uint32_t* codes, const __half* scales, const uint8_t* zeros,
+                             int64_t N, int64_t K, int group, const __half* x, int M, float* y,
+                             cudaStream_t st);
+
 // ---- loss reduction (awq_reduce.cu)
 // Number of 256-row chunks of the padded row space (chunk_sums holds
 // n_alpha * loss_chunks(n_pad) * n_w doubles of scratch).

@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "awq_f32x2.cuh"
 #include "awq_internal.h"
 
 namespace awq {
@@ -85,33 +86,9 @@ __device__ __forceinline__ void load_w16(const __half* p, float* w) {
   }
 }
 
-// Packed fp32 pairs (sm_100 f32x2 arithmetic, both lanes rounded to nearest
-// even).  ptxas fuses a packed multiply into a following packed add even with
-// .rn, so a packed add never consumes a product directly: in the quantizer
-// the rounding add consumes a clamped value (a min / max sits between).
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pack2(float a, float b) {
-  return static_cast<f32x2>(__float_as_uint(a)) | (static_cast<f32x2>(__float_as_uint(b)) << 32);
-}
-__device__ __forceinline__ float lo2(f32x2 v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float hi2(f32x2 v) {
-  return __uint_as_float(static_cast<uint32_t>(v >> 32));
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
+// Packed fp32 pairs come from awq_f32x2.cuh.  In the quantizer no packed
+// add consumes a product directly: the rounding add consumes a clamped value
+// (a min / max sits between).
 // Three-input min / max (exact, like fminf / fmaxf).
 __device__ __forceinline__ float min3f(float a, float b, float c) {
   float d;

@@ -88,6 +88,11 @@ def test_invalid_arguments_rejected_before_launch(L):
     assert L.awq_quantize_pack(None, 0, 256, None, _cfg(), None, None, None, None) == 0
     assert L.awq_unpack_codes(None, 2, 100, 4, None, None) == INVALID
     assert L.awq_reference_output(None, 4, None, 4, 100, None, None, None) == INVALID
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(bits=3), None, 1, None,
+                              None) == UNSUPPORTED
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 9, None, None) == INVALID
+    assert L.awq_w4a16_matvec(None, None, None, 4, 200, _cfg(), None, 1, None, None) == INVALID
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 1, None, None) == INVALID
     assert L.awq_fold_scale(None, 0, 8, None, None, None) == INVALID
     assert L.awq_fold_scale(None, 8, 0, None, None, None) == INVALID
     assert L.awq_fold_scale(None, 8, 8, None, None, None) == INVALID

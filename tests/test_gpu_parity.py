@@ -175,6 +175,50 @@ def test_fold_after_search_keeps_layer_output():
 
 
 # --------------------------------------------------------------------------
+# W4A16 product with the packed layer: within a stated fp32 rounding bound.
+# --------------------------------------------------------------------------
+def _matvec_bound(codes, sc, z, group, x):
+    """|y_gpu - y| <= (words + 8) * 2^-23 * sum_k |deq_k x_k|: every product is
+    exact in fp32; the per-word sums (8 terms), the scaled running sums (one
+    per word) and the 32-lane reduction each round once per step."""
+    deq = O.dequantize_scaled(codes, sc, z, group)
+    mag = np.abs(x.astype(np.float64)) @ np.abs(deq).T
+    return (codes.shape[1] / 8 + 8 + 5) * 2.0 ** -23 * mag
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+@pytest.mark.parametrize("N,K,group", [(1, 128, 128), (37, 256, 64), (300, 1024, 128),
+                                       (129, 4096, -1), (64, 11008, 128)])
+def test_w4a16_matvec(M, N, K, group):
+    rng = workloads.weight_rng(M * 100 + N + K + group)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), 4, group)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), group))
+    oc, osc, oz = O.quantize_groups(W, s, 4, group)
+    want = O.w4a16_matvec(oc, osc, oz, group, x)
+    err = np.abs(y.astype(np.float64) - want)
+    assert np.all(err <= _matvec_bound(oc, osc, oz, group, x) + 1e-30), float(err.max())
+
+
+def test_w4a16_matvec_long_k_chunks():
+    """K = 28672 at M = 8 does not fit shared memory at once: x is staged in
+    chunks along K."""
+    rng = workloads.weight_rng(4242)
+    N, K, M = 40, 28672, 8
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.ones(K, np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), 4, 128)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), 128))
+    oc, osc, oz = O.quantize_groups(W, s, 4, 128)
+    want = O.w4a16_matvec(oc, osc, oz, 128, x)
+    err = np.abs(y.astype(np.float64) - want)
+    assert np.all(err <= _matvec_bound(oc, osc, oz, 128, x) + 1e-30)
+
+
+# --------------------------------------------------------------------------
 # Reference GEMM Y = W X^T (tcgen05).
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("N,T,K", [(128, 256, 64), (1, 1, 64), (200, 300, 192), (256, 64, 512),

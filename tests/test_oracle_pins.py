@@ -493,6 +493,33 @@ def test_symmetric_homogeneity_power_of_two(k):
     assert np.array_equal(s2.astype(np.float64), s1.astype(np.float64) * 2.0 ** k)
 
 
+def test_w4a16_matvec_hand_example():
+    """AWQ explained, "Why weight-only quantization fits decoding" (W4A16):
+    codes [15, 0], scale 0.5, zero 8, x = [1, 2]:
+    (15 - 8) * 0.5 * 1 + (0 - 8) * 0.5 * 2 = 3.5 - 8 = -4.5."""
+    y = O.w4a16_matvec(np.array([[15, 0]], np.uint8), np.array([[0.5]], np.float16),
+                       np.array([[8]], np.uint8), 2, np.array([[1.0, 2.0]], np.float16))
+    assert y.shape == (1, 1) and y[0, 0] == -4.5
+
+
+@pytest.mark.parametrize("zp,group", [(True, 128), (False, 64), (True, -1)])
+def test_w4a16_matvec_within_rounding_of_dense(zp, group):
+    """y from the packed layer differs from W x by at most the rounding of
+    each weight: |y - W x| <= sum_k |w_k - deq_k| |x_k| with |w - deq| <=
+    scale / 2 per weight (unclamped codes), checked row by row."""
+    rng = workloads.weight_rng(93 + group)
+    W = (rng.standard_normal((24, 256)) * 0.02).astype(np.float16)
+    x = rng.standard_normal((3, 256)).astype(np.float16)
+    c, sc, z = O.quantize_groups(W, np.ones(256, np.float32), 4, group, zero_point=zp)
+    y = O.w4a16_matvec(c, sc, z, group, x)
+    dense = x.astype(np.float64) @ W.astype(np.float64).T
+    g = 256 if group == -1 else group
+    half_step = np.repeat(sc.astype(np.float64), g, axis=1) / 2
+    bound = np.abs(x.astype(np.float64)) @ half_step.T
+    assert np.all(np.abs(y - dense) <= bound * (1 + 1e-9))
+    assert np.abs(y - dense).max() > 0
+
+
 @pytest.mark.parametrize("bits", [3, 4])
 def test_pack_roundtrip_random(bits):
     rng = workloads.weight_rng(18 + bits)
