@@ -488,6 +488,32 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         "clocks": clk,
         "wall_s": t_wall,
     }
+    # Workloads with more calibration tokens than channels: the same search
+    # with the loss in its Gram form, reported as a separate variant (its
+    # flops are not the metric's; the roofline above stays the direct form's).
+    if any(wl.spec(c.x).rows > wl.spec(c.x).cols for c in wl.calls):
+        gsteps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            for X, Ws, bits, group in calls:
+                awq.search(X, Ws, bits, group, N_GRID, gram=True).free()
+        barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        gms = 0.0
+        for i in range(gsteps):
+            flush.fill_(i)
+            g0.record(stream)
+            res = [awq.search(X, Ws, bits, group, N_GRID, gram=True) for X, Ws, bits, group in calls]
+            g1.record(stream)
+            g1.synchronize()
+            gms += g0.elapsed_time(g1)
+            for r in res:
+                r.check()
+                r.free()
+        line["gram_variant"] = {
+            "value": weights_per_step * gsteps / (gms / 1e3), "unit": UNIT,
+            "ms_per_step": gms / gsteps, "speedup_vs_direct": (total_ms / args.steps) / (gms / gsteps),
+            "note": "awq_search_layer_gram: loss as d^T (X^T X) d; same outputs within 1e-3"}
     # The residual pass: W read once, n_grid fp16 residuals written.
     res_ms = stage_sum["residual"] / args.steps
     res_bytes = sum(2 * wl.spec(w).rows * wl.spec(w).cols * (1 + N_GRID)

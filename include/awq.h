@@ -225,6 +225,21 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
                             const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
                             awq_result** out);
 
+/* The same search with the loss evaluated in its Gram form: for output row n
+ * with residual d_n, sum_t (d_n . x_t)^2 = d_n^T G d_n with G = X^T X ("AWQ
+ * Explained", multigrid.ai, "How the scale is chosen": the layer-output error
+ * over the calibration batch; the identity is plain linear algebra).  G is
+ * formed once (T K^2 flops, fp32 on the tensor cores) and stored as fp16
+ * G * c / T with a power of two c chosen from max |G|; each grid point then
+ * costs N K^2 flops instead of N K T, so the variant pays off when T > K.
+ * Arguments, outputs, ownership and errors as awq_search_layer; losses agree
+ * with it within the fp16 rounding of G (about 1e-5 relative on the
+ * workloads tested, bar 1e-3).  Extra scratch: 2*K*Tp + 6*K*K bytes
+ * (Tp = T rounded up to 64). */
+awq_status awq_search_layer_gram(const void* X, int64_t T, int64_t K, const double* sX,
+                                 const awq_weight* Ws, int n_w, const awq_qconfig* cfg,
+                                 void* stream, awq_result** out);
+
 /* After the search's stream is synchronised: AWQ_OK, or AWQ_ERR_TIMEOUT if a
  * bounded device wait expired during the search. */
 awq_status awq_result_check(const awq_result* r);

@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
     "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
     "awq_result_stage_ms", "awq_stats_noalloc", "awq_fold_scale", "awq_w4a16_matvec",
+    "awq_search_layer_gram",
 )
 
 # Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
                                   vp]),
         "awq_search_layer": (st, [vp, i64, i64, vp, ctypes.POINTER(Weight), i32,
                                   ctypes.POINTER(QConfig), vp, ctypes.POINTER(vp)]),
+        "awq_search_layer_gram": (st, [vp, i64, i64, vp, ctypes.POINTER(Weight), i32,
+                                       ctypes.POINTER(QConfig), vp, ctypes.POINTER(vp)]),
         "awq_result_check": (st, [vp]),
         "awq_result_n_grid": (i32, [vp]),
         "awq_result_n_weights": (i32, [vp]),
@@ -381,9 +384,10 @@ class SearchResult:
 
 def search(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: int = 128,
            n_grid: int = 20, sX: Optional[torch.Tensor] = None,
-           zero_point: bool = True) -> SearchResult:
+           zero_point: bool = True, gram: bool = False) -> SearchResult:
     """Run awq_search_layer for the weights ``Ws`` sharing activations ``X``
-    (group -1: one group per output row; zero_point False: symmetric)."""
+    (group -1: one group per output row; zero_point False: symmetric;
+    gram True: awq_search_layer_gram, the loss as d^T (X^T X) d)."""
     _require(X, "X", torch.float16, 2)
     T, K = X.shape
     arr = (Weight * len(Ws))()
@@ -399,8 +403,9 @@ def search(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, group: in
         sxp = sX.data_ptr()
     cfg = _cfg(bits, group, n_grid, zero_point)
     out = ctypes.c_void_p()
-    _check(lib().awq_search_layer(X.data_ptr(), T, K, sxp, arr, len(Ws), ctypes.byref(cfg),
-                                  _stream(), ctypes.byref(out)))
+    entry = lib().awq_search_layer_gram if gram else lib().awq_search_layer
+    _check(entry(X.data_ptr(), T, K, sxp, arr, len(Ws), ctypes.byref(cfg), _stream(),
+                 ctypes.byref(out)))
     return SearchResult(out.value, [W.shape[0] for W in Ws], K, T, bits, group, n_grid, X.device)
 
 

@@ -391,9 +391,12 @@ awq_status awq_reference_output(const void* W, int64_t N, const void* X, int64_t
   return ok();
 }
 
-awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* sX,
-                            const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
-                            awq_result** out) {
+}  // extern "C"
+
+// The search; gram: evaluate the loss in the Gram form d^T (X^T X) d.
+static awq_status search_impl(const void* X, int64_t T, int64_t K, const double* sX,
+                              const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
+                              awq_result** out, bool gram) {
   if (out == nullptr) return fail(AWQ_ERR_INVALID, "out is NULL");
   *out = nullptr;
   awq_status st;
@@ -427,7 +430,9 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   n_pad = ceil_div(n_pad, kPairRows) * kPairRows;   // whole pair tiles for the error GEMM
   const int G = cfg->n_grid;
   const int64_t groups = groups_per_row(K, cfg);
-  const int64_t n_tiles = ceil_div(T, kTileN);
+  // Column tiles of the error GEMM: tokens, or channels in the Gram form.
+  const int64_t n_tiles = ceil_div(gram ? K : T, kTileN);
+  const int64_t Tp = ceil_div(T, kTileK) * kTileK;   // Gram form: tokens padded for X^T
   if (K > (int64_t(1) << 30) || T > (int64_t(1) << 30) || n_pad > (int64_t(1) << 30) ||
       (n_pad / kTileM) * n_tiles * G > (int64_t(1) << 30))
     return fail(AWQ_ERR_INVALID, "shape too large for one call");
@@ -488,6 +493,11 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   int64_t max_rows = 0;
   for (int i = 0; i < n_w; ++i) max_rows = std::max<int64_t>(max_rows, Ws[i].N);
   const size_t o_mmr = wc.take<float2>(cfg->group_size == -1 ? int64_t(G) * max_rows : 1);
+  const size_t o_xt = wc.take<__half>(gram ? K * Tp : 1);
+  const size_t o_g32 = wc.take<float>(gram ? K * K : 1);
+  const size_t o_gs = wc.take<__half>(gram ? K * K : 1);
+  const size_t o_gmx = wc.take<unsigned int>(1);
+  const size_t o_rsc = wc.take<double>(1);
 
   AWQ_CUDA(pool_alloc(&r->block, rc.off, s), "result allocation");
   AWQ_CUDA(pool_alloc(&ws, wc.off, s), "scratch allocation");
@@ -513,6 +523,11 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   auto* partials = reinterpret_cast<float*>(wb + o_pt);
   auto* chunk_sums = reinterpret_cast<double*>(wb + o_cs);
   auto* rowmm = reinterpret_cast<float2*>(wb + o_mmr);   // per-row min / max (group -1)
+  auto* xt = reinterpret_cast<__half*>(wb + o_xt);        // Gram form scratch
+  auto* g32 = reinterpret_cast<float*>(wb + o_g32);
+  auto* gs = reinterpret_cast<__half*>(wb + o_gs);
+  auto* gmx = reinterpret_cast<unsigned int*>(wb + o_gmx);
+  auto* rsc = reinterpret_cast<double*>(wb + o_rsc);
   auto* counter = reinterpret_cast<unsigned int*>(range + 2);
   const __half* Xh = static_cast<const __half*>(X);
 
@@ -568,14 +583,23 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
     r->launches += cfg->group_size == -1 ? 2 : 1;
   }
   AWQ_CUDA(mark(AWQ_STAGE_ERROR_GEMM), "event record");
-  // 4. error GEMM for every grid point: per-row sums of (residual X^T)^2
-  AWQ_CUDA(launch_gemm_error(delta, Xh, T, K, n_pad, G, partials, r->status, s), "error GEMM");
+  // 4. error GEMM for every grid point: per-row sums of (residual X^T)^2, or
+  //    in the Gram form sum_j (residual G)[n][j] residual[n][j] with G = X^T X
+  if (gram) {
+    AWQ_CUDA(launch_gram_prepare(Xh, T, K, xt, Tp, g32, gmx, gs, rsc, r->status, s,
+                                 &r->launches),
+             "Gram matrix");
+    AWQ_CUDA(launch_gemm_error_gram(delta, gs, K, n_pad, G, partials, r->status, s),
+             "error GEMM (Gram form)");
+  } else {
+    AWQ_CUDA(launch_gemm_error(delta, Xh, T, K, n_pad, G, partials, r->status, s), "error GEMM");
+  }
   r->launches += 1;
   AWQ_CUDA(mark(AWQ_STAGE_LOSS), "event record");
   // 5. losses and argmin
   AWQ_CUDA(launch_loss_reduce(partials, G, static_cast<int>(n_tiles), n_pad, T, map, n_total,
                               chunk_sums, r->row_losses, r->losses, r->best, r->alpha,
-                              r->s_grid, K, r->s, counter, s),
+                              r->s_grid, K, r->s, counter, gram ? rsc : nullptr, s),
            "loss reduction");
   r->launches += 1;
   AWQ_CUDA(mark(AWQ_STAGE_FINAL), "event record");
@@ -602,6 +626,20 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
   ws = nullptr;
   *out = r;
   return ok();
+}
+
+extern "C" {
+
+awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* sX,
+                            const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
+                            awq_result** out) {
+  return search_impl(X, T, K, sX, Ws, n_w, cfg, stream, out, false);
+}
+
+awq_status awq_search_layer_gram(const void* X, int64_t T, int64_t K, const double* sX,
+                                 const awq_weight* Ws, int n_w, const awq_qconfig* cfg,
+                                 void* stream, awq_result** out) {
+  return search_impl(X, T, K, sX, Ws, n_w, cfg, stream, out, true);
 }
 
 awq_status awq_result_check(const awq_result* r) {

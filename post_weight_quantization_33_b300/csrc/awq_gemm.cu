@@ -310,14 +310,19 @@ constexpr uint32_t kPairTmemCols = 512;
 
 struct PairArgs {
   int num_mp;        // pair tiles along residual rows (256 rows each)
-  int num_n_tiles;   // token tiles (256 tokens each)
+  int num_n_tiles;   // column tiles (256 tokens, or 256 channels for the Gram form)
   int num_alpha;     // grid points
   int k_blocks;      // K / 64
   int64_t n_pad;     // rows of the residual and partials layout (multiple of 256)
   float* partials;   // [alpha][n_tiles][n_pad]
   int* status;
+  const __half* delta;   // Gram form: the residual [alpha][n_pad][K] (the epilogue's weights)
+  int64_t K;             // Gram form: channels (columns of Gs and of delta)
 };
 
+// kGram: the B operand is Gs (K x K) instead of X, and the epilogue forms
+// sum_j E[n][j] * delta[n][j] over its 256 columns instead of sum E^2.
+template <bool kGram>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_err_pair(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const PairArgs p) {
@@ -477,17 +482,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PN;
       float sum0 = 0.f, sum1 = 0.f;
+      const __half* drow =
+          kGram ? p.delta + (static_cast<int64_t>(a) * p.n_pad + static_cast<int64_t>(mp) * 2 * PM +
+                             static_cast<int64_t>(rank) * PM + row) * p.K
+                : nullptr;
 #pragma unroll 1
       for (int c = 0; c < PN / 32; ++c) {
+        uint4 dv[4];
+        const int64_t j0 = static_cast<int64_t>(nt) * PN + c * 32;   // Gram: first column
+        const bool in = kGram && j0 < p.K;   // K % 64 == 0: a 32-column chunk is all in or out
+        if (in) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dv[i] = __ldg(reinterpret_cast<const uint4*>(drow + j0) + i);
+        }
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + c * 32, v);
         tmem_ld_wait();
+        if (kGram) {
+          if (in) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float e0 = __uint_as_float(v[j]);
-          const float e1 = __uint_as_float(v[j + 1]);
-          sum0 = fmaf(e0, e0, sum0);
-          sum1 = fmaf(e1, e1, sum1);
+            for (int i = 0; i < 4; ++i) {
+              const __half2* h = reinterpret_cast<const __half2*>(&dv[i]);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float2 d = __half22float2(h[t]);
+                sum0 = fmaf(__uint_as_float(v[8 * i + 2 * t]), d.x, sum0);
+                sum1 = fmaf(__uint_as_float(v[8 * i + 2 * t + 1]), d.y, sum1);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float e0 = __uint_as_float(v[j]);
+            const float e1 = __uint_as_float(v[j + 1]);
+            sum0 = fmaf(e0, e0, sum0);
+            sum1 = fmaf(e1, e1, sum1);
+          }
         }
       }
       tc_fence_before();
@@ -585,6 +616,50 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
   return cudaGetLastError();
 }
 
+// Residual [alpha][n_pad][K]: box 64 x 128 (one CTA's rows of a pair tile).
+bool make_residual_tmap(CUtensorMap* ta, const __half* delta, int64_t K, int64_t n_pad,
+                        int n_alpha) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(n_pad),
+                              static_cast<cuuint64_t>(n_alpha)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
+                                 static_cast<cuuint64_t>(K) * 2 * static_cast<cuuint64_t>(n_pad)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(PM), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(delta), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kGram>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const PairArgs& a,
+                        cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_err_pair<kGram>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(P_SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  // One pair per co-resident cluster slot (persistent), at most one per tile.
+  const int64_t tiles = static_cast<int64_t>(a.num_mp) * a.num_n_tiles * a.num_alpha;
+  int clusters = sm_count() / 2;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm_err_pair<kGram>, &cfg) ==
+            cudaSuccess &&
+        max_clusters > 0)
+      clusters = std::min(clusters, max_clusters);
+    else
+      cudaGetLastError();
+  }
+  const int pairs = static_cast<int>(std::min<int64_t>(clusters, tiles));
+  k_gemm_err_pair<kGram><<<2 * pairs, kThreads, P_SMEM_BYTES, st>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, int64_t T,
@@ -608,22 +683,8 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
                               int64_t n_pad, int n_alpha, float* partials, int* status,
                               cudaStream_t st) {
   if (n_pad % (2 * PM) != 0) return cudaErrorInvalidValue;
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
-  {
-    // Residual [alpha][n_pad][K]: box 64 x 128 (this CTA's rows of a pair tile).
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(n_pad),
-                                static_cast<cuuint64_t>(n_alpha)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
-                                   static_cast<cuuint64_t>(K) * 2 * static_cast<cuuint64_t>(n_pad)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(PM), 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (fn(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(delta), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!make_residual_tmap(&ta, delta, K, n_pad, n_alpha)) return cudaErrorInvalidValue;
   // X [T][K]: box 64 x 128 (this CTA's half of a 256-token tile; tokens past
   // T read as zeros).
   if (!make_tmap_f16(&tb, X, 1, T, K, PN / 2)) return cudaErrorInvalidValue;
@@ -635,27 +696,28 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
   a.n_pad = n_pad;
   a.partials = partials;
   a.status = status;
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_err_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(P_SMEM_BYTES));
-  if (e != cudaSuccess) return e;
-  // One pair per co-resident cluster slot (persistent), at most one per tile.
-  const int64_t tiles = static_cast<int64_t>(a.num_mp) * a.num_n_tiles * a.num_alpha;
-  int clusters = sm_count() / 2;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm_err_pair, &cfg) == cudaSuccess &&
-        max_clusters > 0)
-      clusters = std::min(clusters, max_clusters);
-    else
-      cudaGetLastError();
-  }
-  const int pairs = static_cast<int>(std::min<int64_t>(clusters, tiles));
-  k_gemm_err_pair<<<2 * pairs, kThreads, P_SMEM_BYTES, st>>>(ta, tb, a);
-  return cudaGetLastError();
+  return launch_pair<false>(ta, tb, a, st);
+}
+
+cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_t K,
+                                   int64_t n_pad, int n_alpha, float* partials, int* status,
+                                   cudaStream_t st) {
+  if (n_pad % (2 * PM) != 0 || K % BK != 0) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_residual_tmap(&ta, delta, K, n_pad, n_alpha)) return cudaErrorInvalidValue;
+  // Gs [K][K] (symmetric): B rows are its columns; box 64 x 128.
+  if (!make_tmap_f16(&tb, Gs, 1, K, K, PN / 2)) return cudaErrorInvalidValue;
+  PairArgs a{};
+  a.num_mp = static_cast<int>(n_pad / (2 * PM));
+  a.num_n_tiles = static_cast<int>(ceil_div(K, PN));
+  a.num_alpha = n_alpha;
+  a.k_blocks = static_cast<int>(K / BK);
+  a.n_pad = n_pad;
+  a.partials = partials;
+  a.status = status;
+  a.delta = delta;
+  a.K = K;
+  return launch_pair<true>(ta, tb, a, st);
 }
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st) {

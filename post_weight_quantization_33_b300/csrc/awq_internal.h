@@ -96,6 +96,18 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaS
 cudaError_t launch_fold(const __half* V, int64_t rows, int64_t cols, const float* s, __half* out,
                         cudaStream_t st);
 
+// ---- Gram form (awq_gram.cu)
+// XT fp16 [K][Tp] (Tp = T rounded up to 64), G fp32 [K][K], mx one u32,
+// Gs fp16 [K][K] = G * (c / T), *row_scale = T / c (c a power of two).
+cudaError_t launch_gram_prepare(const __half* X, int64_t T, int64_t K, __half* XT, int64_t Tp,
+                                float* G, unsigned int* mx, __half* Gs, double* row_scale,
+                                int* status, cudaStream_t st, int* launches);
+// partials[a][j_tile][n_pad] = sum over the tile's 256 columns j of
+// (delta[a] Gs)[n][j] * delta[a][n][j] (Gs fp16 [K][K], symmetric).
+cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_t K,
+                                   int64_t n_pad, int n_alpha, float* partials, int* status,
+                                   cudaStream_t st);
+
 // ---- W4A16 product (awq_matvec.cu)
 // y[m][n] = sum_k (code - zero) * scale * x[m][k], fp32 [M][N], 1 <= M <= 8,
 // INT4 codes [N][K/8], group 64, 128 or -1.
@@ -108,12 +120,13 @@ cudaError_t launch_w4_matvec(const uint32_t* codes, const __half* scales, const 
 // n_alpha * loss_chunks(n_pad) * n_w doubles of scratch).
 int64_t loss_chunks(int64_t n_pad);
 // Also copies s_grid[best] (K floats) to s_out.  counter: one u32 of scratch,
-// zeroed by the caller before the launch.
+// zeroed by the caller before the launch.  row_scale (nullable, device):
+// factor on every row sum (the Gram form's T / c).
 cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
                                int64_t T, const RowMap& map, int64_t n_total,
                                double* chunk_sums, double* row_losses, double* losses, int* best,
                                double* alpha_out, const float* s_grid, int64_t K, float* s_out,
-                               unsigned int* counter, cudaStream_t st);
+                               unsigned int* counter, const double* row_scale, cudaStream_t st);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

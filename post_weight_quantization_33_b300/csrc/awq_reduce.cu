@@ -14,7 +14,8 @@ constexpr int kLossRows = 256;   // rows per block (a chunk)
 
 // Block (c, a): rows [256c, 256c + 256) of the padded row space, grid point
 // a.  Per row: the sum over token tiles of partials[a][tile][row], in tile
-// order, written to row_losses; per weight present in the chunk: the sum of
+// order, times *row_scale when given (the Gram form's scale), written to
+// row_losses; per weight present in the chunk: the sum of
 // its rows by a fixed tree, written to chunk_sums[a][c][w].  The last block
 // to finish (counted on *counter, zeroed by the caller) adds the chunks of
 // every grid point in chunk order, divides by N_w * T, sums the weights, takes
@@ -26,7 +27,7 @@ __global__ void __launch_bounds__(kLossRows)
              double* __restrict__ row_losses, double* __restrict__ losses,
              int* __restrict__ best, double* __restrict__ alpha_out,
              const float* __restrict__ s_grid, int64_t K, float* __restrict__ s_out,
-             unsigned int* __restrict__ counter) {
+             unsigned int* __restrict__ counter, const double* __restrict__ row_scale) {
   __shared__ double red[kLossRows];
   __shared__ int last, chosen;
   const int c = blockIdx.x;
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(kLossRows)
   if (real) {
     const float* pa = partials + static_cast<int64_t>(a) * n_tiles * n_pad + v;
     for (int t = 0; t < n_tiles; ++t) row += static_cast<double>(pa[static_cast<int64_t>(t) * n_pad]);
+    if (row_scale != nullptr) row *= *row_scale;
     row_losses[static_cast<int64_t>(a) * n_total + map.cum[w] + n] = row;
   }
   // Per-weight chunk sums (a chunk of 256 rows meets at most a few weights).
@@ -112,11 +114,11 @@ cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, 
                                int64_t T, const RowMap& map, int64_t n_total,
                                double* chunk_sums, double* row_losses, double* losses, int* best,
                                double* alpha_out, const float* s_grid, int64_t K, float* s_out,
-                               unsigned int* counter, cudaStream_t st) {
+                               unsigned int* counter, const double* row_scale, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(loss_chunks(n_pad)), static_cast<unsigned>(n_alpha));
   k_losses<<<grid, kLossRows, 0, st>>>(partials, n_tiles, n_pad, map, n_total, T, chunk_sums,
                                        row_losses, losses, best, alpha_out, s_grid, K, s_out,
-                                       counter);
+                                       counter, row_scale);
   return cudaGetLastError();
 }
 

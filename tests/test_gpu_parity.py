@@ -248,8 +248,9 @@ def _argmin_ok(gpu_best, oracle_losses):
     return close and gpu_best in (order[0], order[1])
 
 
-def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=2e-3, zero_point=True):
-    res = awq.search(cuda(X), [cuda(W) for W in Ws], bits, group, n_grid, zero_point=zero_point)
+def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=2e-3, zero_point=True, gram=False):
+    res = awq.search(cuda(X), [cuda(W) for W in Ws], bits, group, n_grid, zero_point=zero_point,
+                     gram=gram)
     res.check()
     ref = O.search(X, Ws, bits, group, n_grid, zero_point=zero_point)
     losses = res.losses
@@ -300,6 +301,27 @@ def test_search_quantizer_modes_tiny(bits, group, zp):
     and one group per output row (group_size -1)."""
     t = workloads.generate("tiny")
     _compare_search(t["X"], [t["W"]], bits, group, zero_point=zp)
+
+
+@pytest.mark.parametrize("T", [64, 77, 1024])
+def test_search_gram_form(T):
+    """The loss in its Gram form d^T (X^T X) d (awq_search_layer_gram): the
+    same losses within 1e-3, the same argmin rule, codes bit-exact at the
+    GPU's alpha -- for T below, at and above K (ragged T pads X^T)."""
+    W, X = workloads.random_layer(200, 512, T, seed=700 + T, outliers=(5, 300), factor=30.0)
+    _compare_search(X, [W], 4, 128, gram=True)
+
+
+def test_search_gram_form_tiny_and_two_weights():
+    t = workloads.generate("tiny")
+    _compare_search(t["X"], [t["W"]], 4, 128, gram=True)
+    Ws = []
+    X = None
+    for j, n in enumerate((130, 60)):
+        W, X0 = workloads.random_layer(n, 256, 300, seed=310 + j, outliers=(3, 200), factor=40.0)
+        Ws.append(W)
+        X = X0 if X is None else X
+    _compare_search(X, Ws, 3, 64, gram=True, zero_point=False)
 
 
 def test_search_per_row_two_weights_ragged():
