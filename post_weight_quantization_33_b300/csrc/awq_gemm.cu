@@ -1,22 +1,20 @@
-// The one dense contraction of the scale search, on tcgen05 tensor cores.
+// The dense contractions of the scale search, on tcgen05 tensor cores.
 //
 // AWQ Explained (multigrid.ai), "How the scale is chosen": alpha* minimises
 // || W x - Q(W diag(s)) diag(s)^-1 x || over the calibration batch.  Written
 // as (W - deq(Q(W diag(s))) diag(s)^-1) x, the error of every grid point is
 // one GEMM of the fp16 quantization residual (produced by the quantizer pass)
-// with the calibration activations.  One persistent, warp-specialised kernel
-// evaluates all grid points:
+// with the calibration activations: k_gemm_err_pair below, on CTA pairs.
 //
-//   warp 4      TMA producer: residual tile [128 x 64] and X tile [256 x 64],
-//               both 128-byte swizzled, into a 4-stage shared-memory ring;
+// k_gemm_ref computes Y = W X^T in fp32 (the "W x" term, and the Gram matrix
+// X^T X of the Gram form) with a single-CTA persistent kernel:
+//
+//   warp 4      TMA producer: A tile [128 x 64] and B tile [256 x 64], both
+//               128-byte swizzled, into a 4-stage shared-memory ring;
 //   warp 5      owns TMEM (2 x 256 fp32 columns) and issues tcgen05.mma
 //               (M 128, N 256, K 16, fp16 in, fp32 accumulate);
 //   warps 0-3   epilogue: tcgen05.ld the finished accumulator (warp w reads
-//               lanes 32w..32w+31 = tile rows), square and sum each row over
-//               the tile's 256 tokens, write one fp32 partial per row.
-//
-// The same kernel with a row-major fp32 store in the epilogue computes the
-// reference output Y = W X^T.
+//               lanes 32w..32w+31 = tile rows) and store it row-major.
 #include <algorithm>
 #include <mutex>
 
@@ -51,31 +49,23 @@ static_assert(OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
 
 struct GemmArgs {
-  int num_m_tiles;   // tiles along weight rows
-  int num_n_tiles;   // tiles along tokens
-  int num_alpha;     // grid points (1 for the reference output)
+  int num_m_tiles;   // tiles along rows of W
+  int num_n_tiles;   // tiles along rows of X
   int k_blocks;      // K / BK
-  int64_t T;         // real tokens
-  int64_t n_pad;     // rows of the partials layout (error mode)
-  int64_t n_rows;    // real rows (reference mode)
-  float* y;          // reference mode: [n_rows][T]
-  float* partials;   // error mode: [alpha][n_tiles][n_pad]
+  int64_t T;         // rows of X
+  int64_t n_rows;    // rows of W
+  float* y;          // [n_rows][T]
   int* status;
 };
 
-__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& a, int& nt,
-                                            int& mt) {
-  const int per_alpha = p.num_m_tiles * p.num_n_tiles;
-  a = tile / per_alpha;
-  const int rem = tile - a * per_alpha;
-  nt = rem / p.num_m_tiles;
-  mt = rem - nt * p.num_m_tiles;
+__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& nt, int& mt) {
+  nt = tile / p.num_m_tiles;
+  mt = tile - nt * p.num_m_tiles;
 }
 
-template <bool kError>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-           const GemmArgs p) {
+    k_gemm_ref(const __grid_constant__ CUtensorMap tmap_a,
+               const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -116,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = p.num_m_tiles * p.num_n_tiles * p.num_alpha;
+  const int total_tiles = p.num_m_tiles * p.num_n_tiles;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -124,8 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, fills = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        int a, nt, mt;
-        decode_tile(tile, p, a, nt, mt);
+        int nt, mt;
+        decode_tile(tile, p, nt, mt);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status,
                                  kDevTimeoutEmpty)) {
@@ -134,10 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = bar_full + 8 * stage;
           mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          if (kError)
-            tma_load_3d(sbase + OFF_A + stage * A_BYTES, &tmap_a, fb, kb * BK, mt * BM, a);
-          else
-            tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, fb, kb * BK, mt * BM);
+          tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, fb, kb * BK, mt * BM);
           tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmap_b, fb, kb * BK, nt * BN);
           ++fills;
           if (++stage == STAGES) {
@@ -206,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;    // tile row
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
-      int a, nt, mt;
-      decode_tile(tile, p, a, nt, mt);
+      int nt, mt;
+      decode_tile(tile, p, nt, mt);
       const uint32_t acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       // tcgen05.ld is warp-collective: decide together and reconverge.
@@ -217,44 +204,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ready) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (kError) {
-        float sum0 = 0.f, sum1 = 0.f;
+      const int64_t grow = static_cast<int64_t>(mt) * BM + row;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, v);
-          tmem_ld_wait();
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v);
+        tmem_ld_wait();
+        if (grow < p.n_rows) {
+          float* yr = p.y + grow * p.T;
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float e0 = __uint_as_float(v[j]);
-            const float e1 = __uint_as_float(v[j + 1]);
-            sum0 = fmaf(e0, e0, sum0);
-            sum1 = fmaf(e1, e1, sum1);
+          for (int j = 0; j < 32; ++j) {
+            const int64_t col = static_cast<int64_t>(nt) * BN + c * 32 + j;
+            if (col < p.T) yr[col] = __uint_as_float(v[j]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(bar_tempty + 8 * acc);
-        p.partials[(static_cast<int64_t>(a) * p.num_n_tiles + nt) * p.n_pad +
-                   static_cast<int64_t>(mt) * BM + row] = sum0 + sum1;
-      } else {
-        const int64_t grow = static_cast<int64_t>(mt) * BM + row;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, v);
-          tmem_ld_wait();
-          if (grow < p.n_rows) {
-            float* yr = p.y + grow * p.T;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int64_t col = static_cast<int64_t>(nt) * BN + c * 32 + j;
-              if (col < p.T) yr[col] = __uint_as_float(v[j]);
-            }
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar_tempty + 8 * acc);
       }
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * acc);
     }
   }
 
@@ -604,15 +570,14 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-template <bool kError>
-cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                   cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(k_gemm<kError>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+cudaError_t launch_ref(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
+                       cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_ref, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  const int total = args.num_m_tiles * args.num_n_tiles * args.num_alpha;
+  const int total = args.num_m_tiles * args.num_n_tiles;
   const int grid = total < sm_count() ? total : sm_count();
-  k_gemm<kError><<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, args);
+  k_gemm_ref<<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, args);
   return cudaGetLastError();
 }
 
@@ -670,13 +635,12 @@ cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, i
   GemmArgs a{};
   a.num_m_tiles = static_cast<int>(ceil_div(N, BM));
   a.num_n_tiles = static_cast<int>(ceil_div(T, BN));
-  a.num_alpha = 1;
   a.k_blocks = static_cast<int>(K / BK);
   a.T = T;
   a.n_rows = N;
   a.y = y;
   a.status = status;
-  return launch<false>(ta, tb, a, st);
+  return launch_ref(ta, tb, a, st);
 }
 
 cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
