@@ -176,8 +176,9 @@ awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float
  * "Why weight-only quantization fits decoding": at small batch each token
  * reads every weight once, so 4-bit weights with 16-bit activations cut the
  * dominant traffic about four times).
- *   codes  : device uint32 [N][K/8], INT4 codes as written by the search or
- *            awq_quantize_pack (cfg->bits must be 4, else AWQ_ERR_UNSUPPORTED).
+ *   codes  : device uint32 [N][K/8], 16-byte aligned, INT4 codes as written
+ *            by the search or awq_quantize_pack (cfg->bits must be 4, else
+ *            AWQ_ERR_UNSUPPORTED).
  *   scales : device fp16 [N][K/group] ([N][1] for group_size -1).
  *   zeros  : device uint8, same shape.
  *   cfg    : the configuration the codes were made with (bits, group_size;

@@ -340,7 +340,7 @@ awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uin
     return fail(AWQ_ERR_INVALID, "N=%lld K=%lld (N >= 1; K a multiple of 8 and of the group)",
                 static_cast<long long>(N), static_cast<long long>(K));
   if (M < 1 || M > 8) return fail(AWQ_ERR_INVALID, "M=%d (1..8)", M);
-  if ((st = check_dev(codes, "codes", 4)) != AWQ_OK) return st;
+  if ((st = check_dev(codes, "codes", 16)) != AWQ_OK) return st;   // 16-byte code loads
   if ((st = check_dev(scales, "scales", 2)) != AWQ_OK) return st;
   if ((st = check_dev(zeros, "zeros", 1)) != AWQ_OK) return st;
   if ((st = check_dev(x, "x", 16)) != AWQ_OK) return st;

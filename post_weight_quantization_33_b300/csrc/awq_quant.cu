@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "awq_async.cuh"
 #include "awq_f32x2.cuh"
 #include "awq_internal.h"
 
@@ -42,13 +43,6 @@ __device__ __forceinline__ void ld_v8f(const float* p, float* v) {
                : "l"(p));
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void ld_v8u(const void* p, uint4* v) {
-  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w), "=r"(v[1].x),
-                 "=r"(v[1].y), "=r"(v[1].z), "=r"(v[1].w)
-               : "l"(p));
 }
 
 __device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
@@ -137,41 +131,26 @@ struct GroupQ {
   __half scale;
 };
 
-template <int GROUP, bool SYM>
-__device__ __forceinline__ void group_params2(const float (&ws)[kRowsPerLane][kPerLane], float L,
-                                              const float2* rowmm, GroupQ (&g)[kRowsPerLane]) {
-  float mn[kRowsPerLane], mx[kRowsPerLane];
-  if constexpr (GROUP == 0) {
+// min / max of the 8 (GROUP 128) or 4 (GROUP 64) lanes of each group, for
+// both rows; every lane of the warp calls this.
+template <int GROUP>
+__device__ __forceinline__ void group_reduce2(float (&mn)[kRowsPerLane], float (&mx)[kRowsPerLane]) {
+  constexpr int GLANES = GROUP / kPerLane;
+#pragma unroll
+  for (int off = GLANES / 2; off; off >>= 1) {
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r) {
-      mn[r] = rowmm[r].x;
-      mx[r] = rowmm[r].y;
-    }
-  } else {
-    constexpr int GLANES = GROUP / kPerLane;
-#pragma unroll
-    for (int r = 0; r < kRowsPerLane; ++r) {
-      float mnA = fminf(ws[r][0], ws[r][1]), mxA = fmaxf(ws[r][0], ws[r][1]);
-      float mnB = fminf(ws[r][2], ws[r][3]), mxB = fmaxf(ws[r][2], ws[r][3]);
-#pragma unroll
-      for (int i = 4; i < kPerLane; i += 4) {
-        mnA = min3f(mnA, ws[r][i], ws[r][i + 1]);
-        mxA = max3f(mxA, ws[r][i], ws[r][i + 1]);
-        mnB = min3f(mnB, ws[r][i + 2], ws[r][i + 3]);
-        mxB = max3f(mxB, ws[r][i + 2], ws[r][i + 3]);
-      }
-      mn[r] = fminf(mnA, mnB);
-      mx[r] = fmaxf(mxA, mxB);
-    }
-#pragma unroll
-    for (int off = GLANES / 2; off; off >>= 1) {
-#pragma unroll
-      for (int r = 0; r < kRowsPerLane; ++r) {
-        mn[r] = fminf(mn[r], __shfl_xor_sync(0xFFFFFFFFu, mn[r], off));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], off));
-      }
+      mn[r] = fminf(mn[r], __shfl_xor_sync(0xFFFFFFFFu, mn[r], off));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], off));
     }
   }
+}
+
+// The quantizer's parameters from the group's min / max.
+template <bool SYM>
+__device__ __forceinline__ void group_finish2(const float (&mn)[kRowsPerLane],
+                                              const float (&mx)[kRowsPerLane], float L,
+                                              GroupQ (&g)[kRowsPerLane]) {
 #pragma unroll
   for (int r = 0; r < kRowsPerLane; ++r) {
     if constexpr (SYM) {
@@ -192,6 +171,36 @@ __device__ __forceinline__ void group_params2(const float (&ws)[kRowsPerLane][kP
       g[r].z = fminf(fmaxf(zu, 0.0f), L);
     }
   }
+}
+
+template <int GROUP, bool SYM>
+__device__ __forceinline__ void group_params2(const float (&ws)[kRowsPerLane][kPerLane], float L,
+                                              const float2* rowmm, GroupQ (&g)[kRowsPerLane]) {
+  float mn[kRowsPerLane], mx[kRowsPerLane];
+  if constexpr (GROUP == 0) {
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      mn[r] = rowmm[r].x;
+      mx[r] = rowmm[r].y;
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      float mnA = fminf(ws[r][0], ws[r][1]), mxA = fmaxf(ws[r][0], ws[r][1]);
+      float mnB = fminf(ws[r][2], ws[r][3]), mxB = fmaxf(ws[r][2], ws[r][3]);
+#pragma unroll
+      for (int i = 4; i < kPerLane; i += 4) {
+        mnA = min3f(mnA, ws[r][i], ws[r][i + 1]);
+        mxA = max3f(mxA, ws[r][i], ws[r][i + 1]);
+        mnB = min3f(mnB, ws[r][i + 2], ws[r][i + 3]);
+        mxB = max3f(mxB, ws[r][i + 2], ws[r][i + 3]);
+      }
+      mn[r] = fminf(mnA, mnB);
+      mx[r] = fmaxf(mxA, mxB);
+    }
+    group_reduce2<GROUP>(mn, mx);
+  }
+  group_finish2<SYM>(mn, mx, L, g);
 }
 
 // ws[i] = w[i] * s[i], correctly rounded (packed multiplies; no add follows).
@@ -270,17 +279,37 @@ __global__ void __launch_bounds__(kQuantThreads)
       ld_v8f(sp + 8, sv + 8);
       ld_v8f(rp, rv);
       ld_v8f(rp + 8, rv + 8);
-      float ws[kRowsPerLane][kPerLane];
-#pragma unroll
-      for (int r = 0; r < kRowsPerLane; ++r) scale16(w[r], sv, ws[r]);
-      float2 mm[kRowsPerLane];
+      // w' = w * s is formed twice (here for the group's min / max, below for
+      // the codes) instead of being held: the same correctly rounded
+      // products, 32 fewer live registers.
+      float mn[kRowsPerLane], mx[kRowsPerLane];
       if constexpr (GROUP == 0) {   // per-row groups: min / max of this grid point's rows
 #pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r)
-          mm[r] = rowmm[static_cast<int64_t>(a) * N + min(row0 + r, N - 1)];
+        for (int r = 0; r < kRowsPerLane; ++r) {
+          const float2 m = rowmm[static_cast<int64_t>(a) * N + min(row0 + r, N - 1)];
+          mn[r] = m.x;
+          mx[r] = m.y;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r) {
+          float mnA = INFINITY, mxA = -INFINITY, mnB = INFINITY, mxB = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kPerLane; i += 4) {
+            const f32x2 p = mul2(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+            const f32x2 q = mul2(pack2(w[r][i + 2], w[r][i + 3]), pack2(sv[i + 2], sv[i + 3]));
+            mnA = min3f(mnA, lo2(p), hi2(p));
+            mxA = max3f(mxA, lo2(p), hi2(p));
+            mnB = min3f(mnB, lo2(q), hi2(q));
+            mxB = max3f(mxB, lo2(q), hi2(q));
+          }
+          mn[r] = fminf(mnA, mnB);
+          mx[r] = fmaxf(mxA, mxB);
+        }
+        group_reduce2<GROUP>(mn, mx);
       }
       GroupQ gq[kRowsPerLane];
-      group_params2<GROUP, SYM>(ws, L, mm, gq);
+      group_finish2<SYM>(mn, mx, L, gq);
       // rare: some group of the warp is all negative (both clamp sides needed)
       const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
 #pragma unroll
@@ -295,7 +324,8 @@ __global__ void __launch_bounds__(kQuantThreads)
         float d[kPerLane];
 #pragma unroll
         for (int i = 0; i < kPerLane; i += 2) {
-          const f32x2 t = mul2(pack2(ws[r][i], ws[r][i + 1]), rcp2);
+          const f32x2 ws2 = mul2_again(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+          const f32x2 t = mul2(ws2, rcp2);
           float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
           if (low) {
             t0 = fmaxf(t0, lo);
@@ -331,49 +361,90 @@ __global__ void __launch_bounds__(kQuantThreads)
 // difference of the bit patterns of m and M - z (consecutive integers in
 // [2^23, 2^24) have consecutive patterns).  codes8: the code words are
 // 8-byte aligned (INT4 only), so a lane stores its two words at once.
-template <int BITS, int GROUP, bool SYM, bool A32>
-__global__ void __launch_bounds__(kQuantThreads)
+//
+// One wave of persistent blocks; a warp keeps its 512 channels (and its
+// lanes' s) and walks row pairs.  W reaches registers through a per-warp
+// ring of kFinStages row pairs in shared memory filled with cp.async, so
+// kFinStages - 1 row pairs of loads are in flight while one is quantized.
+// The warp copies a row's 1 KB as two fully coalesced 512-byte requests
+// (lane l: 16-byte chunks l and 32 + l); lane l then reads its own chunks
+// 2l and 2l + 1, stored at chunk ^ ((chunk / 8) % 2) so that both the
+// copies and the 16-byte reads of each quarter-warp hit distinct banks.
+constexpr int kFinStages = 4;
+constexpr int kFinChunks = 32 * kPerLane / 8;                      // 16-byte chunks per row
+constexpr int kFinSmem = (kQuantThreads / 32) * kFinStages * kRowsPerLane * kFinChunks * 16;
+static_assert(kFinSmem == 64 * 1024, "ring size");
+
+__device__ __forceinline__ int fin_slot(int c) { return c ^ ((c >> 3) & 1); }
+
+template <int BITS, int GROUP, bool SYM>
+__global__ void __launch_bounds__(kQuantThreads, 3)
     k_quant_final(const __half* __restrict__ W, int64_t N, int64_t K,
                   const float* __restrict__ s_base, const int* __restrict__ sel,
                   uint32_t* __restrict__ codes, __half* __restrict__ scales,
                   uint8_t* __restrict__ zeros, bool codes8, const float2* __restrict__ rowmm) {
+  extern __shared__ uint4 fin_ring[];
   constexpr int LEVELS = (1 << BITS) - 1;
   const float L = static_cast<float>(LEVELS);
   const int64_t groups = GROUP == 0 ? 1 : K / (GROUP == 0 ? 1 : GROUP);
   const int64_t words = BITS == 4 ? K / 8 : 3 * K / 32;
   const float* s = s_base + (sel ? static_cast<int64_t>(*sel) * K : 0);
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const Lane lw = lane_chunk(K);
-  for (int64_t row0 = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + (threadIdx.x >> 5)) *
-                      kRowsPerLane;
-       row0 < N; row0 += static_cast<int64_t>(gridDim.y) * kRowsPerBlock) {
-    // Both rows' weights, then s: with A32 (W and s 32-byte aligned) one
-    // 256-bit load per 32 bytes, so a warp's request covers whole lines.
+  const int64_t kbase = static_cast<int64_t>(blockIdx.x) * (32 * kPerLane);
+  const int64_t rest = (K - kbase) / 8;
+  const int valid = static_cast<int>(rest < kFinChunks ? rest : kFinChunks);
+  const int mine = static_cast<int>((lw.k0 - kbase) / 8);   // first of the lane's two chunks
+  uint4* ring = fin_ring + warp * (kFinStages * kRowsPerLane * kFinChunks);
+  const uint32_t ring_u32 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+  const int64_t row_step = static_cast<int64_t>(gridDim.y) * kRowsPerBlock;
+  const int64_t first = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + warp) *
+                        kRowsPerLane;
+  const int64_t iters = first < N ? (N - first + row_step - 1) / row_step : 0;
+  auto issue = [&](int64_t it) {
+    if (it < iters) {
+      const int st = static_cast<int>(it % kFinStages);
+      const int64_t row0 = first + it * row_step;
+#pragma unroll
+      for (int r = 0; r < kRowsPerLane; ++r) {   // a lone last row loads itself twice
+        const __half* src = W + min(row0 + r, N - 1) * K + kbase;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = 32 * j + lane;
+          if (c < valid)
+            cp_async16(ring_u32 + ((st * kRowsPerLane + r) * kFinChunks + fin_slot(c)) * 16,
+                       src + 8 * c);
+        }
+      }
+    }
+    cp_async_commit();   // possibly empty: one group per row pair
+  };
+#pragma unroll
+  for (int i = 0; i < kFinStages - 1; ++i) issue(i);
+  // The lane's s: the same 16 channels for every row.
+  float sv[kPerLane];
+#pragma unroll
+  for (int v = 0; v < kPerLane / 4; ++v) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(s + lw.k0) + v);
+    sv[4 * v] = f.x;
+    sv[4 * v + 1] = f.y;
+    sv[4 * v + 2] = f.z;
+    sv[4 * v + 3] = f.w;
+  }
+  for (int64_t it = 0; it < iters; ++it) {
+    issue(it + kFinStages - 1);
+    cp_async_wait<kFinStages - 1>();
+    __syncwarp();   // every lane's copies of this row pair have landed
+    const int st = static_cast<int>(it % kFinStages);
+    const int64_t row0 = first + it * row_step;
     uint4 raw[kRowsPerLane][2];
 #pragma unroll
-    for (int r = 0; r < kRowsPerLane; ++r) {   // a lone last row loads itself twice
-      const __half* src = W + min(row0 + r, N - 1) * K + lw.k0;
-      if (A32) {
-        ld_v8u(src, raw[r]);
-      } else {
-        raw[r][0] = __ldg(reinterpret_cast<const uint4*>(src));
-        raw[r][1] = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-      }
+    for (int r = 0; r < kRowsPerLane; ++r) {
+      const uint4* slot = ring + (st * kRowsPerLane + r) * kFinChunks;
+      raw[r][0] = slot[fin_slot(mine)];
+      raw[r][1] = slot[fin_slot(mine + 1)];
     }
-    float sv[kPerLane];
-    if (A32) {
-      ld_v8f(s + lw.k0, sv);
-      ld_v8f(s + lw.k0 + 8, sv + 8);
-    } else {
-#pragma unroll
-      for (int v = 0; v < kPerLane / 4; ++v) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(s + lw.k0) + v);
-        sv[4 * v] = f.x;
-        sv[4 * v + 1] = f.y;
-        sv[4 * v + 2] = f.z;
-        sv[4 * v + 3] = f.w;
-      }
-    }
+    __syncwarp();   // the slot is refilled at the next row pair
     float ws[kRowsPerLane][kPerLane];
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r) {
@@ -559,16 +630,29 @@ template <int BITS, int GROUP, bool SYM>
 cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, const int* sel,
                          uint32_t* codes, __half* scales, uint8_t* zeros, const float2* rowmm,
                          cudaStream_t st) {
+  auto kern = k_quant_final<BITS, GROUP, SYM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kFinSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148, per_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQuantThreads, kFinSmem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  // One wave of resident blocks: every block keeps a 512-channel chunk and
+  // takes an equal share of the 16-row blocks.
+  const int64_t gx = ceil_div(K / kPerLane, 32);
+  const int64_t row_blocks = ceil_div(N, kRowsPerBlock);
+  int64_t gy = std::max<int64_t>(1, (static_cast<int64_t>(per_sm) * sms) / gx);
+  gy = std::min<int64_t>(gy, row_blocks);
+  gy = ceil_div(row_blocks, ceil_div(row_blocks, gy));
   const bool c8 = (reinterpret_cast<uintptr_t>(codes) % 8) == 0;
-  const bool a32 = (reinterpret_cast<uintptr_t>(W) % 32) == 0 &&
-                   (reinterpret_cast<uintptr_t>(s) % 32) == 0;
-  const dim3 grid = quant_grid(N, K);
-  if (a32)
-    k_quant_final<BITS, GROUP, SYM, true><<<grid, kQuantThreads, 0, st>>>(
-        W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
-  else
-    k_quant_final<BITS, GROUP, SYM, false><<<grid, kQuantThreads, 0, st>>>(
-        W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
+  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kQuantThreads, kFinSmem,
+         st>>>(W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
   return cudaGetLastError();
 }
 

@@ -93,6 +93,10 @@ def test_invalid_arguments_rejected_before_launch(L):
     assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 9, None, None) == INVALID
     assert L.awq_w4a16_matvec(None, None, None, 4, 200, _cfg(), None, 1, None, None) == INVALID
     assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 1, None, None) == INVALID
+    # codes are read 16 bytes at a time: a 4-byte aligned pointer is refused
+    assert L.awq_w4a16_matvec(ctypes.c_void_p(0x1004), None, None, 4, 256, _cfg(), None, 1, None,
+                              None) == INVALID
+    assert b"codes is not 16-byte aligned" in L.awq_last_error()
     assert L.awq_fold_scale(None, 0, 8, None, None, None) == INVALID
     assert L.awq_fold_scale(None, 8, 0, None, None, None) == INVALID
     assert L.awq_fold_scale(None, 8, 8, None, None, None) == INVALID
