@@ -146,31 +146,44 @@ __device__ __forceinline__ void group_reduce2(float (&mn)[kRowsPerLane], float (
   }
 }
 
-// The quantizer's parameters from the group's min / max.
+// The quantizer's parameters from the group's min / max.  The two lanes
+// 2i and 2i + 1 hold the same groups (a group is 4 or 8 whole lanes, or a
+// whole row), so each computes the parameters of one row (row lane & 1) and
+// takes the other row's from its neighbour: the divide and the reciprocal
+// are paid once per lane instead of twice.
 template <bool SYM>
 __device__ __forceinline__ void group_finish2(const float (&mn)[kRowsPerLane],
                                               const float (&mx)[kRowsPerLane], float L,
                                               GroupQ (&g)[kRowsPerLane]) {
-#pragma unroll
-  for (int r = 0; r < kRowsPerLane; ++r) {
-    if constexpr (SYM) {
-      const float half_levels = 0.5f * (L - 1.0f);   // 7 or 3, exact
-      const float step = __fdiv_rn(fmaxf(fmaxf(-mn[r], mx[r]), 1e-5f), half_levels);
-      g[r].scale = __float2half_rn(step);
-      g[r].sf = __half2float(g[r].scale);
-      g[r].rcp = __frcp_rn(g[r].sf);
-      g[r].low = false;
-      g[r].z = 0.5f * (L + 1.0f);                      // 8 or 4, exact
-    } else {
-      const float step = __fdiv_rn(fmaxf(__fsub_rn(mx[r], mn[r]), 1e-5f), L);
-      g[r].scale = __float2half_rn(step);
-      g[r].sf = __half2float(g[r].scale);
-      g[r].rcp = __frcp_rn(g[r].sf);
-      const float zu = rne_small(__fmul_rn(-mn[r], g[r].rcp));
-      g[r].low = zu > L;
-      g[r].z = fminf(fmaxf(zu, 0.0f), L);
-    }
+  static_assert(kRowsPerLane == 2, "one row per lane of a pair");
+  const bool odd = (threadIdx.x & 1) != 0;
+  const float lo_v = odd ? mn[1] : mn[0], hi_v = odd ? mx[1] : mx[0];
+  GroupQ q;
+  if constexpr (SYM) {
+    const float half_levels = 0.5f * (L - 1.0f);   // 7 or 3, exact
+    const float step = __fdiv_rn(fmaxf(fmaxf(-lo_v, hi_v), 1e-5f), half_levels);
+    q.scale = __float2half_rn(step);
+    q.sf = __half2float(q.scale);
+    q.rcp = __frcp_rn(q.sf);
+    q.low = false;
+    q.z = 0.5f * (L + 1.0f);                        // 8 or 4, exact
+  } else {
+    const float step = __fdiv_rn(fmaxf(__fsub_rn(hi_v, lo_v), 1e-5f), L);
+    q.scale = __float2half_rn(step);
+    q.sf = __half2float(q.scale);
+    q.rcp = __frcp_rn(q.sf);
+    const float zu = rne_small(__fmul_rn(-lo_v, q.rcp));
+    q.low = zu > L;
+    q.z = fminf(fmaxf(zu, 0.0f), L);
   }
+  GroupQ o;   // the neighbour's row
+  o.sf = __shfl_xor_sync(0xFFFFFFFFu, q.sf, 1);
+  o.rcp = __shfl_xor_sync(0xFFFFFFFFu, q.rcp, 1);
+  o.z = __shfl_xor_sync(0xFFFFFFFFu, q.z, 1);
+  o.low = __shfl_xor_sync(0xFFFFFFFFu, static_cast<int>(q.low), 1) != 0;
+  o.scale = __float2half_rn(o.sf);   // exact: sf is an fp16 value
+  g[0] = odd ? o : q;
+  g[1] = odd ? q : o;
 }
 
 template <int GROUP, bool SYM>
