@@ -35,16 +35,6 @@ constexpr int kPerLane = 16;        // consecutive channels per lane
 constexpr int kRowsPerLane = 2;     // rows per lane
 
 // ---------------------------------------------------------------- helpers
-__device__ __forceinline__ void ld_v8f(const float* p, float* v) {
-  uint32_t r[8];
-  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "l"(p));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 __device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
@@ -56,21 +46,6 @@ __device__ __forceinline__ void raw_to_f32(const uint4* raw, float* w) {
 #pragma unroll
   for (int v = 0; v < 2; ++v) {
     const uint32_t u[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
-      w[8 * v + 2 * i] = f.x;
-      w[8 * v + 2 * i + 1] = f.y;
-    }
-  }
-}
-
-__device__ __forceinline__ void load_w16(const __half* p, float* w) {
-  const uint4* wp = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int v = 0; v < 2; ++v) {
-    const uint4 q = __ldg(wp + v);
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
@@ -226,14 +201,12 @@ __device__ __forceinline__ void scale16(const float* w, const float* s, float* w
   }
 }
 
-// Launch geometry shared by both kernels, without integer division:
-// blockIdx.x is a chunk of 32 lanes x kPerLane channels, and the 8 warps of a
-// block take 16 consecutive rows (two per warp) at those channels, so their
-// loads of s share L1 lines; blockIdx.y walks 16-row blocks (grid-stride).
-// Blocks are issued x-fastest, so consecutive blocks cover whole 16-row slabs
-// of W.  Lanes past the end of a row form whole groups (K % GROUP == 0), so
-// their dummy values (they re-read the row's last chunk) never meet real
-// ones in a reduction.
+// Launch geometry shared by both kernels: blockIdx.x is a chunk of 32 lanes x
+// kPerLane channels, and the 8 warps of a block take 16 consecutive rows (two
+// per warp) at those channels; blockIdx.y walks 16-row blocks (grid-stride,
+// one wave of persistent blocks).  Lanes past the end of a row form whole
+// groups (K % GROUP == 0), so their dummy values (they re-read the row's last
+// chunk) never meet real ones in a reduction.
 constexpr int kRowsPerBlock = (kQuantThreads / 32) * kRowsPerLane;
 
 struct Lane {
@@ -251,6 +224,17 @@ __device__ __forceinline__ Lane lane_chunk(int64_t K) {
   return l;
 }
 
+// ---------------------------------------------------------------- W rings
+// Both kernels stream W through per-warp rings in shared memory filled with
+// cp.async.  A warp's 512 channels of one row (1 KB) are copied as two fully
+// coalesced 512-byte requests (lane l: 16-byte chunks l and 32 + l); lane l
+// then reads its own chunks 2l and 2l + 1.  Chunk c is stored at
+// c ^ ((c / 8) % 2), so that the copies and the 16-byte reads of each
+// quarter-warp hit distinct banks.
+constexpr int kRowChunks = 32 * kPerLane / 8;   // 16-byte chunks of a warp's row segment
+
+__device__ __forceinline__ int fin_slot(int c) { return c ^ ((c >> 3) & 1); }
+
 // ---------------------------------------------------------------- residual
 // Search output: the quantization residual of every grid point, in the units
 // of W,
@@ -262,105 +246,189 @@ __device__ __forceinline__ Lane lane_chunk(int64_t K) {
 // significand); w - that * (1/s_k) is one fused multiply-add, and the one
 // coarse rounding is the final one to fp16, relative to the residual.
 //
-// A lane loads s and 1/s of a grid point once for its two rows and evaluates
-// every grid point, so W is read and converted to fp32 once.  The 8 warps of
-// a block take 16 consecutive rows at the same channels, so their 256-bit
-// loads of s and 1/s hit the same L1 lines.  Each lane writes one whole
-// 32-byte sector per row and grid point.
+//
+// Persistent blocks (two per SM) each keep one 512-channel chunk.  s and 1/s
+// of up to kResAlphaTile grid points for those channels are staged once per
+// block in shared memory; a lane reads its 16 channels' values there (16-byte
+// chunk c of a grid point's 512 channels stored at c ^ ((c / 8) % 8): the 8
+// lanes of a quarter-warp read distinct banks).  W comes through a per-warp
+// ring of kResStages row pairs, so the next row pair's loads are in flight
+// while every grid point of the current one is evaluated.  Each lane writes
+// one whole 32-byte sector per row and grid point.  More than kResAlphaTile
+// grid points are done in tiles (W is read once per tile).
+constexpr int kResAlphaTile = 20;
+constexpr int kResStages = 2;
+constexpr int kResSChunks = 32 * kPerLane / 4;                        // 16-byte chunks of s
+constexpr int kResSRBytes = kResAlphaTile * 2 * kResSChunks * 16;     // 80 KB: s and 1/s
+constexpr int kResRingBytes = (kQuantThreads / 32) * kResStages * kRowsPerLane * kRowChunks * 16;
+constexpr int kResSmem = kResSRBytes + kResRingBytes;                 // 112 KB
+
+__device__ __forceinline__ int res_slot(int c) { return c ^ ((c >> 3) & 7); }
+
 template <int GROUP, bool SYM>
 __global__ void __launch_bounds__(kQuantThreads)
     k_quant_residual(const __half* __restrict__ W, int64_t N, int64_t K, int levels,
                      const float* __restrict__ s_grid, const float* __restrict__ r_grid,
                      int n_alpha, int64_t row_off, int64_t n_pad, __half* __restrict__ delta,
                      const float2* __restrict__ rowmm) {
+  extern __shared__ uint4 res_smem[];
+  float4* s_tile = reinterpret_cast<float4*>(res_smem);      // [kResAlphaTile][kResSChunks]
+  float4* r_tile = s_tile + kResAlphaTile * kResSChunks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4* ring = reinterpret_cast<uint4*>(r_tile + kResAlphaTile * kResSChunks) +
+                warp * (kResStages * kRowsPerLane * kRowChunks);
+  const uint32_t ring_u32 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
   const float L = static_cast<float>(levels);
   const int64_t slab = n_pad * K;                     // halves per grid point
   const Lane lw = lane_chunk(K);
-  for (int64_t row0 = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + (threadIdx.x >> 5)) *
-                      kRowsPerLane;
-       row0 < N; row0 += static_cast<int64_t>(gridDim.y) * kRowsPerBlock) {
-    float w[kRowsPerLane][kPerLane];
+  const int64_t kbase = static_cast<int64_t>(blockIdx.x) * (32 * kPerLane);
+  const int64_t w_rest = (K - kbase) / 8, s_rest = (K - kbase) / 4;
+  const int w_valid = static_cast<int>(w_rest < kRowChunks ? w_rest : kRowChunks);
+  const int s_valid = static_cast<int>(s_rest < kResSChunks ? s_rest : kResSChunks);
+  const int w_mine = static_cast<int>((lw.k0 - kbase) / 8);   // the lane's 2 chunks of W
+  const int s_mine = static_cast<int>((lw.k0 - kbase) / 4);   // the lane's 4 chunks of s
+  const int64_t row_step = static_cast<int64_t>(gridDim.y) * kRowsPerBlock;
+  const int64_t first = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + warp) *
+                        kRowsPerLane;
+  const int64_t iters = first < N ? (N - first + row_step - 1) / row_step : 0;
+  auto issue = [&](int64_t it) {
+    if (it < iters) {
+      const int st = static_cast<int>(it % kResStages);
+      const int64_t row0 = first + it * row_step;
 #pragma unroll
-    for (int r = 0; r < kRowsPerLane; ++r)   // a lone last row loads itself twice
-      load_w16(W + min(row0 + r, N - 1) * K + lw.k0, w[r]);
-#pragma unroll 1
-    for (int a = 0; a < n_alpha; ++a) {
-      float sv[kPerLane], rv[kPerLane];
-      const float* sp = s_grid + static_cast<int64_t>(a) * K + lw.k0;
-      const float* rp = r_grid + static_cast<int64_t>(a) * K + lw.k0;
-      ld_v8f(sp, sv);
-      ld_v8f(sp + 8, sv + 8);
-      ld_v8f(rp, rv);
-      ld_v8f(rp + 8, rv + 8);
-      // w' = w * s is formed twice (here for the group's min / max, below for
-      // the codes) instead of being held: the same correctly rounded
-      // products, 32 fewer live registers.
-      float mn[kRowsPerLane], mx[kRowsPerLane];
-      if constexpr (GROUP == 0) {   // per-row groups: min / max of this grid point's rows
+      for (int r = 0; r < kRowsPerLane; ++r) {   // a lone last row loads itself twice
+        const __half* src = W + min(row0 + r, N - 1) * K + kbase;
 #pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r) {
-          const float2 m = rowmm[static_cast<int64_t>(a) * N + min(row0 + r, N - 1)];
-          mn[r] = m.x;
-          mx[r] = m.y;
+        for (int j = 0; j < 2; ++j) {
+          const int c = 32 * j + lane;
+          if (c < w_valid)
+            cp_async16(ring_u32 + ((st * kRowsPerLane + r) * kRowChunks + fin_slot(c)) * 16,
+                       src + 8 * c);
         }
-      } else {
-#pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r) {
-          float mnA = INFINITY, mxA = -INFINITY, mnB = INFINITY, mxB = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < kPerLane; i += 4) {
-            const f32x2 p = mul2(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
-            const f32x2 q = mul2(pack2(w[r][i + 2], w[r][i + 3]), pack2(sv[i + 2], sv[i + 3]));
-            mnA = min3f(mnA, lo2(p), hi2(p));
-            mxA = max3f(mxA, lo2(p), hi2(p));
-            mnB = min3f(mnB, lo2(q), hi2(q));
-            mxB = max3f(mxB, lo2(q), hi2(q));
-          }
-          mn[r] = fminf(mnA, mnB);
-          mx[r] = fmaxf(mxA, mxB);
-        }
-        group_reduce2<GROUP>(mn, mx);
-      }
-      GroupQ gq[kRowsPerLane];
-      group_finish2<SYM>(mn, mx, L, gq);
-      // rare: some group of the warp is all negative (both clamp sides needed)
-      const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
-#pragma unroll
-      for (int r = 0; r < kRowsPerLane; ++r) {
-        const GroupQ& g = gq[r];
-        const float lo = -g.z, hi = L - g.z;
-        const f32x2 nsf = pack2(-g.sf, -g.sf);
-        // d = clamp(rne(w' * rcp), -z, L - z): the bounds are integers, so
-        // the clamp may come before the rounding adds.
-        const f32x2 rcp2 = pack2(g.rcp, g.rcp);
-        const f32x2 magic2 = pack2(kMagic, kMagic), nmagic2 = pack2(-kMagic, -kMagic);
-        float d[kPerLane];
-#pragma unroll
-        for (int i = 0; i < kPerLane; i += 2) {
-          const f32x2 ws2 = mul2_again(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
-          const f32x2 t = mul2(ws2, rcp2);
-          float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
-          if (low) {
-            t0 = fmaxf(t0, lo);
-            t1 = fmaxf(t1, lo);
-          }
-          const f32x2 m = add2(add2(pack2(t0, t1), magic2), nmagic2);
-          d[i] = lo2(m);
-          d[i + 1] = hi2(m);
-        }
-        uint32_t o[kPerLane / 2];
-#pragma unroll
-        for (int i = 0; i < kPerLane; i += 2) {
-          // w - (d * sf) * (1/s): the product d * sf is exact.
-          const f32x2 e = fma2(mul2(pack2(d[i], d[i + 1]), nsf), pack2(rv[i], rv[i + 1]),
-                               pack2(w[r][i], w[r][i + 1]));
-          const __half2 hv = __floats2half2_rn(lo2(e), hi2(e));
-          o[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-        const int64_t row = row0 + r;
-        if (lw.active && row < N) st_v8(delta + a * slab + (row_off + row) * K + lw.k0, o);
       }
     }
+    cp_async_commit();   // possibly empty: one group per row pair
+  };
+  for (int a0 = 0; a0 < n_alpha; a0 += kResAlphaTile) {
+    const int na = n_alpha - a0 < kResAlphaTile ? n_alpha - a0 : kResAlphaTile;
+    __syncthreads();   // every warp is done with the previous tile of s and 1/s
+    for (int a = warp; a < na; a += kQuantThreads / 32) {
+      const float* sp = s_grid + static_cast<int64_t>(a0 + a) * K + kbase;
+      const float* rp = r_grid + static_cast<int64_t>(a0 + a) * K + kbase;
+      for (int c = lane; c < s_valid; c += 32) {
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(
+                       s_tile + a * kResSChunks + res_slot(c))), sp + 4 * c);
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(
+                       r_tile + a * kResSChunks + res_slot(c))), rp + 4 * c);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();   // the tile of s and 1/s is in place
+#pragma unroll
+    for (int i = 0; i < kResStages - 1; ++i) issue(i);
+    for (int64_t it = 0; it < iters; ++it) {
+      issue(it + kResStages - 1);
+      cp_async_wait<kResStages - 1>();
+      __syncwarp();   // every lane's copies of this row pair have landed
+      const int st = static_cast<int>(it % kResStages);
+      const int64_t row0 = first + it * row_step;
+      float w[kRowsPerLane][kPerLane];
+#pragma unroll
+      for (int r = 0; r < kRowsPerLane; ++r) {
+        const uint4* slot = ring + (st * kRowsPerLane + r) * kRowChunks;
+        const uint4 raw[2] = {slot[fin_slot(w_mine)], slot[fin_slot(w_mine + 1)]};
+        raw_to_f32(raw, w[r]);
+      }
+      __syncwarp();   // the slot is refilled at the next row pair
+#pragma unroll 1
+      for (int a = 0; a < na; ++a) {
+        float sv[kPerLane], rv[kPerLane];
+#pragma unroll
+        for (int q = 0; q < kPerLane / 4; ++q) {
+          const float4 fs = s_tile[a * kResSChunks + res_slot(s_mine + q)];
+          const float4 fr = r_tile[a * kResSChunks + res_slot(s_mine + q)];
+          sv[4 * q] = fs.x;
+          sv[4 * q + 1] = fs.y;
+          sv[4 * q + 2] = fs.z;
+          sv[4 * q + 3] = fs.w;
+          rv[4 * q] = fr.x;
+          rv[4 * q + 1] = fr.y;
+          rv[4 * q + 2] = fr.z;
+          rv[4 * q + 3] = fr.w;
+        }
+        const int ga = a0 + a;
+        // w' = w * s is formed twice (here for the group's min / max, below
+        // for the codes) instead of being held: the same correctly rounded
+        // products, 32 fewer live registers.
+        float mn[kRowsPerLane], mx[kRowsPerLane];
+        if constexpr (GROUP == 0) {   // per-row groups: min / max of this grid point's rows
+#pragma unroll
+          for (int r = 0; r < kRowsPerLane; ++r) {
+            const float2 m = rowmm[static_cast<int64_t>(ga) * N + min(row0 + r, N - 1)];
+            mn[r] = m.x;
+            mx[r] = m.y;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kRowsPerLane; ++r) {
+            float mnA = INFINITY, mxA = -INFINITY, mnB = INFINITY, mxB = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kPerLane; i += 4) {
+              const f32x2 p = mul2(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+              const f32x2 q = mul2(pack2(w[r][i + 2], w[r][i + 3]), pack2(sv[i + 2], sv[i + 3]));
+              mnA = min3f(mnA, lo2(p), hi2(p));
+              mxA = max3f(mxA, lo2(p), hi2(p));
+              mnB = min3f(mnB, lo2(q), hi2(q));
+              mxB = max3f(mxB, lo2(q), hi2(q));
+            }
+            mn[r] = fminf(mnA, mnB);
+            mx[r] = fmaxf(mxA, mxB);
+          }
+          group_reduce2<GROUP>(mn, mx);
+        }
+        GroupQ gq[kRowsPerLane];
+        group_finish2<SYM>(mn, mx, L, gq);
+        // rare: some group of the warp is all negative (both clamp sides needed)
+        const bool low = __any_sync(0xFFFFFFFFu, gq[0].low || gq[1].low);
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r) {
+          const GroupQ& g = gq[r];
+          const float lo = -g.z, hi = L - g.z;
+          const f32x2 nsf = pack2(-g.sf, -g.sf);
+          // d = clamp(rne(w' * rcp), -z, L - z): the bounds are integers, so
+          // the clamp may come before the rounding adds.
+          const f32x2 rcp2 = pack2(g.rcp, g.rcp);
+          const f32x2 magic2 = pack2(kMagic, kMagic), nmagic2 = pack2(-kMagic, -kMagic);
+          float d[kPerLane];
+#pragma unroll
+          for (int i = 0; i < kPerLane; i += 2) {
+            const f32x2 ws2 = mul2_again(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+            const f32x2 t = mul2(ws2, rcp2);
+            float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
+            if (low) {
+              t0 = fmaxf(t0, lo);
+              t1 = fmaxf(t1, lo);
+            }
+            const f32x2 m = add2(add2(pack2(t0, t1), magic2), nmagic2);
+            d[i] = lo2(m);
+            d[i + 1] = hi2(m);
+          }
+          uint32_t o[kPerLane / 2];
+#pragma unroll
+          for (int i = 0; i < kPerLane; i += 2) {
+            // w - (d * sf) * (1/s): the product d * sf is exact.
+            const f32x2 e = fma2(mul2(pack2(d[i], d[i + 1]), nsf), pack2(rv[i], rv[i + 1]),
+                                 pack2(w[r][i], w[r][i + 1]));
+            const __half2 hv = __floats2half2_rn(lo2(e), hi2(e));
+            o[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          const int64_t row = row0 + r;
+          if (lw.active && row < N) st_v8(delta + ga * slab + (row_off + row) * K + lw.k0, o);
+        }
+      }
+    }
+    cp_async_wait<0>();
   }
 }
 
@@ -384,11 +452,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 // 2l and 2l + 1, stored at chunk ^ ((chunk / 8) % 2) so that both the
 // copies and the 16-byte reads of each quarter-warp hit distinct banks.
 constexpr int kFinStages = 4;
-constexpr int kFinChunks = 32 * kPerLane / 8;                      // 16-byte chunks per row
-constexpr int kFinSmem = (kQuantThreads / 32) * kFinStages * kRowsPerLane * kFinChunks * 16;
+constexpr int kFinSmem = (kQuantThreads / 32) * kFinStages * kRowsPerLane * kRowChunks * 16;
 static_assert(kFinSmem == 64 * 1024, "ring size");
-
-__device__ __forceinline__ int fin_slot(int c) { return c ^ ((c >> 3) & 1); }
 
 template <int BITS, int GROUP, bool SYM>
 __global__ void __launch_bounds__(kQuantThreads, 3)
@@ -406,9 +471,9 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
   const Lane lw = lane_chunk(K);
   const int64_t kbase = static_cast<int64_t>(blockIdx.x) * (32 * kPerLane);
   const int64_t rest = (K - kbase) / 8;
-  const int valid = static_cast<int>(rest < kFinChunks ? rest : kFinChunks);
+  const int valid = static_cast<int>(rest < kRowChunks ? rest : kRowChunks);
   const int mine = static_cast<int>((lw.k0 - kbase) / 8);   // first of the lane's two chunks
-  uint4* ring = fin_ring + warp * (kFinStages * kRowsPerLane * kFinChunks);
+  uint4* ring = fin_ring + warp * (kFinStages * kRowsPerLane * kRowChunks);
   const uint32_t ring_u32 = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
   const int64_t row_step = static_cast<int64_t>(gridDim.y) * kRowsPerBlock;
   const int64_t first = (static_cast<int64_t>(blockIdx.y) * (kQuantThreads / 32) + warp) *
@@ -425,7 +490,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
         for (int j = 0; j < 2; ++j) {
           const int c = 32 * j + lane;
           if (c < valid)
-            cp_async16(ring_u32 + ((st * kRowsPerLane + r) * kFinChunks + fin_slot(c)) * 16,
+            cp_async16(ring_u32 + ((st * kRowsPerLane + r) * kRowChunks + fin_slot(c)) * 16,
                        src + 8 * c);
         }
       }
@@ -453,7 +518,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     uint4 raw[kRowsPerLane][2];
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r) {
-      const uint4* slot = ring + (st * kRowsPerLane + r) * kFinChunks;
+      const uint4* slot = ring + (st * kRowsPerLane + r) * kRowChunks;
       raw[r][0] = slot[fin_slot(mine)];
       raw[r][1] = slot[fin_slot(mine + 1)];
     }
@@ -633,12 +698,6 @@ __global__ void k_unpack(const uint32_t* __restrict__ codes, int64_t N, int64_t 
   }
 }
 
-dim3 quant_grid(int64_t N, int64_t K) {
-  const int64_t gx = ceil_div(K / kPerLane, 32);
-  const int64_t gy = std::min<int64_t>(ceil_div(N, kRowsPerBlock), 65535);
-  return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(std::max<int64_t>(gy, 1)));
-}
-
 template <int BITS, int GROUP, bool SYM>
 cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, const int* sel,
                          uint32_t* codes, __half* scales, uint8_t* zeros, const float2* rowmm,
@@ -688,12 +747,32 @@ cudaError_t launch_row_minmax(const __half* W, int64_t N, int64_t K, const float
 }
 
 template <int GROUP, bool SYM>
-void launch_residual_t(dim3 grid, cudaStream_t st, const __half* W, int64_t N, int64_t K,
-                       int levels, const float* s_grid, const float* r_grid, int n_alpha,
-                       int64_t row_off, int64_t n_pad, __half* delta, const float2* rowmm) {
-  k_quant_residual<GROUP, SYM><<<grid, kQuantThreads, 0, st>>>(W, N, K, levels, s_grid, r_grid,
-                                                               n_alpha, row_off, n_pad, delta,
-                                                               rowmm);
+cudaError_t launch_residual_t(cudaStream_t st, const __half* W, int64_t N, int64_t K, int levels,
+                              const float* s_grid, const float* r_grid, int n_alpha,
+                              int64_t row_off, int64_t n_pad, __half* delta, const float2* rowmm) {
+  auto kern = k_quant_residual<GROUP, SYM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kResSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148, per_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQuantThreads, kResSmem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  // One wave of resident blocks, each with a 512-channel chunk and an equal
+  // share of the 16-row blocks.
+  const int64_t gx = ceil_div(K / kPerLane, 32);
+  const int64_t row_blocks = ceil_div(N, kRowsPerBlock);
+  int64_t gy = std::max<int64_t>(1, (static_cast<int64_t>(per_sm) * sms) / gx);
+  gy = std::min<int64_t>(gy, row_blocks);
+  gy = ceil_div(row_blocks, ceil_div(row_blocks, gy));
+  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kQuantThreads, kResSmem,
+         st>>>(W, N, K, levels, s_grid, r_grid, n_alpha, row_off, n_pad, delta, rowmm);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -703,25 +782,23 @@ cudaError_t launch_quant_residual(const __half* W, int64_t N, int64_t K, int bit
                                   int n_alpha, int64_t row_off, int64_t n_pad, __half* delta,
                                   float2* rowmm, cudaStream_t st) {
   const int levels = (1 << bits) - 1;
-  const dim3 grid = quant_grid(N, K);
   const bool sym = zero_point == 0;
   if (group == -1) {
     cudaError_t e = launch_row_minmax(W, N, K, s_grid, nullptr, n_alpha, rowmm, st);
     if (e != cudaSuccess) return e;
   }
   auto go = [&](auto g, auto y) {
-    launch_residual_t<decltype(g)::value, decltype(y)::value>(
-        grid, st, W, N, K, levels, s_grid, r_grid, n_alpha, row_off, n_pad, delta, rowmm);
+    return launch_residual_t<decltype(g)::value, decltype(y)::value>(
+        st, W, N, K, levels, s_grid, r_grid, n_alpha, row_off, n_pad, delta, rowmm);
   };
   using I128 = std::integral_constant<int, 128>;
   using I64 = std::integral_constant<int, 64>;
   using I0 = std::integral_constant<int, 0>;
   using T = std::true_type;
   using F = std::false_type;
-  if (group == 128) sym ? go(I128{}, T{}) : go(I128{}, F{});
-  else if (group == 64) sym ? go(I64{}, T{}) : go(I64{}, F{});
-  else sym ? go(I0{}, T{}) : go(I0{}, F{});
-  return cudaGetLastError();
+  if (group == 128) return sym ? go(I128{}, T{}) : go(I128{}, F{});
+  if (group == 64) return sym ? go(I64{}, T{}) : go(I64{}, F{});
+  return sym ? go(I0{}, T{}) : go(I0{}, F{});
 }
 
 cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, int group,
