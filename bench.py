@@ -290,6 +290,11 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     nbytes = 2 * T * K
     out["stats"] = {"shape": f"X {T}x{K} fp16", "ms": ms, "bytes": nbytes,
                     "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
+    # Context, not a denominator: a library reduction (torch.amax) reading the
+    # same bytes -- the rate a plain read-only pass reaches at this size.
+    ms = timed(lambda: torch.amax(X))
+    out["read_only_context"] = {"X": {"bytes": nbytes, "ms": ms, "gbs": nbytes / ms / 1e6,
+                                      "kernel": "torch.amax"}}
     del X
     N, K = 28672, 8192
     W = (torch.randn(N, K, generator=g, device=dev) * 0.015).half()
@@ -304,6 +309,9 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     nbytes = 2 * N * K + N * K // 2 + 3 * N * K // 128
     out["quantize_pack"] = {"shape": f"W {N}x{K} fp16 -> INT4 g128", "ms": ms, "bytes": nbytes,
                             "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
+    ms = timed(lambda: torch.amax(W))
+    out["read_only_context"]["W"] = {"bytes": 2 * N * K, "ms": ms, "gbs": 2 * N * K / ms / 1e6,
+                                     "kernel": "torch.amax"}
     # The packed layer consumed at decode: W4A16 product for one token, and a
     # cuBLAS fp16 GEMV on the dense weight of the same shape for context.
     x = torch.randn(1, K, generator=g, device=dev).half()
@@ -434,22 +442,32 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
             n, k = W.shape
             d2h += awq.packed_words(n, k, bits) * 4 + 3 * n * (k // group)
         d2h += X.shape[1] * 4 + N_GRID * 8
+    # Steps run through search_host_stream: step i+1's inputs are copied in
+    # and step i-1's results copied out while step i is searched.  Every step
+    # still copies its own inputs in and its results out inside the timed
+    # region; the region spans all steps, pipeline fill and drain included.
     e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        for X, Ws, bits, group in host_calls:
-            awq.search_host(X, Ws, bits, group, N_GRID, device=dev)
+    by_cfg = {}
+    for X, Ws, bits, group in host_calls:
+        by_cfg.setdefault((bits, group), []).append((X, Ws))
+
+    def e2e_pass(n_steps):
+        for (bits, group), calls in by_cfg.items():
+            awq.search_host_stream(calls * n_steps, bits, group, N_GRID, device=dev)
+
+    # Warm-up with as many steps as are timed: the pinned host buffers the
+    # results land in come from torch's caching host allocator, so the timed
+    # pass does not pay for page-locking fresh memory.
+    e2e_pass(e2e_steps)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e2e_ms = 0.0
-    for i in range(e2e_steps):
-        flush.fill_(i)
-        e0.record(stream)
-        for X, Ws, bits, group in host_calls:
-            awq.search_host(X, Ws, bits, group, N_GRID, device=dev)
-        e1.record(stream)
-        e1.synchronize()
-        e2e_ms += e0.elapsed_time(e1)
+    flush.fill_(0)
+    e0.record(stream)
+    e2e_pass(e2e_steps)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
     t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)

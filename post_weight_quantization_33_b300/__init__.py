@@ -21,7 +21,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import List, Optional, Sequence
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 import torch
@@ -356,6 +356,32 @@ class SearchResult:
                       (self.Ns[i], groups_per_row(self.K, self.group)), "|u1",
                       self.device).clone()
 
+    def host_values(self) -> dict:
+        """best, alpha, losses and the status check, without synchronising
+        the stream: valid once the search's work has completed (the caller
+        waits on an event recorded after it)."""
+        h = self._handle()
+        _check(lib().awq_result_check(h))
+        p = lib().awq_result_losses(h)
+        return {"best": int(lib().awq_result_best_index(h)),
+                "alpha": float(lib().awq_result_alpha(h)),
+                "losses": np.array([p[i] for i in range(self.n_grid)], dtype=np.float64)}
+
+    def device_views(self) -> dict:
+        """Library-owned device tensors (no copy) of s and of each weight's
+        codes, scales and zeros; valid until free()."""
+        h = self._handle()
+        gpr = groups_per_row(self.K, self.group)
+        return {
+            "s": _alias(lib().awq_result_s(h), (self.K,), "<f4", self.device),
+            "codes": [_alias(lib().awq_result_codes(h, i), (packed_words(n, self.K, self.bits),),
+                             "<i4", self.device) for i, n in enumerate(self.Ns)],
+            "scales": [_alias(lib().awq_result_scales(h, i), (n, gpr), "<f2", self.device)
+                       for i, n in enumerate(self.Ns)],
+            "zeros": [_alias(lib().awq_result_zeros(h, i), (n, gpr), "|u1", self.device)
+                      for i, n in enumerate(self.Ns)],
+        }
+
     @property
     def kernel_launches(self) -> int:
         return int(lib().awq_result_kernel_launches(self._handle()))
@@ -431,6 +457,93 @@ def search_host(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, grou
         out["alpha"] = r.alpha
     finally:
         r.free()
+    return out
+
+
+def search_host_stream(calls: Sequence[Tuple[torch.Tensor, Sequence[torch.Tensor]]],
+                       bits: int = 4, group: int = 128, n_grid: int = 20, device="cuda",
+                       zero_point: bool = True) -> List[dict]:
+    """search_host over a sequence of layers ``(X, [W, ...])`` in host memory
+    (pinned for asynchronous copies), pipelined over three streams: while
+    layer i is searched, layer i+1's inputs are copied in and layer i-1's
+    results are copied out.  Device inputs are double-buffered; each result is
+    freed (stream-ordered) after its copy-out.  Returns one dict per layer,
+    as search_host does."""
+    device = torch.device(device)
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    calls = [(X, list(Ws)) for X, Ws in calls]
+    if not calls:
+        return []
+    compute = torch.cuda.current_stream(device)
+    s_in = torch.cuda.Stream(device)
+    s_out = torch.cuda.Stream(device)
+    # Two input slots sized for the largest layer, allocated on the compute
+    # stream before any copy (no allocator traffic inside the pipeline).
+    x_max = max(X.numel() for X, _ in calls)
+    w_max = max(sum(W.numel() for W in Ws) for _, Ws in calls)
+    with torch.cuda.device(device):
+        slots = [(torch.empty(x_max, dtype=torch.float16, device=device),
+                  torch.empty(w_max, dtype=torch.float16, device=device)) for _ in range(2)]
+    slot_free = [None, None]
+    pending = []
+    out: List[dict] = [None] * len(calls)
+
+    def retire(item):
+        idx, r, done, copied, host = item
+        done.synchronize()                    # this search only, not the stream
+        try:
+            host.update(r.host_values())
+        finally:
+            compute.wait_event(copied)        # the free follows the copy-out
+            with torch.cuda.stream(compute):
+                r.free()
+        copied.synchronize()
+        out[idx] = host
+
+    for i, (X, Ws) in enumerate(calls):
+        k = i % 2
+        xs, ws = slots[k]
+        with torch.cuda.stream(s_in):
+            if slot_free[k] is not None:
+                s_in.wait_event(slot_free[k])
+            Xd = xs[:X.numel()].view(X.shape)
+            Xd.copy_(X, non_blocking=True)
+            Wd, off = [], 0
+            for W in Ws:
+                Wd.append(ws[off:off + W.numel()].view(W.shape))
+                Wd[-1].copy_(W, non_blocking=True)
+                off += W.numel()
+            ready = torch.cuda.Event()
+            ready.record(s_in)
+        compute.wait_event(ready)
+        with torch.cuda.stream(compute):
+            r = search(Xd, Wd, bits, group, n_grid, zero_point=zero_point)
+            done = torch.cuda.Event()
+            done.record(compute)
+        slot_free[k] = done
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            v = r.device_views()
+
+            def pinned_copy(t):
+                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                h.copy_(t, non_blocking=True)
+                return h
+
+            host = {
+                "codes": [pinned_copy(t) for t in v["codes"]],
+                "scales": [pinned_copy(t) for t in v["scales"]],
+                "zeros": [pinned_copy(t) for t in v["zeros"]],
+                "s": pinned_copy(v["s"]),
+            }
+            copied = torch.cuda.Event()
+            copied.record(s_out)
+        pending.append((i, r, done, copied, host))
+        if len(pending) > 1:
+            retire(pending.pop(0))
+    while pending:
+        retire(pending.pop(0))
     return out
 
 

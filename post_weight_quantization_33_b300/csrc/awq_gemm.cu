@@ -563,20 +563,14 @@ bool make_tmap_f16(CUtensorMap* m, const void* base, int64_t depth, int64_t rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
-}
-
 cudaError_t launch_ref(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
                        cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_ref, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
+  LaunchFacts lf;
+  cudaError_t e = launch_facts(reinterpret_cast<const void*>(k_gemm_ref), kThreads,
+                               static_cast<int>(SMEM_BYTES), &lf);
   if (e != cudaSuccess) return e;
   const int total = args.num_m_tiles * args.num_n_tiles;
-  const int grid = total < sm_count() ? total : sm_count();
+  const int grid = total < lf.sms ? total : lf.sms;
   k_gemm_ref<<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, args);
   return cudaGetLastError();
 }
@@ -600,26 +594,13 @@ bool make_residual_tmap(CUtensorMap* ta, const __half* delta, int64_t K, int64_t
 template <bool kGram>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const PairArgs& a,
                         cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_err_pair<kGram>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(P_SMEM_BYTES));
-  if (e != cudaSuccess) return e;
   // One pair per co-resident cluster slot (persistent), at most one per tile.
   const int64_t tiles = static_cast<int64_t>(a.num_mp) * a.num_n_tiles * a.num_alpha;
-  int clusters = sm_count() / 2;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm_err_pair<kGram>, &cfg) ==
-            cudaSuccess &&
-        max_clusters > 0)
-      clusters = std::min(clusters, max_clusters);
-    else
-      cudaGetLastError();
-  }
+  int max_clusters = 0;
+  cudaError_t e = cluster_facts(reinterpret_cast<const void*>(k_gemm_err_pair<kGram>), kThreads,
+                                static_cast<int>(P_SMEM_BYTES), &max_clusters);
+  if (e != cudaSuccess) return e;
+  const int clusters = std::min(device_sm_count() / 2, max_clusters);
   const int pairs = static_cast<int>(std::min<int64_t>(clusters, tiles));
   k_gemm_err_pair<kGram><<<2 * pairs, kThreads, P_SMEM_BYTES, st>>>(ta, tb, a);
   return cudaGetLastError();

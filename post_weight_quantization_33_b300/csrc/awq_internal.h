@@ -130,4 +130,17 @@ cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, 
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Launch facts of a kernel on the current device, looked up once per
+// (device, kernel, threads, dynamic shared memory) and cached: the SM count
+// and the blocks resident per SM.  The first lookup raises the kernel's
+// dynamic shared memory limit to `smem`.
+struct LaunchFacts {
+  int sms;
+  int per_sm;
+};
+cudaError_t launch_facts(const void* fn, int threads, int smem, LaunchFacts* out);
+// Co-resident clusters of a kernel compiled with cluster dimensions (cached).
+cudaError_t cluster_facts(const void* fn, int threads, int smem, int* max_clusters);
+int device_sm_count();
+
 }  // namespace awq

@@ -184,21 +184,12 @@ cudaError_t launch_mv_m(int group, const uint32_t* codes, const __half* scales,
   int64_t kc = (kMvSmemBytes / (M * 4)) / 256 * 256;
   if (kc >= K) kc = K;
   const int smem = static_cast<int>(M * kc * 4);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    LaunchFacts lf;   // resident blocks per SM: one wave of persistent blocks
+    cudaError_t e = launch_facts(reinterpret_cast<const void*>(kern), kMvThreads, smem, &lf);
     if (e != cudaSuccess) return e;
-    int per_sm = 1;   // resident blocks per SM: one wave of persistent blocks
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMvThreads, smem) !=
-            cudaSuccess ||
-        per_sm < 1) {
-      cudaGetLastError();
-      per_sm = 1;
-    }
     const int64_t blocks =
-        std::min<int64_t>(ceil_div(N, kMvRowsPerBlock), static_cast<int64_t>(per_sm) * sms);
+        std::min<int64_t>(ceil_div(N, kMvRowsPerBlock), static_cast<int64_t>(lf.per_sm) * lf.sms);
     kern<<<static_cast<unsigned>(blocks), kMvThreads, smem, st>>>(codes, scales, zeros, N, K, x, y,
                                                                   kc);
     return cudaGetLastError();

@@ -703,18 +703,10 @@ cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, 
                          uint32_t* codes, __half* scales, uint8_t* zeros, const float2* rowmm,
                          cudaStream_t st) {
   auto kern = k_quant_final<BITS, GROUP, SYM>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kFinSmem);
+  LaunchFacts lf;
+  cudaError_t e = launch_facts(reinterpret_cast<const void*>(kern), kQuantThreads, kFinSmem, &lf);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 148, per_sm = 1;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQuantThreads, kFinSmem) !=
-          cudaSuccess ||
-      per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
+  const int sms = lf.sms, per_sm = lf.per_sm;
   // One wave of resident blocks: every block keeps a 512-channel chunk and
   // takes an equal share of the 16-row blocks.
   const int64_t gx = ceil_div(K / kPerLane, 32);
@@ -751,18 +743,10 @@ cudaError_t launch_residual_t(cudaStream_t st, const __half* W, int64_t N, int64
                               const float* s_grid, const float* r_grid, int n_alpha,
                               int64_t row_off, int64_t n_pad, __half* delta, const float2* rowmm) {
   auto kern = k_quant_residual<GROUP, SYM>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kResSmem);
+  LaunchFacts lf;
+  cudaError_t e = launch_facts(reinterpret_cast<const void*>(kern), kQuantThreads, kResSmem, &lf);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 148, per_sm = 1;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQuantThreads, kResSmem) !=
-          cudaSuccess ||
-      per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
+  const int sms = lf.sms, per_sm = lf.per_sm;
   // One wave of resident blocks, each with a 512-channel chunk and an equal
   // share of the 16-row blocks.
   const int64_t gx = ceil_div(K / kPerLane, 32);

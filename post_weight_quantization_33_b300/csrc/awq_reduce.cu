@@ -3,8 +3,10 @@
 // AWQ Explained (multigrid.ai), "How the scale is chosen": alpha* is the
 // argmin over the grid of the layer-output error.  The error is the squared
 // norm divided by N*T; weights sharing one X add their losses.  Every sum
-// here runs in a fixed order in fp64, so the result is deterministic; the
-// argmin takes the first minimum and treats NaN as +inf.
+// here runs in a fixed order, so the result is deterministic: in fp64, except
+// the per-row sums over token tiles, which are compensated fp32 (about 2^-48
+// relative) because this part has little fp64 throughput.  The argmin takes
+// the first minimum and treats NaN as +inf.
 #include "awq_internal.h"
 
 namespace awq {
@@ -14,7 +16,7 @@ constexpr int kLossRows = 256;   // rows per block (a chunk)
 
 // Block (c, a): rows [256c, 256c + 256) of the padded row space, grid point
 // a.  Per row: the sum over token tiles of partials[a][tile][row], in tile
-// order, times *row_scale when given (the Gram form's scale), written to
+// order (compensated fp32, then fp64), times *row_scale when given (the Gram form's scale), written to
 // row_losses; per weight present in the chunk: the sum of
 // its rows by a fixed tree, written to chunk_sums[a][c][w].  The last block
 // to finish (counted on *counter, zeroed by the caller) adds the chunks of
@@ -41,8 +43,19 @@ __global__ void __launch_bounds__(kLossRows)
   const bool real = v < n_pad && n < map.rows[w];
   double row = 0.0;
   if (real) {
+    // Sum over token tiles in tile order, compensated: s + c carries the
+    // sum to about 2^-48 relative (each TwoSum error term is exact), and only
+    // one fp64 add per row remains -- this part has little fp64 throughput.
     const float* pa = partials + static_cast<int64_t>(a) * n_tiles * n_pad + v;
-    for (int t = 0; t < n_tiles; ++t) row += static_cast<double>(pa[static_cast<int64_t>(t) * n_pad]);
+    float s = 0.f, c = 0.f;
+    for (int t = 0; t < n_tiles; ++t) {
+      const float x = pa[static_cast<int64_t>(t) * n_pad];
+      const float sn = __fadd_rn(s, x);
+      const float bp = __fsub_rn(sn, s);
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, __fsub_rn(sn, bp)), __fsub_rn(x, bp)));
+      s = sn;
+    }
+    row = static_cast<double>(s) + static_cast<double>(c);
     if (row_scale != nullptr) row *= *row_scale;
     row_losses[static_cast<int64_t>(a) * n_total + map.cum[w] + n] = row;
   }
@@ -73,14 +86,16 @@ __global__ void __launch_bounds__(kLossRows)
   if (!last) return;
   __threadfence();
   // Final reduction: thread i handles grid point i (n_grid <= 64 <= 256).
-  const volatile double* vcs = chunk_sums;
+  // The other blocks' chunk sums are read from L2 (__ldcg: not through this
+  // SM's L1), several loads in flight, added in chunk order.
   if (threadIdx.x < n_grid) {
     const int ga = threadIdx.x;
     double total = 0.0;
     for (int wi = 0; wi < map.n_w; ++wi) {
       double sw = 0.0;
+#pragma unroll 8
       for (int ci = 0; ci < n_chunks; ++ci)
-        sw += vcs[(static_cast<int64_t>(ga) * n_chunks + ci) * map.n_w + wi];
+        sw += __ldcg(chunk_sums + (static_cast<int64_t>(ga) * n_chunks + ci) * map.n_w + wi);
       total += sw / (static_cast<double>(map.rows[wi]) * static_cast<double>(T));
     }
     losses[ga] = total;

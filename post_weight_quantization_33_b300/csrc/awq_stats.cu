@@ -218,18 +218,19 @@ __global__ void k_scales(const double* __restrict__ sX, int64_t K, int n_grid,
 
 cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
                                     unsigned long long* acc, cudaStream_t st) {
+  LaunchFacts lf;
+  cudaError_t e = launch_facts(reinterpret_cast<const void*>(k_stats_accumulate), kStatsThreads,
+                               kStatSmem, &lf);
+  if (e != cudaSuccess) return e;
   const int64_t kchunks = K / 8;
   const int64_t gx = ceil_div(kchunks, 32);
-  // About three resident blocks per SM (148 SMs; 64 KB of ring each) in one
-  // wave; token slices a multiple of 32 rows (8 warps x 4 tokens per step).
-  int64_t gy = std::max<int64_t>(1, ceil_div(148 * 3, gx));
+  // About one wave of resident blocks (64 KB of ring each); token slices a
+  // multiple of 32 rows (8 warps x 4 tokens per step).
+  int64_t gy = std::max<int64_t>(1, ceil_div(static_cast<int64_t>(lf.per_sm) * lf.sms, gx));
   int64_t rows = ceil_div(T, gy);
   rows = std::max<int64_t>(32, ceil_div(rows, 32) * 32);
   gy = ceil_div(T, rows);
-  cudaError_t e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long) * K, st);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_stats_accumulate, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kStatSmem);
+  e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long) * K, st);
   if (e != cudaSuccess) return e;
   k_stats_accumulate<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
                        kStatsThreads, kStatSmem, st>>>(reinterpret_cast<const uint4*>(X), T,
@@ -254,7 +255,8 @@ cudaError_t launch_sx_range(const double* sX, int64_t K, unsigned long long* ran
 
 cudaError_t launch_scales(const double* sX, int64_t K, int n_grid,
                           const unsigned long long* range, float* s, float* r, cudaStream_t st) {
-  k_scales<<<static_cast<unsigned>(ceil_div(K, 128)), 128, 0, st>>>(sX, K, n_grid, range, s, r);
+  // One warp per block: the fp64 logs and exps run on as many SMs as possible.
+  k_scales<<<static_cast<unsigned>(ceil_div(K, 32)), 32, 0, st>>>(sX, K, n_grid, range, s, r);
   return cudaGetLastError();
 }
 
