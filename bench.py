@@ -328,6 +328,25 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     return out
 
 
+# --------------------------------------------------------------------------- ranks
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The largest of the ranks' timed milliseconds: an all-reduce (MAX) over
+    the process group when world > 1 (a CUDA tensor for nccl, a CPU one for
+    gloo), else ms itself."""
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Units all ranks processed per second: every rank runs the same steps
+    on its own replica (weak scaling), timed by the slowest rank."""
+    return units_per_rank_step * steps * world / (max_ms / 1e3)
+
+
 # --------------------------------------------------------------------------- arms
 def run_reference(args, rank: int, world: int) -> None:
     if rank != 0:
@@ -424,12 +443,8 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
                 stage_sum[name] += st[name]
             r.free()
     awq.set_stage_timing(False)
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    value = weights_per_step * args.steps * world / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = whole_job_rate(weights_per_step, args.steps, world, total_ms)
 
     # End to end through the public API with host (pinned) buffers.
     host_calls = [(torch.from_numpy(data[c.x]).pin_memory(),
@@ -467,11 +482,8 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     e2e_pass(e2e_steps)
     e1.record(stream)
     e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = weights_per_step * e2e_steps * world / (float(t.item()) / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = whole_job_rate(weights_per_step, e2e_steps, world, e2e_ms)
 
     if rank != 0:
         return
