@@ -338,12 +338,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.num_mp * p.num_n_tiles * p.num_alpha;
+  // Token (column) tile fastest: the pairs working at one time share a few
+  // residual row tiles, each read from HBM once while all its token tiles
+  // consume it, and X (or Gs) stays in L2.
   auto decode = [&](int tile, int& a, int& nt, int& mp) {
     const int per_alpha = p.num_mp * p.num_n_tiles;
     a = tile / per_alpha;
     const int rem = tile - a * per_alpha;
-    nt = rem / p.num_mp;
-    mp = rem - nt * p.num_mp;
+    mp = rem / p.num_n_tiles;
+    nt = rem - mp * p.num_n_tiles;
   };
 
   if (warp == kProducerWarp) {
