@@ -284,6 +284,7 @@ struct PairArgs {
   int* status;
   const __half* delta;   // Gram form: the residual [alpha][n_pad][K] (the epilogue's weights)
   int64_t K;             // Gram form: channels (columns of Gs and of delta)
+  int group_rows;        // tile order: row tiles per group (see pair_group_rows)
 };
 
 // kGram: the B operand is Gs (K x K) instead of X, and the epilogue forms
@@ -338,15 +339,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.num_mp * p.num_n_tiles * p.num_alpha;
-  // Token (column) tile fastest: the pairs working at one time share a few
-  // residual row tiles, each read from HBM once while all its token tiles
-  // consume it, and X (or Gs) stays in L2.
+  // Tile order (grid point, group of group_rows row tiles, column tile, row
+  // tile in the group): the pairs working at one time share a few residual
+  // row tiles and a few column tiles of X (or Gs), each read from HBM about
+  // once per group.  group_rows = 1 walks every column tile of one row tile
+  // before the next (X stays in L2 when it fits there).
   auto decode = [&](int tile, int& a, int& nt, int& mp) {
     const int per_alpha = p.num_mp * p.num_n_tiles;
     a = tile / per_alpha;
     const int rem = tile - a * per_alpha;
-    mp = rem / p.num_n_tiles;
-    nt = rem - mp * p.num_n_tiles;
+    const int per_group = p.group_rows * p.num_n_tiles;
+    const int g = rem / per_group;
+    const int r2 = rem - g * per_group;
+    const int rows = min(p.group_rows, p.num_mp - g * p.group_rows);
+    nt = r2 / rows;
+    mp = g * p.group_rows + (r2 - nt * rows);
   };
 
   if (warp == kProducerWarp) {
@@ -627,6 +634,18 @@ cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, i
   return launch_ref(ta, tb, a, st);
 }
 
+// Row tiles per group of the tile order.  When the B operand (X, or Gs) fits
+// comfortably in L2 it stays there, and one row tile at a time (all its column
+// tiles) reads each residual tile once.  Otherwise as many row tiles as fit
+// in an L2 budget share each column tile of B, so B is read once per group.
+static int pair_group_rows(int64_t b_rows, int64_t K, int num_mp) {
+  constexpr int64_t kL2Budget = 48ll << 20;   // of the 126 MB L2
+  if (b_rows * K * 2 <= kL2Budget) return 1;
+  const int64_t row_tile_bytes = 2ll * PM * K * 2;   // one 256-row residual tile
+  const int64_t g = std::max<int64_t>(1, kL2Budget / row_tile_bytes);
+  return static_cast<int>(std::min<int64_t>(g, num_mp));
+}
+
 cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
                               int64_t n_pad, int n_alpha, float* partials, int* status,
                               cudaStream_t st) {
@@ -644,6 +663,7 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
   a.n_pad = n_pad;
   a.partials = partials;
   a.status = status;
+  a.group_rows = pair_group_rows(T, K, a.num_mp);
   return launch_pair<false>(ta, tb, a, st);
 }
 
@@ -665,6 +685,7 @@ cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_
   a.status = status;
   a.delta = delta;
   a.K = K;
+  a.group_rows = pair_group_rows(K, K, a.num_mp);
   return launch_pair<true>(ta, tb, a, st);
 }
 
