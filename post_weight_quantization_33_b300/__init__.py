@@ -501,49 +501,59 @@ def search_host_stream(calls: Sequence[Tuple[torch.Tensor, Sequence[torch.Tensor
         copied.synchronize()
         out[idx] = host
 
-    for i, (X, Ws) in enumerate(calls):
-        k = i % 2
-        xs, ws = slots[k]
-        with torch.cuda.stream(s_in):
-            if slot_free[k] is not None:
-                s_in.wait_event(slot_free[k])
-            Xd = xs[:X.numel()].view(X.shape)
-            Xd.copy_(X, non_blocking=True)
-            Wd, off = [], 0
-            for W in Ws:
-                Wd.append(ws[off:off + W.numel()].view(W.shape))
-                Wd[-1].copy_(W, non_blocking=True)
-                off += W.numel()
-            ready = torch.cuda.Event()
-            ready.record(s_in)
-        compute.wait_event(ready)
-        with torch.cuda.stream(compute):
-            r = search(Xd, Wd, bits, group, n_grid, zero_point=zero_point)
-            done = torch.cuda.Event()
-            done.record(compute)
-        slot_free[k] = done
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done)
-            v = r.device_views()
+    try:
+        for i, (X, Ws) in enumerate(calls):
+            k = i % 2
+            xs, ws = slots[k]
+            with torch.cuda.stream(s_in):
+                if slot_free[k] is not None:
+                    s_in.wait_event(slot_free[k])
+                Xd = xs[:X.numel()].view(X.shape)
+                Xd.copy_(X, non_blocking=True)
+                Wd, off = [], 0
+                for W in Ws:
+                    Wd.append(ws[off:off + W.numel()].view(W.shape))
+                    Wd[-1].copy_(W, non_blocking=True)
+                    off += W.numel()
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            compute.wait_event(ready)
+            with torch.cuda.stream(compute):
+                r = search(Xd, Wd, bits, group, n_grid, zero_point=zero_point)
+                done = torch.cuda.Event()
+                done.record(compute)
+            slot_free[k] = done
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                v = r.device_views()
 
-            def pinned_copy(t):
-                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                h.copy_(t, non_blocking=True)
-                return h
+                def pinned_copy(t):
+                    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    h.copy_(t, non_blocking=True)
+                    return h
 
-            host = {
-                "codes": [pinned_copy(t) for t in v["codes"]],
-                "scales": [pinned_copy(t) for t in v["scales"]],
-                "zeros": [pinned_copy(t) for t in v["zeros"]],
-                "s": pinned_copy(v["s"]),
-            }
-            copied = torch.cuda.Event()
-            copied.record(s_out)
-        pending.append((i, r, done, copied, host))
-        if len(pending) > 1:
+                host = {
+                    "codes": [pinned_copy(t) for t in v["codes"]],
+                    "scales": [pinned_copy(t) for t in v["scales"]],
+                    "zeros": [pinned_copy(t) for t in v["zeros"]],
+                    "s": pinned_copy(v["s"]),
+                }
+                copied = torch.cuda.Event()
+                copied.record(s_out)
+            pending.append((i, r, done, copied, host))
+            if len(pending) > 1:
+                retire(pending.pop(0))
+        while pending:
             retire(pending.pop(0))
-    while pending:
-        retire(pending.pop(0))
+    except BaseException:
+        # A failed call: let the searches already enqueued finish, then free
+        # their results, so nothing is left pending on the device.
+        for _, r, done, copied, _ in pending:
+            try:
+                copied.synchronize()
+            finally:
+                r.free()
+        raise
     return out
 
 

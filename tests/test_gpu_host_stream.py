@@ -62,3 +62,20 @@ def test_search_host_stream_empty_and_single():
     assert g["best"] == ref["best"]
     assert np.array_equal(g["losses"], ref["losses"])
     assert torch.equal(g["codes"][0], ref["codes"][0])
+
+
+def test_search_host_stream_failure_frees_in_flight_results():
+    """A layer that fails validation in the middle of the sequence raises;
+    the layers already in flight are completed and freed, and the library
+    keeps working."""
+    layers = _layers()[:3]
+    X, Ws = layers[1]
+    bad_W = Ws[0][:, : X.shape[1] // 2].contiguous().pin_memory()   # K does not match X
+    seq = [layers[0], (X, [bad_W]), layers[2]]
+    with pytest.raises(ValueError):
+        awq.search_host_stream(seq, 4, 128)
+    torch.cuda.synchronize()
+    got = awq.search_host_stream(layers, 4, 128)
+    ref = awq.search_host(*layers[2], 4, 128)
+    assert np.array_equal(got[2]["losses"], ref["losses"])
+    assert torch.equal(got[2]["codes"][0], ref["codes"][0])
