@@ -77,7 +77,7 @@ extern "C" {
 typedef enum awq_status {
   AWQ_OK = 0,
   AWQ_ERR_INVALID = 1,     /* bad argument (null, misaligned, host pointer, bad size) */
-  AWQ_ERR_UNSUPPORTED = 2, /* well-formed configuration this build does not implement */
+  AWQ_ERR_UNSUPPORTED = 2, /* well-formed configuration this library does not implement */
   AWQ_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
   AWQ_ERR_OOM = 4,         /* device memory exhausted */
   AWQ_ERR_TIMEOUT = 5      /* a bounded device-side wait expired */

@@ -34,7 +34,7 @@ it follows.  Pages (by title):
   the layer's input (the preceding LayerNorm / RMSNorm weight, or a preceding
   linear layer), so what ships is the quantized matrix and a modified norm.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 1. Normalisation of s: u_j = max(sX_j, 1e-4)^alpha in fp64, then
    s_j = fp32(u_j / sqrt(max_j u * min_j u)).  A global factor on s leaves the
