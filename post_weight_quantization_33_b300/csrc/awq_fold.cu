@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kFoldThreads)
 cudaError_t launch_fold(const __half* V, int64_t rows, int64_t cols, const float* s, __half* out,
                         cudaStream_t st) {
   if (cols == 1) {
-    const int64_t blocks = std::min<int64_t>(ceil_div(rows, kFoldThreads), 148 * 8);
+    const int64_t blocks = std::min<int64_t>(ceil_div(rows, kFoldThreads), static_cast<int64_t>(device_sm_count()) * 8);
     k_fold_vec<<<static_cast<unsigned>(blocks), kFoldThreads, 0, st>>>(V, rows, s, out);
     return cudaGetLastError();
   }
@@ -72,7 +72,7 @@ cudaError_t launch_fold(const __half* V, int64_t rows, int64_t cols, const float
                    reinterpret_cast<uintptr_t>(out) % 16 == 0;
   const int64_t gx = ceil_div(ceil_div(cols, 8), kFoldThreads);
   // Enough blocks for ~8 per SM in total, rows walked grid-stride.
-  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>({rows, 65535, ceil_div(148 * 8, gx)}));
+  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>({rows, 65535, ceil_div(static_cast<int64_t>(device_sm_count()) * 8, gx)}));
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   if (vec)
     k_fold_rows<true><<<grid, kFoldThreads, 0, st>>>(V, rows, cols, s, out);

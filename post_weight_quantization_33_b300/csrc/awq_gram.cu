@@ -82,7 +82,7 @@ cudaError_t launch_gram_prepare(const __half* X, int64_t T, int64_t K, __half* X
   e = cudaMemsetAsync(mx, 0, sizeof(unsigned int), st);
   if (e != cudaSuccess) return e;
   const int64_t n = K * K;
-  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(ceil_div(n, 256), 148 * 8));
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(ceil_div(n, 256), static_cast<int64_t>(device_sm_count()) * 8));
   k_absmax<<<blocks, 256, 0, st>>>(G, n, mx);
   k_gram_half<<<blocks, 256, 0, st>>>(G, n, T, mx, Gs, row_scale);
   *launches += 4;

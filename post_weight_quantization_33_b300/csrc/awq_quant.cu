@@ -698,25 +698,32 @@ __global__ void k_unpack(const uint32_t* __restrict__ codes, int64_t N, int64_t 
   }
 }
 
+// One wave of resident blocks of a quantizer kernel: x = 512-channel chunks,
+// y = an equal share of the 16-row blocks for each (at most as many blocks
+// as are resident at once).
+cudaError_t one_wave_grid(const void* kern, int smem, int64_t N, int64_t K, dim3* grid) {
+  LaunchFacts lf;
+  const cudaError_t e = launch_facts(kern, kQuantThreads, smem, &lf);
+  if (e != cudaSuccess) return e;
+  const int64_t gx = ceil_div(K / kPerLane, 32);
+  const int64_t row_blocks = ceil_div(N, kRowsPerBlock);
+  int64_t gy = std::max<int64_t>(1, (static_cast<int64_t>(lf.per_sm) * lf.sms) / gx);
+  gy = std::min<int64_t>(gy, row_blocks);
+  gy = ceil_div(row_blocks, ceil_div(row_blocks, gy));
+  *grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  return cudaSuccess;
+}
+
 template <int BITS, int GROUP, bool SYM>
 cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, const int* sel,
                          uint32_t* codes, __half* scales, uint8_t* zeros, const float2* rowmm,
                          cudaStream_t st) {
   auto kern = k_quant_final<BITS, GROUP, SYM>;
-  LaunchFacts lf;
-  cudaError_t e = launch_facts(reinterpret_cast<const void*>(kern), kQuantThreads, kFinSmem, &lf);
+  dim3 grid;
+  const cudaError_t e = one_wave_grid(reinterpret_cast<const void*>(kern), kFinSmem, N, K, &grid);
   if (e != cudaSuccess) return e;
-  const int sms = lf.sms, per_sm = lf.per_sm;
-  // One wave of resident blocks: every block keeps a 512-channel chunk and
-  // takes an equal share of the 16-row blocks.
-  const int64_t gx = ceil_div(K / kPerLane, 32);
-  const int64_t row_blocks = ceil_div(N, kRowsPerBlock);
-  int64_t gy = std::max<int64_t>(1, (static_cast<int64_t>(per_sm) * sms) / gx);
-  gy = std::min<int64_t>(gy, row_blocks);
-  gy = ceil_div(row_blocks, ceil_div(row_blocks, gy));
   const bool c8 = (reinterpret_cast<uintptr_t>(codes) % 8) == 0;
-  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kQuantThreads, kFinSmem,
-         st>>>(W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
+  kern<<<grid, kQuantThreads, kFinSmem, st>>>(W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
   return cudaGetLastError();
 }
 
@@ -733,7 +740,8 @@ cudaError_t launch_final_g(int group, const __half* W, int64_t N, int64_t K, con
 
 cudaError_t launch_row_minmax(const __half* W, int64_t N, int64_t K, const float* s_grid,
                               const int* sel, int n_alpha, float2* rowmm, cudaStream_t st) {
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(N, 148 * 8));
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>(N, static_cast<int64_t>(device_sm_count()) * 8));
   k_row_minmax<<<grid, 256, 0, st>>>(W, N, K, s_grid, sel, n_alpha, rowmm);
   return cudaGetLastError();
 }
@@ -743,19 +751,11 @@ cudaError_t launch_residual_t(cudaStream_t st, const __half* W, int64_t N, int64
                               const float* s_grid, const float* r_grid, int n_alpha,
                               int64_t row_off, int64_t n_pad, __half* delta, const float2* rowmm) {
   auto kern = k_quant_residual<GROUP, SYM>;
-  LaunchFacts lf;
-  cudaError_t e = launch_facts(reinterpret_cast<const void*>(kern), kQuantThreads, kResSmem, &lf);
+  dim3 grid;
+  const cudaError_t e = one_wave_grid(reinterpret_cast<const void*>(kern), kResSmem, N, K, &grid);
   if (e != cudaSuccess) return e;
-  const int sms = lf.sms, per_sm = lf.per_sm;
-  // One wave of resident blocks, each with a 512-channel chunk and an equal
-  // share of the 16-row blocks.
-  const int64_t gx = ceil_div(K / kPerLane, 32);
-  const int64_t row_blocks = ceil_div(N, kRowsPerBlock);
-  int64_t gy = std::max<int64_t>(1, (static_cast<int64_t>(per_sm) * sms) / gx);
-  gy = std::min<int64_t>(gy, row_blocks);
-  gy = ceil_div(row_blocks, ceil_div(row_blocks, gy));
-  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kQuantThreads, kResSmem,
-         st>>>(W, N, K, levels, s_grid, r_grid, n_alpha, row_off, n_pad, delta, rowmm);
+  kern<<<grid, kQuantThreads, kResSmem, st>>>(W, N, K, levels, s_grid, r_grid, n_alpha, row_off,
+                                              n_pad, delta, rowmm);
   return cudaGetLastError();
 }
 
@@ -803,7 +803,7 @@ cudaError_t launch_quant_final(const __half* W, int64_t N, int64_t K, int bits, 
 cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                           cudaStream_t st) {
   const int64_t blocks = ceil_div(N * K, kQuantThreads);
-  k_unpack<<<static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(blocks, 148 * 16))),
+  k_unpack<<<static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(blocks, static_cast<int64_t>(device_sm_count()) * 16))),
              kQuantThreads, 0, st>>>(codes, N, K, bits, q);
   return cudaGetLastError();
 }
