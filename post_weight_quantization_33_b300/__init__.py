@@ -469,12 +469,18 @@ def search_host_stream(calls: Sequence[Tuple[torch.Tensor, Sequence[torch.Tensor
     results are copied out.  Device inputs are double-buffered; each result is
     freed (stream-ordered) after its copy-out.  Returns one dict per layer,
     as search_host does."""
-    device = torch.device(device)
-    if device.index is None:
-        device = torch.device("cuda", torch.cuda.current_device())
     calls = [(X, list(Ws)) for X, Ws in calls]
     if not calls:
         return []
+    for i, (X, Ws) in enumerate(calls):
+        if not isinstance(X, torch.Tensor) or X.is_cuda or X.dim() != 2:
+            raise ValueError(f"calls[{i}]: X must be a 2-D host tensor")
+        if not Ws or any(not isinstance(W, torch.Tensor) or W.is_cuda or W.dim() != 2
+                         or W.shape[1] != X.shape[1] for W in Ws):
+            raise ValueError(f"calls[{i}]: weights must be 2-D host tensors with K = {X.shape[1]}")
+    device = torch.device(device)
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
     compute = torch.cuda.current_stream(device)
     s_in = torch.cuda.Stream(device)
     s_out = torch.cuda.Stream(device)

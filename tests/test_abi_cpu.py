@@ -134,3 +134,20 @@ def test_binding_validates_tensors():
         awq.stats(X.float())
     with pytest.raises(ValueError):
         awq.stats(torch.zeros(64, dtype=torch.float16))
+
+
+def test_binding_validates_search_arguments_before_any_cuda_call():
+    X = torch.zeros((8, 128), dtype=torch.float16)
+    W = torch.zeros((16, 128), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        awq.search(X, [W])                          # host tensors
+    with pytest.raises(TypeError):
+        awq.search(X.float(), [W])
+    with pytest.raises(TypeError):
+        awq.quantize_pack(W.float(), torch.ones(128))
+    # the pipelined host search checks its layers on the host first
+    assert awq.search_host_stream([], 4, 128) == []
+    with pytest.raises(ValueError):
+        awq.search_host_stream([(X, [torch.zeros((16, 64), dtype=torch.float16)])], 4, 128)
+    with pytest.raises(ValueError):
+        awq.search_host_stream([(X, [])], 4, 128)

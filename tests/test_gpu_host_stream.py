@@ -69,10 +69,12 @@ def test_search_host_stream_failure_frees_in_flight_results():
     the layers already in flight are completed and freed, and the library
     keeps working."""
     layers = _layers()[:3]
-    X, Ws = layers[1]
-    bad_W = Ws[0][:, : X.shape[1] // 2].contiguous().pin_memory()   # K does not match X
-    seq = [layers[0], (X, [bad_W]), layers[2]]
-    with pytest.raises(ValueError):
+    # K = 96 passes the host-side checks but is not a multiple of the group
+    # size: the library refuses it after the first layer is already in flight.
+    bad = (torch.zeros((32, 96), dtype=torch.float16).pin_memory(),
+           [torch.zeros((64, 96), dtype=torch.float16).pin_memory()])
+    seq = [layers[0], bad, layers[2]]
+    with pytest.raises(awq.AwqError):
         awq.search_host_stream(seq, 4, 128)
     torch.cuda.synchronize()
     got = awq.search_host_stream(layers, 4, 128)
