@@ -32,6 +32,11 @@
  *  - Device-side waits inside the tensor-core kernels are bounded (2 s); an
  *    expired wait is reported as AWQ_ERR_TIMEOUT through a status word
  *    (never a trap), see awq_result_check and awq_reference_output.
+ *  - Calls may come from several host threads at once: the library's caches
+ *    (memory pool, pinned result mirrors, launch facts) are locked and the
+ *    error message is per thread.  Each call's work is ordered only on its
+ *    own stream; awq_stats_noalloc is the one call whose concurrent use must
+ *    be ordered by the caller (it shares one fixed array).
  *
  * Quantizer (fp32, every operation correctly rounded, none fused), per group
  * of `group_size` consecutive input channels of one output row (group_size
