@@ -151,3 +151,27 @@ def test_binding_validates_search_arguments_before_any_cuda_call():
         awq.search_host_stream([(X, [torch.zeros((16, 64), dtype=torch.float16)])], 4, 128)
     with pytest.raises(ValueError):
         awq.search_host_stream([(X, [])], 4, 128)
+
+
+def test_last_error_is_per_thread(L):
+    """Two host threads fail different calls; each reads back its own message."""
+    import threading
+    barrier = threading.Barrier(2)
+    seen = {}
+
+    def worker(name, call, expect):
+        barrier.wait()
+        for _ in range(200):
+            assert call() == awq.AWQ_ERR_INVALID
+            msg = L.awq_last_error()
+            if expect not in msg:
+                seen[name] = msg
+                return
+        seen[name] = "ok"
+
+    t1 = threading.Thread(target=worker, args=(
+        "stats", lambda: L.awq_stats(None, 0, 64, None, None), b"T=0"))
+    t2 = threading.Thread(target=worker, args=(
+        "fold", lambda: L.awq_fold_scale(None, 8, 0, None, None, None), b"cols"))
+    t1.start(); t2.start(); t1.join(); t2.join()
+    assert seen == {"stats": "ok", "fold": "ok"}, seen
