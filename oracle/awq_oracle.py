@@ -66,8 +66,15 @@ Readings where the pages are silent:
    rcp = fp32(1 / scale), the zero point is the fixed mid-code 2^(b-1), and
    q = clamp(rne(w' * rcp) + 2^(b-1), 0, 2^b - 1) -- the same stored layout
    and dequantization (q - z) * scale.
-9. group_size -1 (the AwqConfig knob in [MG] "How the scale is chosen"):
-   one group spans an output row's K channels.
+9. group_size -1 (the AwqConfig knob in [MG] "How the scale is chosen",
+   "-1 meaning per-column"): one group spans an output row's K channels.  The
+   pages write the layer as W x; the packed AWQ format stores the transpose
+   W^T [in x out], whose column is one output channel, so a per-column group
+   is one output row of W [N x K] here.
+10. Non-finite inputs: the pages assume finite activations and weights.
+   ``channel_magnitude`` keeps the IEEE fp64 sum's answer for a channel that
+   holds an infinity (+inf) or a NaN (NaN); ``search`` rejects X or W with a
+   non-finite value (ValueError): its steps have no meaning there.
 
 Parity pins for every function here live in ``tests/test_oracle_pins.py``.
 """
@@ -90,7 +97,8 @@ def channel_magnitude(X: np.ndarray) -> np.ndarray:
 
     Every fp16 value is an integer multiple of 2^-24, so every partial sum is
     too; for |sum| < 2^29 the fp64 sum is exact and independent of order.
-    The mean is then one correctly rounded division.
+    The mean is then one correctly rounded division.  A channel holding an
+    infinity gives +inf, one holding a NaN gives NaN (reading 10).
     """
     X = np.asarray(X)
     if X.ndim != 2 or X.shape[0] == 0:
@@ -284,6 +292,8 @@ def search(X: np.ndarray, Ws: Sequence[np.ndarray], bits: int = 4, group: int = 
     """
     X = np.asarray(X, np.float16)
     T, K = X.shape
+    if not np.all(np.isfinite(X)) or not all(np.all(np.isfinite(np.asarray(W))) for W in Ws):
+        raise ValueError("X and W must be finite (reading 10)")
     if sX is None:
         sX = channel_magnitude(X)
     alphas = alpha_grid(n_grid)

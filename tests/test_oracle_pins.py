@@ -100,6 +100,31 @@ def test_statistic_constant_columns_and_order_independence():
     assert O.channel_magnitude(X2)[5] == float(exact)
 
 
+def test_statistic_non_finite_channels_follow_ieee_sums():
+    """Reading 10: +inf for a channel holding an infinity of either sign, NaN
+    for one holding a NaN (also together with an infinity); the other
+    channels keep their exact means."""
+    X = np.ones((5, 8), np.float16)
+    X[2, 1] = np.float16(np.inf)
+    X[4, 2] = np.float16(-np.inf)
+    X[0, 3] = np.float16(np.nan)
+    X[1, 4] = np.float16(np.inf)
+    X[3, 4] = np.float16(np.nan)
+    sx = O.channel_magnitude(X)
+    assert sx[1] == np.inf and sx[2] == np.inf
+    assert np.isnan(sx[3]) and np.isnan(sx[4])
+    assert np.array_equal(sx[[0, 5, 6, 7]], np.ones(4))
+
+
+def test_search_rejects_non_finite_inputs():
+    W, X = workloads.random_layer(8, 128, 4, seed=12)
+    for bad in ("X", "W"):
+        Xb, Wb = X.copy(), W.copy()
+        (Xb if bad == "X" else Wb)[1, 3] = np.float16(np.nan if bad == "X" else np.inf)
+        with pytest.raises(ValueError):
+            O.search(Xb, [Wb], 4, 128, 4)
+
+
 def test_scale_closed_form_ratios():
     rng = workloads.weight_rng(2)
     sX = np.exp(rng.uniform(-2, 4, 300))
