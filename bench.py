@@ -5,18 +5,21 @@
 
 One step is one full search (channel statistic, scales, residuals for the
 20-point grid, tcgen05 error GEMM, losses, argmin, final quantize + pack) of
-the workload's calls.  The default workload is the LLaMA-7B attention
-projection: W 4096x4096 fp16, X 4096 tokens x 4096 fp16 with 1 % outlier
-channels, INT4 group 128.  Metric: weights searched per second (sum of N*K
-over the searched weights / time).  Timing: CUDA events on the launching
-stream around each step, L2 flushed (256 MiB write) between steps outside the
-events, a barrier and a device synchronisation on both sides of the timed
-region, the maximum over ranks.  Under torchrun every rank searches its own
-replica of the workload (independent layers: no collective on the data path,
-weak scaling).
+the workload's calls.  The default workload is the largest one that fits one
+GPU, the 70B-class layer shapes: W 8192x8192 and 28672x8192 fp16, one X of
+8192 tokens x 8192 fp16 with 0.5 % outlier channels, INT4 group 128, two
+search calls per step.  Metric: weights searched per second (sum of N*K over
+the searched weights / time).  Timing: CUDA events on the launching stream
+around each step; between steps, outside the events, L2 is flushed by a
+256 MiB write followed by a 256 MiB read of another buffer (so the step finds
+none of its inputs in L2 and no dirty lines of the flush to write back); a
+barrier and a device synchronisation on both sides of the timed region; the
+maximum over ranks.  Under torchrun every rank searches its own replica of the
+workload (independent layers: no collective on the data path, weak scaling).
 
 ``--impl reference`` times the CPU oracle (numpy, fp64) on the host cores on
-a bounded row sample of the same workload, rank 0 only.
+a bounded row sample of the same workload, rank 0 only; the ``cpu_baseline``
+leg of the default run times the same sample the same way.
 """
 from __future__ import annotations
 
@@ -44,7 +47,12 @@ METRIC = "AWQ search: weights searched/s (20-α grid, T calib tokens); % of roof
 UNIT = "weights/s"
 N_GRID = 20
 L2_FLUSH_BYTES = 256 << 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "error_gemm_llama7b_attn.md")
+L2_NOTE = ("flushed between timed steps, outside the step events: 256 MiB write, then a "
+           "256 MiB read of another buffer")
+DEFAULT_WORKLOAD = "llama70b"
+# A timed region at least this long runs the tensor cores under the power
+# cap: the roofline then takes the sustained peak instead of the burst one.
+SUSTAINED_AFTER_MS = 1000.0
 GEMM_SOURCES = [os.path.join(ROOT, "post_weight_quantization_33_b300", "csrc", f)
                 for f in ("awq_gemm.cu", "awq_ptx.cuh")]
 
@@ -69,13 +77,18 @@ def gemm_source_hash() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic():
-    """DRAM bytes per error-GEMM launch from the committed ncu summary, if the
-    kernel sources are unchanged since the capture; else None."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def profile_summary(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"error_gemm_{workload}.md")
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per error-GEMM launch from the committed ncu summary of this
+    workload, if the kernel sources are unchanged since the capture; else None."""
+    path = profile_summary(workload)
+    if not os.path.exists(path):
         return None
     vals = {}
-    with open(PROFILE_SUMMARY) as f:
+    with open(path) as f:
         for line in f:
             line = line.strip().lstrip("-").strip()
             if line.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
@@ -153,7 +166,7 @@ def algorithmic_bytes(wl) -> int:
     return total
 
 
-def config_for(name: str, sample: str | None = None) -> dict:
+def config_for(name: str) -> dict:
     wl = workloads.WORKLOADS[name]
     calls = []
     for c in wl.calls:
@@ -161,96 +174,52 @@ def config_for(name: str, sample: str | None = None) -> dict:
         calls.append({"X": [x.rows, x.cols],
                       "W": [[wl.spec(w).rows, wl.spec(w).cols] for w in c.ws],
                       "bits": c.bits, "group": c.group})
-    cfg = {"workload": f"{name}: {wl.description}", "calls": calls, "grid_points": N_GRID,
-           "l2": "flushed between timed steps (256 MiB write, outside the step events)"}
-    if sample:
-        cfg["sample"] = sample
-    return cfg
+    return {"workload": f"{name}: {wl.description}", "calls": calls, "grid_points": N_GRID,
+            "l2": L2_NOTE}
 
 
 # --------------------------------------------------------------------------- oracle timing
-def oracle_step(data, wl, rows_per_weight: int):
-    from oracle import awq_oracle as O
-    done = 0
+def oracle_pool(data):
+    """A spawn-started pool of oracle workers, one per host core (BLAS on one
+    thread each), with the workload's tensors in shared memory."""
+    from oracle.row_pool import OraclePool
+    return OraclePool(data)
+
+
+def oracle_step(pool, wl, rows_per_weight: int) -> int:
+    """One oracle search of every call of the workload on the first
+    ``rows_per_weight`` output rows of every weight (all tokens, all grid
+    points); the rows of all calls are cut into one batch of blocks over the
+    pool's workers.  Returns the weights searched."""
+    done, calls = 0, []
     for call in wl.calls:
-        X = data[call.x]
-        Ws = [data[w] for w in call.ws]
-        rows = [np.arange(min(rows_per_weight, W.shape[0])) for W in Ws]
-        O.search(X, Ws, call.bits, call.group, N_GRID, rows=rows)
-        done += sum(len(r) * W.shape[1] for r, W in zip(rows, Ws))
+        rows = [np.arange(min(rows_per_weight, wl.spec(w).rows)) for w in call.ws]
+        calls.append(dict(x=call.x, ws=call.ws, bits=call.bits, group=call.group, n_grid=N_GRID,
+                          rows=rows))
+        done += sum(len(r) * wl.spec(w).cols for r, w in zip(rows, call.ws))
+    pool.search_calls(calls)
     return done
 
 
-def _openblas_calls():
-    """(get, set) of the OpenBLAS bundled with numpy, through its public
-    thread-count API, for hosts without threadpoolctl; (None, None) if absent."""
-    import ctypes
-    import glob
-    libdir = os.path.join(os.path.dirname(os.path.dirname(np.__file__)), "numpy.libs")
-    for path in sorted(glob.glob(os.path.join(libdir, "*openblas*.so*"))):
-        try:
-            lib = ctypes.CDLL(path)
-        except OSError:
-            continue
-        for prefix in ("scipy_openblas", "openblas"):
-            for suffix in ("64_", "_64_", ""):
-                get = getattr(lib, f"{prefix}_get_num_threads{suffix}", None)
-                put = getattr(lib, f"{prefix}_set_num_threads{suffix}", None)
-                if get is not None and put is not None:
-                    get.restype = ctypes.c_int
-                    put.argtypes = [ctypes.c_int]
-                    return get, put
-    return None, None
+def oracle_sample(rows: int, workers: int) -> str:
+    return (f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid points, "
+            f"per step; oracle.awq_oracle.search on row blocks in {workers} spawned worker "
+            f"processes (numpy fp64, one BLAS thread each)")
 
 
-def blas_threads() -> int:
-    """Threads of numpy's BLAS pool (the oracle's one multi-threaded step)."""
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
-    except Exception:
-        pass
-    get, _ = _openblas_calls()
-    return int(get()) if get is not None else 1
-
-
-def use_all_cores() -> None:
-    """Let the oracle's one library matmul use every core this process may run
-    on (the host may start with the BLAS pool limited)."""
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
-    try:
-        from threadpoolctl import threadpool_limits
-        threadpool_limits(limits=cores, user_api="blas")
-        return
-    except Exception:
-        pass
-    _, put = _openblas_calls()
-    if put is not None:
-        put(cores)
-
-
-def cpu_baseline(data, wl, target_s: float = 15.0) -> dict:
-    """The oracle as it stands on a bounded row sample (about target_s of CPU work).
-
-    The row count grows until one timed sample takes at least a third of
-    target_s (each step's cost has a part that does not scale with rows)."""
-    use_all_cores()
-    max_rows = min(wl.spec(w).rows for c in wl.calls for w in c.ws)
-    rows = 64
-    while True:
+def cpu_baseline(data, wl, rows: int, steps: int = 2) -> dict:
+    """The oracle as it stands, timed the way --impl reference times it: the
+    same row sample, the same pool, one untimed step then ``steps`` timed."""
+    with oracle_pool(data) as pool:
+        oracle_step(pool, wl, rows)
         t0 = time.perf_counter()
-        n = oracle_step(data, wl, rows)
+        n = 0
+        for _ in range(steps):
+            n += oracle_step(pool, wl, rows)
         dt = time.perf_counter() - t0
-        if dt >= target_s / 3 or rows >= max_rows:
-            break
-        rows = int(min(max_rows, max(2 * rows, rows * target_s / max(dt, 1e-3))))
-        rows = max(64, rows // 64 * 64)
-    return {"value": n / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid "
-                      f"points ({n} weights searched in {dt:.1f} s; numpy fp64, BLAS threads as "
-                      f"in 'cores', elementwise work single-threaded)"}
+        workers = pool.workers
+    return {"value": n / dt, "unit": UNIT, "cores": workers, "kind": "oracle",
+            "sample": oracle_sample(rows, workers) + f"; {steps} timed steps, {dt:.1f} s"}
 
 
 def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
@@ -273,7 +242,7 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
         ts = []
         fn()
         for i in range(reps):
-            flush.fill_(i)
+            flush(i)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -328,6 +297,23 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     return out
 
 
+class L2Flush:
+    """Between timed launches: write a buffer larger than L2, then read
+    another one, so L2 holds neither the timed kernel's inputs nor dirty
+    lines that the kernel would have to write back."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self, i: int) -> None:
+        import torch
+        self.w.fill_(i)
+        torch.sum(self.r, out=self.sink)
+
+
 # --------------------------------------------------------------------------- ranks
 def max_over_ranks(ms: float, world: int, device) -> float:
     """The largest of the ranks' timed milliseconds: an all-reduce (MAX) over
@@ -351,27 +337,27 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_ms: f
 def run_reference(args, rank: int, world: int) -> None:
     if rank != 0:
         return
-    use_all_cores()
     wl = workloads.WORKLOADS[args.workload]
     data = workloads.generate(args.workload)
     rows = args.reference_rows
-    for _ in range(args.warmup):
-        oracle_step(data, wl, rows)
-    times, n = [], 0
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        n = oracle_step(data, wl, rows)
-        times.append(time.perf_counter() - t0)
+    with oracle_pool(data) as pool:
+        for _ in range(args.warmup):
+            oracle_step(pool, wl, rows)
+        times, n = [], 0
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            n = oracle_step(pool, wl, rows)
+            times.append(time.perf_counter() - t0)
+        workers = pool.workers
     total = sum(times)
     value = n * args.steps / total
-    sample = (f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid points "
-              f"per step ({n} weights)")
+    sample = oracle_sample(rows, workers) + f" ({n} weights per step)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_for(args.workload, sample),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
+            "config": config_for(args.workload),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -394,7 +380,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         calls.append((torch.from_numpy(data[c.x]).to(dev),
                       [torch.from_numpy(data[w]).to(dev) for w in c.ws], c.bits, c.group))
     weights_per_step = wl.weights_searched()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         res = [awq.search(X, Ws, bits, group, N_GRID) for X, Ws, bits, group in calls]
@@ -422,7 +408,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     clocks = ClockSampler(gpu_id)
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i)
+        flush(i)
         starts[i].record(stream)
         kept.append(step())
         ends[i].record(stream)
@@ -477,7 +463,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    flush.fill_(0)
+    flush(0)
     e0.record(stream)
     e2e_pass(e2e_steps)
     e1.record(stream)
@@ -495,8 +481,8 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     ideal_s = max(wl.gemm_flops(N_GRID) / (pk["tflops"] * 1e12),
                   algorithmic_bytes(wl) / (pk["hbm_gbs"] * 1e9))
     # The GEMM runs inside the step: the burst peak for a short timed region,
-    # the sustained (power-capped, seconds-long) peak for a long one.
-    long_run = total_ms > 2000.0
+    # the sustained (power-capped) peak for one that lasts a second or more.
+    long_run = total_ms >= SUSTAINED_AFTER_MS
     gemm_peak = pk["tflops_sustained"] if long_run else pk["tflops"]
     peak_kind = "sustained" if long_run else "burst"
     line = {
@@ -506,7 +492,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         "data": "synthetic", "config": config_for(args.workload),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": gemm_peak,
                      "unit": "TFLOP/s", "frac": achieved / gemm_peak,
-                     "traffic": profiled_traffic(),
+                     "traffic": profiled_traffic(args.workload),
                      "kernel": "k_gemm_err_pair (tcgen05 cta_group::2 error GEMM), fp16 operands, f32 accumulate",
                      "peak_source": f"{pk['source']} bf16 {peak_kind} (dense fp16 taken equal)",
                      "launch_ms": gemm_avg_ms},
@@ -531,7 +517,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         g1 = torch.cuda.Event(enable_timing=True)
         gms = 0.0
         for i in range(gsteps):
-            flush.fill_(i)
+            flush(i)
             g0.record(stream)
             res = [awq.search(X, Ws, bits, group, N_GRID, gram=True) for X, Ws, bits, group in calls]
             g1.record(stream)
@@ -553,21 +539,22 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
         "shape": "this workload, every grid point", "ms": res_ms, "bytes": res_bytes,
         "gbs": res_bytes / res_ms / 1e6, "frac": res_bytes / res_ms / 1e6 / pk["hbm_gbs"]}
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(data, wl)
+        line["cpu_baseline"] = cpu_baseline(data, wl, args.reference_rows)
     print(json.dumps(line), flush=True)
 
 
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["awq", "reference"], default="awq")
-    ap.add_argument("--workload", default="llama7b_attn", choices=list(workloads.WORKLOAD_ORDER))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOAD_ORDER))
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (used for profiler runs)")
-    ap.add_argument("--reference-rows", type=int, default=64,
-                    help="output rows per weight in each oracle step of --impl reference")
+    ap.add_argument("--reference-rows", type=int, default=256,
+                    help="output rows per weight in each oracle step (--impl reference and "
+                         "the cpu_baseline leg)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -69,6 +69,11 @@ extern "C" {
 #define AWQ_ABI_VERSION 1
 #define AWQ_MAX_GRID 64
 #define AWQ_MAX_WEIGHTS 16
+/* Largest T of the channel statistic (awq_stats, awq_stats_noalloc, and
+ * awq_search_layer* when they compute sX): its exact 64-bit channel sums stay
+ * below 2^62 units of 2^-24, and the top two bits mark channels that held an
+ * infinity or a NaN.  Larger T: AWQ_ERR_INVALID. */
+#define AWQ_MAX_STAT_TOKENS 4194304
 
 /* Stages of awq_search_layer, in order (for awq_result_stage_ms). */
 #define AWQ_STAGE_STATS 0       /* channel statistic (skipped when sX is given) */
@@ -127,11 +132,14 @@ int64_t awq_packed_words(int64_t N, int64_t K, int bits);
 /* Channel statistic sX_k = (1/T) sum_t |X[t][k]| ("AWQ explained",
  * "Scaling instead of mixed precision": average activation magnitude per
  * input channel).
- *   X  : device fp16 [T][K], T >= 1, K >= 8 and K % 8 == 0.
+ *   X  : device fp16 [T][K], 1 <= T <= AWQ_MAX_STAT_TOKENS, K >= 8 and
+ *        K % 8 == 0.
  *   sX : device fp64 [K], written.  The channel sums are exact (64-bit
  *        integer accumulation of |x| in units of 2^-24); the mean is one
- *        correctly rounded fp64 division.
- * Allocates K*8 bytes of stream-ordered scratch from the library's pool. */
+ *        correctly rounded fp64 division.  A channel that holds an infinity
+ *        gets +inf, one that holds a NaN gets NaN (what an IEEE fp64 sum
+ *        gives).  If a bounded device wait expired, every sX is NaN.
+ * Allocates K*8 + 8 bytes of stream-ordered scratch from the library's pool. */
 awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stream);
 
 /* Scale vectors for every grid point ("AWQ explained": s = sX^alpha).
@@ -217,6 +225,9 @@ awq_status awq_reference_output(const void* W, int64_t N, const void* X, int64_t
  *         one alpha; the loss is the sum of their losses).
  *   cfg : quantizer configuration.
  *   out : receives a library-owned result (free with awq_free).
+ * Inputs must be finite: if X or W holds an infinity or a NaN, a grid
+ * point's loss is not finite, and awq_result_check reports AWQ_ERR_INVALID
+ * (the outputs are then undefined).  With sX NULL, T <= AWQ_MAX_STAT_TOKENS.
  * Steps, all stream-ordered on the device: sX; s for every grid point; for
  * every weight and grid point the fp16 quantization residual
  * W - deq(Q(W diag(s))) diag(s)^-1 (the same quantizer as awq_quantize_pack);
@@ -246,8 +257,9 @@ awq_status awq_search_layer_gram(const void* X, int64_t T, int64_t K, const doub
                                  const awq_weight* Ws, int n_w, const awq_qconfig* cfg,
                                  void* stream, awq_result** out);
 
-/* After the search's stream is synchronised: AWQ_OK, or AWQ_ERR_TIMEOUT if a
- * bounded device wait expired during the search. */
+/* After the search's stream is synchronised: AWQ_OK; AWQ_ERR_INVALID if a
+ * grid point's loss is not finite (X or W held an infinity or a NaN); or
+ * AWQ_ERR_TIMEOUT if a bounded device wait expired during the search. */
 awq_status awq_result_check(const awq_result* r);
 
 /* Result accessors.  Host values (alpha, best index, losses) are valid once
@@ -295,12 +307,13 @@ awq_status awq_release_cached_memory(void);
  * allocations, latency-critical loops in which cudaMalloc/cudaFree would
  * synchronise the device, or code running inside another allocator's
  * callback.  The 64-bit accumulator lives in a fixed array inside the
- * library (AWQ_STATS_NOALLOC_MAX_K * 8 bytes = 512 KiB, held on every device
- * that loads the library until the process exits).
+ * library (AWQ_STATS_NOALLOC_MAX_K * 8 + 8 bytes, about 512 KiB, held on
+ * every device that loads the library until the process exits).
  *   X, T, K, sX, stream : as awq_stats; K <= AWQ_STATS_NOALLOC_MAX_K, else
  *                         AWQ_ERR_INVALID (use awq_stats for wider layers).
- * The first call on each device looks the array's device address up (with
- * that device current); make that first call before any stream capture.
+ * The first call in each CUDA context (normally the first call on each
+ * device; again after a device reset) looks the array's device address up,
+ * with that device current; make that first call before any stream capture.
  * Every call on a device shares the one array, which keeps the last call's
  * sums; each call clears the K entries it uses, on its stream, before
  * accumulating.  Calls whose work overlaps on the GPU (different streams, or

@@ -38,6 +38,7 @@ _LIB_PATH = os.path.join(_HERE, "libawq.so")
 _lib = None
 
 AWQ_OK, AWQ_ERR_INVALID, AWQ_ERR_UNSUPPORTED, AWQ_ERR_CUDA, AWQ_ERR_OOM, AWQ_ERR_TIMEOUT = range(6)
+MAX_STAT_TOKENS = 1 << 22     # AWQ_MAX_STAT_TOKENS
 
 # Every symbol include/awq.h declares.
 EXPORTED_SYMBOLS = (

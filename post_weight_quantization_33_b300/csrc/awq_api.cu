@@ -239,10 +239,13 @@ int64_t awq_packed_words(int64_t N, int64_t K, int bits) {
 
 awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stream) {
   if (T < 1) return fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
+  if (T > kMaxStatTokens)
+    return fail(AWQ_ERR_INVALID,
+                "T=%lld exceeds AWQ_MAX_STAT_TOKENS=%lld (the exact 64-bit channel sums)",
+                static_cast<long long>(T), static_cast<long long>(kMaxStatTokens));
   if (K < 8 || K % 8) return fail(AWQ_ERR_INVALID, "K=%lld (must be a positive multiple of 8)",
                                   static_cast<long long>(K));
-  if (T > (int64_t(1) << 31) || K > (int64_t(1) << 31))
-    return fail(AWQ_ERR_INVALID, "T or K too large");
+  if (K > (int64_t(1) << 31)) return fail(AWQ_ERR_INVALID, "K too large");
   awq_status st;
   if ((st = check_dev(X, "X", 16)) != AWQ_OK) return st;
   if ((st = check_dev(sX, "sX", 8)) != AWQ_OK) return st;
@@ -251,10 +254,14 @@ awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stre
   auto cleanup = [&] {
     if (ws) cudaFreeAsync(ws, s);
   };
-  AWQ_CUDA(pool_alloc(&ws, sizeof(unsigned long long) * K, s), "scratch allocation");
+  // K 64-bit sums, then the status word of the bounded waits.
+  AWQ_CUDA(pool_alloc(&ws, sizeof(unsigned long long) * (K + 1), s), "scratch allocation");
   auto* acc = static_cast<unsigned long long*>(ws);
-  AWQ_CUDA(launch_stats_accumulate(static_cast<const __half*>(X), T, K, acc, s), "stats kernel");
-  AWQ_CUDA(launch_stats_finalize(acc, T, K, sX, s), "stats finalize kernel");
+  int* status = reinterpret_cast<int*>(acc + K);
+  AWQ_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s), "status reset");
+  AWQ_CUDA(launch_stats_accumulate(static_cast<const __half*>(X), T, K, acc, status, s),
+           "stats kernel");
+  AWQ_CUDA(launch_stats_finalize(acc, T, K, sX, status, s), "stats finalize kernel");
   AWQ_CUDA(cudaFreeAsync(ws, s), "scratch release");
   return ok();
 }
@@ -402,6 +409,10 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
   awq_status st;
   if ((st = check_cfg(cfg)) != AWQ_OK) return st;
   if (T < 1) return fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
+  if (sX == nullptr && T > kMaxStatTokens)
+    return fail(AWQ_ERR_INVALID,
+                "T=%lld exceeds AWQ_MAX_STAT_TOKENS=%lld for the channel statistic (pass sX)",
+                static_cast<long long>(T), static_cast<long long>(kMaxStatTokens));
   if (!k_fits(K, cfg))
     return fail(AWQ_ERR_INVALID,
                 "K=%lld (must be a positive multiple of group_size=%d; of 64 for -1)",
@@ -560,8 +571,9 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
   const double* sxp = sX;
   AWQ_CUDA(cudaMemsetAsync(range, 0, 3 * sizeof(unsigned long long), s), "range reset");
   if (sxp == nullptr) {
-    AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, s), "stats kernel");
-    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, s, range), "stats finalize kernel");
+    AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, r->status, s), "stats kernel");
+    AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, r->status, s, range),
+             "stats finalize kernel");
     r->launches += 2;
     sxp = sx_ws;
   }
@@ -599,7 +611,7 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
   // 5. losses and argmin
   AWQ_CUDA(launch_loss_reduce(partials, G, static_cast<int>(n_tiles), n_pad, T, map, n_total,
                               chunk_sums, r->row_losses, r->losses, r->best, r->alpha,
-                              r->s_grid, K, r->s, counter, gram ? rsc : nullptr, s),
+                              r->s_grid, K, r->s, counter, gram ? rsc : nullptr, r->status, s),
            "loss reduction");
   r->launches += 1;
   AWQ_CUDA(mark(AWQ_STAGE_FINAL), "event record");
@@ -644,6 +656,10 @@ awq_status awq_search_layer_gram(const void* X, int64_t T, int64_t K, const doub
 
 awq_status awq_result_check(const awq_result* r) {
   if (r == nullptr) return fail(AWQ_ERR_INVALID, "result is NULL");
+  if (r->host->status == kDevNonFinite)
+    return fail(AWQ_ERR_INVALID,
+                "X or W holds a non-finite value (a grid point's loss is not finite); "
+                "the result is undefined");
   if (r->host->status != 0)
     return fail(AWQ_ERR_TIMEOUT, "a bounded device wait expired (device code %d)",
                 r->host->status);

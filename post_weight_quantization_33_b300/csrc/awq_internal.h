@@ -19,6 +19,7 @@ enum DeviceError : int {
   kDevTimeoutTmemEmpty = 5, // accumulator never drained
   kDevTimeoutDrain = 6,     // in-flight copies/MMAs did not finish on abort
   kDevTimeoutSelfTest = 7,  // the self-test wait expired (expected there)
+  kDevNonFinite = 8,        // a grid point's loss is not finite: X or W holds inf/NaN
 };
 
 constexpr int kMaxWeights = 16;
@@ -42,12 +43,19 @@ struct RowMap {
 };
 
 // ---- statistics and scales (awq_stats.cu)
+// Largest token count of the exact statistic: the 64-bit sums stay below
+// 2^62, and the top two bits flag channels that held an infinity or a NaN.
+constexpr int64_t kMaxStatTokens = int64_t(1) << 22;
+// acc: K 64-bit words of scratch (zeroed here, on the stream); status: a
+// device int (zeroed by the caller) that receives a code if a bounded wait
+// expired, nullable.
 cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
-                                    unsigned long long* acc, cudaStream_t st);
+                                    unsigned long long* acc, int* status, cudaStream_t st);
 // range (nullable, 2 words zeroed by the caller): also the range of
-// max(sX, 1e-4) over the channels, for launch_scales.
+// max(sX, 1e-4) over the channels, for launch_scales.  A non-zero *status
+// (nullable) makes every sX NaN.
 cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int64_t K,
-                                  double* sX, cudaStream_t st,
+                                  double* sX, const int* status, cudaStream_t st,
                                   unsigned long long* range = nullptr);
 // The same range for a caller-given sX (zeroes `range` first).
 cudaError_t launch_sx_range(const double* sX, int64_t K, unsigned long long* range,
@@ -121,12 +129,14 @@ cudaError_t launch_w4_matvec(const uint32_t* codes, const __half* scales, const 
 int64_t loss_chunks(int64_t n_pad);
 // Also copies s_grid[best] (K floats) to s_out.  counter: one u32 of scratch,
 // zeroed by the caller before the launch.  row_scale (nullable, device):
-// factor on every row sum (the Gram form's T / c).
+// factor on every row sum (the Gram form's T / c).  status: the call's device
+// status word; a non-finite loss sets kDevNonFinite (unless a code is there).
 cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, int64_t n_pad,
                                int64_t T, const RowMap& map, int64_t n_total,
                                double* chunk_sums, double* row_losses, double* losses, int* best,
                                double* alpha_out, const float* s_grid, int64_t K, float* s_out,
-                               unsigned int* counter, const double* row_scale, cudaStream_t st);
+                               unsigned int* counter, const double* row_scale, int* status,
+                               cudaStream_t st);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -142,5 +152,14 @@ cudaError_t launch_facts(const void* fn, int threads, int smem, LaunchFacts* out
 // Co-resident clusters of a kernel compiled with cluster dimensions (cached).
 cudaError_t cluster_facts(const void* fn, int threads, int smem, int* max_clusters);
 int device_sm_count();
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime
+// (nullptr if the driver lacks it).  Linked statically, the library does not
+// need the driver at load time.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 }  // namespace awq

@@ -70,6 +70,20 @@ cudaError_t launch_facts(const void* fn, int threads, int smem, LaunchFacts* out
   return cudaSuccess;
 }
 
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
 cudaError_t cluster_facts(const void* fn, int threads, int smem, int* max_clusters) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

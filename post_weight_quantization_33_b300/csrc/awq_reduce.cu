@@ -23,13 +23,15 @@ constexpr int kLossRows = 256;   // rows per block (a chunk)
 // every grid point in chunk order, divides by N_w * T, sums the weights, takes
 // the argmin -- first minimum, NaN as +inf -- and copies the chosen scale
 // vector to s_out.  Every sum has a fixed order: the result is deterministic.
+// A grid point whose loss is not finite sets *status to kDevNonFinite.
 __global__ void __launch_bounds__(kLossRows)
     k_losses(const float* __restrict__ partials, int n_tiles, int64_t n_pad, RowMap map,
              int64_t n_total, int64_t T, double* __restrict__ chunk_sums,
              double* __restrict__ row_losses, double* __restrict__ losses,
              int* __restrict__ best, double* __restrict__ alpha_out,
              const float* __restrict__ s_grid, int64_t K, float* __restrict__ s_out,
-             unsigned int* __restrict__ counter, const double* __restrict__ row_scale) {
+             unsigned int* __restrict__ counter, const double* __restrict__ row_scale,
+             int* __restrict__ status) {
   __shared__ double red[kLossRows];
   __shared__ int last, chosen;
   const int c = blockIdx.x;
@@ -100,6 +102,9 @@ __global__ void __launch_bounds__(kLossRows)
     }
     losses[ga] = total;
     red[ga] = total;
+    // Finite inputs give finite losses; an infinity or NaN in X or W reaches
+    // every grid point's loss (through s, the residual or the product).
+    if (!isfinite(total)) atomicCAS(status, 0, kDevNonFinite);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -129,11 +134,12 @@ cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, 
                                int64_t T, const RowMap& map, int64_t n_total,
                                double* chunk_sums, double* row_losses, double* losses, int* best,
                                double* alpha_out, const float* s_grid, int64_t K, float* s_out,
-                               unsigned int* counter, const double* row_scale, cudaStream_t st) {
+                               unsigned int* counter, const double* row_scale, int* status,
+                               cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(loss_chunks(n_pad)), static_cast<unsigned>(n_alpha));
   k_losses<<<grid, kLossRows, 0, st>>>(partials, n_tiles, n_pad, map, n_total, T, chunk_sums,
                                        row_losses, losses, best, alpha_out, s_grid, K, s_out,
-                                       counter, row_scale);
+                                       counter, row_scale, status);
   return cudaGetLastError();
 }
 

@@ -115,6 +115,28 @@ def test_invalid_arguments_rejected_before_launch(L):
     L.awq_free(None)   # ignored
 
 
+def test_statistic_token_bound(L):
+    """The exact 64-bit channel sums hold at most AWQ_MAX_STAT_TOKENS tokens
+    (|x| * 2^24 < 2^40 per token, the top two bits of each sum are flags):
+    every entry point that computes the statistic refuses more, before
+    touching its pointers; a search given sX has no such bound."""
+    INVALID = awq.AWQ_ERR_INVALID
+    T = awq.MAX_STAT_TOKENS + 1
+    assert awq.MAX_STAT_TOKENS == 1 << 22
+    for entry in ("awq_stats", "awq_stats_noalloc"):
+        assert getattr(L, entry)(None, T, 64, None, None) == INVALID
+        assert b"AWQ_MAX_STAT_TOKENS" in L.awq_last_error()
+        assert getattr(L, entry)(None, T - 1, 64, None, None) == INVALID
+        assert b"AWQ_MAX_STAT_TOKENS" not in L.awq_last_error()
+    out = ctypes.c_void_p()
+    w = (awq.Weight * 1)()
+    assert L.awq_search_layer(None, T, 256, None, w, 1, _cfg(), None, ctypes.byref(out)) == INVALID
+    assert b"AWQ_MAX_STAT_TOKENS" in L.awq_last_error()
+    sx = ctypes.c_void_p(0x1000)
+    assert L.awq_search_layer(None, T, 256, sx, w, 1, _cfg(), None, ctypes.byref(out)) == INVALID
+    assert b"AWQ_MAX_STAT_TOKENS" not in L.awq_last_error()
+
+
 def test_host_pointer_rejected(L):
     # A host buffer must be refused by the pointer check, never launched on.
     buf = (ctypes.c_char * 4096)()

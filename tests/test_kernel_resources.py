@@ -21,7 +21,7 @@ BUDGET = [
     ("awq_quant.cu", r"k_quant_residual", 128, 0),
     ("awq_quant.cu", r"k_quant_finalILi4E", 85, 0),
     ("awq_quant.cu", r"k_quant_finalILi3E", 85, 16),
-    ("awq_stats.cu", r"k_stats_accumulate", 80, 0),
+    ("awq_stats.cu", r"k_stats_accumulate", 112, 0),   # 2 blocks of 288 threads per SM
     ("awq_matvec.cu", r"k_w4_matvec", 128, 0),
     ("awq_reduce.cu", r"k_losses", 64, 0),
 ]

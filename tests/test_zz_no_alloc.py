@@ -1,7 +1,8 @@
 """awq_stats_noalloc: the channel statistic for callers that cannot let the
 library allocate device memory (see include/awq.h).  Called through the C ABI
 and compared with awq_stats, which takes its scratch from the library's pool.
-The statistic is exact on both paths, so the comparison is bit for bit.
+The statistic is exact on both paths, so the comparison is bit for bit,
+and it is also checked directly against the CPU oracle.
 
 This file is collected last so that a stop-at-first-failure run has already
 run every other test when it gets here; it also passes on its own."""
@@ -11,6 +12,7 @@ import torch
 
 import post_weight_quantization_33_b300 as awq
 import workloads
+from oracle import awq_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +44,9 @@ def test_noalloc_matches_pool_version_on_two_calls_in_a_row():
     got2 = _stats_through_abi("awq_stats_noalloc", X2)
     assert np.array_equal(got1, _stats_through_abi("awq_stats", X1))
     assert np.array_equal(got2, _stats_through_abi("awq_stats", X2))
+    # and directly against the CPU oracle's exact mean
+    assert np.array_equal(got1, O.channel_magnitude(X1.cpu().numpy()))
+    assert np.array_equal(got2, O.channel_magnitude(X2.cpu().numpy()))
 
 
 def test_noalloc_rejects_more_channels_than_its_scratch():
