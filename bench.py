@@ -180,10 +180,15 @@ def config_for(name: str) -> dict:
 
 # --------------------------------------------------------------------------- oracle timing
 def oracle_pool(data):
-    """A spawn-started pool of oracle workers, one per host core (BLAS on one
-    thread each), with the workload's tensors in shared memory."""
-    from oracle.row_pool import OraclePool
-    return OraclePool(data)
+    """A spawn-started pool of oracle workers with the workload's tensors in
+    shared memory, filling every host core: a quarter as many workers as
+    cores, each with a BLAS pool of 4 threads.  (Every worker repeats a call's
+    work on the whole X -- the inverse-scaled activations of each grid point
+    -- so fewer, wider workers move less memory per sampled row.)"""
+    from oracle.row_pool import OraclePool, default_workers
+    cores = default_workers()
+    workers = max(1, cores // 4)
+    return OraclePool(data, workers, blas_threads=cores // workers)
 
 
 def oracle_step(pool, wl, rows_per_weight: int) -> int:
@@ -201,10 +206,10 @@ def oracle_step(pool, wl, rows_per_weight: int) -> int:
     return done
 
 
-def oracle_sample(rows: int, workers: int) -> str:
+def oracle_sample(rows: int, pool) -> str:
     return (f"first {rows} output rows of every weight, all tokens, all {N_GRID} grid points, "
-            f"per step; oracle.awq_oracle.search on row blocks in {workers} spawned worker "
-            f"processes (numpy fp64, one BLAS thread each)")
+            f"per step; oracle.awq_oracle.search on row blocks in {pool.workers} spawned worker "
+            f"processes (numpy fp64, {pool.blas_threads} BLAS threads each)")
 
 
 def cpu_baseline(data, wl, rows: int, steps: int = 2) -> dict:
@@ -217,9 +222,8 @@ def cpu_baseline(data, wl, rows: int, steps: int = 2) -> dict:
         for _ in range(steps):
             n += oracle_step(pool, wl, rows)
         dt = time.perf_counter() - t0
-        workers = pool.workers
-    return {"value": n / dt, "unit": UNIT, "cores": workers, "kind": "oracle",
-            "sample": oracle_sample(rows, workers) + f"; {steps} timed steps, {dt:.1f} s"}
+    return {"value": n / dt, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+            "sample": oracle_sample(rows, pool) + f"; {steps} timed steps, {dt:.1f} s"}
 
 
 def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
@@ -281,18 +285,30 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     ms = timed(lambda: torch.amax(W))
     out["read_only_context"]["W"] = {"bytes": 2 * N * K, "ms": ms, "gbs": 2 * N * K / ms / 1e6,
                                      "kernel": "torch.amax"}
-    # The packed layer consumed at decode: W4A16 product for one token, and a
-    # cuBLAS fp16 GEMV on the dense weight of the same shape for context.
-    x = torch.randn(1, K, generator=g, device=dev).half()
-    y = torch.empty(1, N, dtype=torch.float32, device=dev)
-    ms = timed(lambda: awq._check(L.awq_w4a16_matvec(
-        codes.data_ptr(), sc.data_ptr(), z.data_ptr(), N, K, ctypes.byref(cfg), x.data_ptr(), 1,
-        y.data_ptr(), st)))
-    nbytes = N * K // 2 + 3 * N * K // 128 + 2 * K + 4 * N
-    dense_ms = timed(lambda: torch.matmul(x, W.t()))
-    out["w4a16_matvec"] = {"shape": f"W {N}x{K} INT4 g128, 1 token", "ms": ms, "bytes": nbytes,
-                           "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs,
-                           "fp16_cublas_gemv_ms": dense_ms, "speedup_vs_fp16": dense_ms / ms}
+    # The packed layer consumed at decode: the W4A16 product for 1 and 16
+    # tokens and the W3A16 product for one token, each beside a cuBLAS fp16
+    # product with the dense weight of the same shape.
+    codes3 = torch.empty(N * 3 * K // 32, dtype=torch.int32, device=dev)
+    sc3 = torch.empty(N * K // 128, dtype=torch.float16, device=dev)
+    z3 = torch.empty(N * K // 128, dtype=torch.uint8, device=dev)
+    cfg3 = awq.QConfig(3, 128, 1, N_GRID)
+    awq._check(L.awq_quantize_pack(W.data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg3),
+                                   codes3.data_ptr(), sc3.data_ptr(), z3.data_ptr(), st))
+    decode = {}
+    for bits, M in ((4, 1), (4, 16), (3, 1)):
+        c_, s_, z_, cf = (codes, sc, z, cfg) if bits == 4 else (codes3, sc3, z3, cfg3)
+        x = torch.randn(M, K, generator=g, device=dev).half()
+        y = torch.empty(M, N, dtype=torch.float32, device=dev)
+        ms = timed(lambda: awq._check(L.awq_w4a16_matvec(
+            c_.data_ptr(), s_.data_ptr(), z_.data_ptr(), N, K, ctypes.byref(cf), x.data_ptr(), M,
+            y.data_ptr(), st)))
+        nbytes = N * K * bits // 8 + 3 * N * K // 128 + 2 * M * K + 4 * M * N
+        dense_ms = timed(lambda: torch.matmul(x, W.t()))
+        decode[f"int{bits}_m{M}"] = {
+            "shape": f"W {N}x{K} INT{bits} g128, {M} token(s)", "ms": ms, "bytes": nbytes,
+            "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs,
+            "fp16_cublas_ms": dense_ms, "speedup_vs_fp16": dense_ms / ms}
+    out["decode_product"] = decode
     del W
     return out
 
@@ -305,13 +321,13 @@ class L2Flush:
     def __init__(self, dev):
         import torch
         self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def __call__(self, i: int) -> None:
         import torch
         self.w.fill_(i)
-        torch.sum(self.r, out=self.sink)
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 # --------------------------------------------------------------------------- ranks
@@ -348,16 +364,15 @@ def run_reference(args, rank: int, world: int) -> None:
             t0 = time.perf_counter()
             n = oracle_step(pool, wl, rows)
             times.append(time.perf_counter() - t0)
-        workers = pool.workers
     total = sum(times)
     value = n * args.steps / total
-    sample = oracle_sample(rows, workers) + f" ({n} weights per step)"
+    sample = oracle_sample(rows, pool) + f" ({n} weights per step)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_for(args.workload),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -443,8 +458,9 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
             n, k = W.shape
             d2h += awq.packed_words(n, k, bits) * 4 + 3 * n * (k // group)
         d2h += X.shape[1] * 4 + N_GRID * 8
-    # Steps run through search_host_stream: step i+1's inputs are copied in
-    # and step i-1's results copied out while step i is searched.  Every step
+    # Steps run through awq_search_host_layers (the C ABI's host-buffer
+    # pipeline, via search_host_stream): step i+1's inputs are copied in and
+    # step i-1's results copied out while step i is searched.  Every step
     # still copies its own inputs in and its results out inside the timed
     # region; the region spans all steps, pipeline fill and drain included.
     e2e_steps = max(3, min(args.steps, 20))
@@ -498,7 +514,7 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
                      "launch_ms": gemm_avg_ms},
         "step_roofline": {"ideal_ms": ideal_s * 1e3, "frac": ideal_s * 1e3 / (total_ms / args.steps)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h), "api": "awq_search_host_layers"},
         "gpu_launches": launches,
         "stages_ms_per_step": {k: v / args.steps for k, v in stage_sum.items()},
         "clocks": clk,

@@ -185,25 +185,27 @@ awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bit
 awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float* s, void* out,
                           void* stream);
 
-/* W4A16 decode product with a packed layer ("AWQ explained",
+/* Decode product with a packed layer, W4A16 or W3A16 ("AWQ explained",
  * "Why weight-only quantization fits decoding": at small batch each token
- * reads every weight once, so 4-bit weights with 16-bit activations cut the
- * dominant traffic about four times).
- *   codes  : device uint32 [N][K/8], 16-byte aligned, INT4 codes as written
- *            by the search or awq_quantize_pack (cfg->bits must be 4, else
- *            AWQ_ERR_UNSUPPORTED).
+ * reads every weight once, so 3- or 4-bit weights with 16-bit activations cut
+ * the dominant traffic four times or more).
+ *   codes  : device uint32 packed codes as written by the search or
+ *            awq_quantize_pack (INT4 [N][K/8] or INT3 [N][3K/32]), 16-byte
+ *            aligned.
  *   scales : device fp16 [N][K/group] ([N][1] for group_size -1).
  *   zeros  : device uint8, same shape.
- *   cfg    : the configuration the codes were made with (bits, group_size;
- *            zero_point and n_grid are not used).
- *   x      : device fp16 [M][K], 1 <= M <= 8, 16-byte aligned: activations
+ *   cfg    : the configuration the codes were made with (bits 3 or 4,
+ *            group_size; zero_point and n_grid are not used).
+ *   x      : device fp16 [M][K], 1 <= M <= 16, 16-byte aligned: activations
  *            with diag(s)^-1 already folded into their producer
  *            (awq_fold_scale).
  *   y      : device fp32 [M][N], written:
- *            y[m][n] = sum_g scale[n][g] * sum_{k in g} (code - zero) * x[m][k],
- *            all sums in fp32.
- * K % 8 == 0 and K % group == 0 (K % 64 for group_size -1).  Allocates
- * nothing. */
+ *            y[m][n] = sum_g scale[n][g] * sum_{k in g} (code - zero) * x[m][k];
+ *            (code - zero) * x is exact, the sums are fp32 on the tensor cores
+ *            (mma.sync, fp16 operands), and each group's sum is scaled in fp32.
+ *            Deterministic: run-to-run identical.
+ * K % 64 == 0 and K % group == 0.  Allocates nothing (y is zeroed on the
+ * stream, then accumulated). */
 awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uint8_t* zeros,
                             int64_t N, int64_t K, const awq_qconfig* cfg, const void* x, int M,
                             float* y, void* stream);
@@ -256,6 +258,40 @@ awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* s
 awq_status awq_search_layer_gram(const void* X, int64_t T, int64_t K, const double* sX,
                                  const awq_weight* Ws, int n_w, const awq_qconfig* cfg,
                                  void* stream, awq_result** out);
+
+/* One layer of awq_search_host_layers: inputs and outputs in host memory
+ * (pinned memory lets the copies overlap the searches; pageable memory works
+ * but serialises them).  Output buffers are owned by the caller. */
+typedef struct awq_host_layer {
+  const void* X;             /* host fp16 [T][K] calibration activations */
+  int64_t T;                 /* 1 <= T <= AWQ_MAX_STAT_TOKENS */
+  int64_t K;                 /* as awq_search_layer: K % group == 0, K % 32 for INT3 */
+  const awq_weight* Ws;      /* host array of n_w weights; each W is host fp16 [N][K] */
+  int n_w;                   /* 1..AWQ_MAX_WEIGHTS, sharing X (one s, one alpha) */
+  uint32_t* const* codes;    /* n_w host buffers, uint32 [awq_packed_words(N_i, K, bits)] */
+  void* const* scales;       /* n_w host buffers, fp16 [N_i][K/group] ([N_i][1] for -1) */
+  uint8_t* const* zeros;     /* n_w host buffers, uint8, same shape as scales */
+  float* s;                  /* host fp32 [K]: s at alpha* */
+  double* losses;            /* host fp64 [n_grid]: the loss of every grid point */
+  int* best;                 /* host int: index of alpha* (alpha* = best / n_grid) */
+} awq_host_layer;
+
+/* The search of awq_search_layer for a sequence of layers whose inputs and
+ * outputs are in host memory (the end-to-end use: calibration data and
+ * weights on the host, quantized layers back to the host).  Each layer's
+ * search runs on `stream`; two library-owned streams copy layer i+1's inputs
+ * in and layer i-1's outputs out while layer i is searched.  Device inputs
+ * are double-buffered in two slots sized for the largest layer (from the
+ * library's pool); each layer's device result is freed after its copy-out.
+ * Every layer is checked on the host before anything is copied.  Returns
+ * when every output is in the caller's buffers (synchronous).  On failure
+ * (a layer the search refuses, a CUDA error, AWQ_ERR_OOM, or a non-finite
+ * loss / expired wait reported by awq_result_check) the work already enqueued
+ * is completed, every device buffer of the call is released, and the status
+ * of the first failure is returned; the outputs are then incomplete.
+ * n_layers 0 is a no-op. */
+awq_status awq_search_host_layers(const awq_host_layer* layers, int n_layers,
+                                  const awq_qconfig* cfg, void* stream);
 
 /* After the search's stream is synchronised: AWQ_OK; AWQ_ERR_INVALID if a
  * grid point's loss is not finite (X or W held an infinity or a NaN); or
@@ -321,6 +357,18 @@ awq_status awq_release_cached_memory(void);
  * results: order them. */
 #define AWQ_STATS_NOALLOC_MAX_K 65536
 awq_status awq_stats_noalloc(const void* X, int64_t T, int64_t K, double* sX, void* stream);
+
+/* Test hook of the out-of-memory path: after the next `skip` device
+ * allocations from the library's pool, the following `count` fail as if the
+ * device memory were exhausted, without reaching the allocator (the calls
+ * that make them return AWQ_ERR_OOM and release what they held).  count 0
+ * disarms it.  Process-wide; for tests of callers' error handling. */
+void awq_inject_allocation_failures(int skip, int count);
+
+/* Bytes of the library pool on the current device: handed out to results or
+ * in-flight scratch (used), and held from the driver (reserved, >= used;
+ * freed blocks stay cached until awq_release_cached_memory). */
+awq_status awq_pool_usage(int64_t* used_bytes, int64_t* reserved_bytes);
 
 /* Self-test of the bounded device wait: launches one CTA that waits on a
  * barrier nothing arrives at, with a limit of limit_ns nanoseconds

@@ -14,9 +14,10 @@ call's loss at a grid point is then sum_i (sum over rows of W_i) / (N_i T) in
 fp64, and alpha* is the first index of its minimum (``first_argmin``).
 
 Workers are started with the ``spawn`` method, so a process that has already
-initialised CUDA can use this safely.  Each worker runs its BLAS on one thread,
-so ``workers`` is the number of cores the oracle uses.  The inputs are placed
-once in shared memory, and workers map them read-only.
+initialised CUDA can use this safely.  Each worker runs its BLAS on
+``blas_threads`` threads (default 1), so ``workers * blas_threads`` is the
+number of cores the oracle uses.  The inputs are placed once in shared
+memory, and workers map them read-only.
 """
 from __future__ import annotations
 
@@ -63,8 +64,11 @@ class OraclePool:
     Use as a context manager; ``close()`` ends the workers and frees the
     shared memory."""
 
-    def __init__(self, arrays: Dict[str, np.ndarray], workers: Optional[int] = None):
+    def __init__(self, arrays: Dict[str, np.ndarray], workers: Optional[int] = None,
+                 blas_threads: int = 1):
         self.workers = int(workers or default_workers())
+        self.blas_threads = max(1, int(blas_threads))
+        self.cores = self.workers * self.blas_threads
         self._own: List[shared_memory.SharedMemory] = []
         layout = {}
         self.arrays: Dict[str, np.ndarray] = {}
@@ -76,11 +80,11 @@ class OraclePool:
             self._own.append(shm)
             self.arrays[name] = view
             layout[name] = (shm.name, a.shape, a.dtype.str)
-        # One BLAS thread per worker: the children read these at numpy import.
+        # The workers' BLAS threads: the children read these at numpy import.
         saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS",
                                                 "MKL_NUM_THREADS")}
         for k in saved:
-            os.environ[k] = "1"
+            os.environ[k] = str(self.blas_threads)
         try:
             ctx = mp.get_context("spawn")
             self._pool = ctx.Pool(self.workers, initializer=_attach, initargs=(layout,))

@@ -30,7 +30,8 @@ __all__ = [
     "AwqError", "lib", "library_path", "groups_per_row", "stats", "stats_noalloc", "scales", "quantize_pack", "unpack_codes",
     "reference_output", "fold_scale", "w4a16_matvec", "search", "search_host", "SearchResult", "packed_words",
     "release_cached_memory", "selftest_bounded_wait", "set_stage_timing", "STAGES",
-    "EXPORTED_SYMBOLS",
+    "EXPORTED_SYMBOLS", "search_host_stream", "HostLayer", "inject_allocation_failures",
+    "pool_usage", "MAX_STAT_TOKENS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,7 +51,8 @@ EXPORTED_SYMBOLS = (
     "awq_result_scales", "awq_result_zeros", "awq_free", "awq_release_cached_memory",
     "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
     "awq_result_stage_ms", "awq_stats_noalloc", "awq_fold_scale", "awq_w4a16_matvec",
-    "awq_search_layer_gram",
+    "awq_search_layer_gram", "awq_search_host_layers", "awq_inject_allocation_failures",
+    "awq_pool_usage",
 )
 
 # Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
@@ -70,6 +72,16 @@ class QConfig(ctypes.Structure):
 
 class Weight(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("N", ctypes.c_int64)]
+
+
+class HostLayer(ctypes.Structure):
+    """awq_host_layer: one layer of awq_search_host_layers (host memory)."""
+    _fields_ = [("X", ctypes.c_void_p), ("T", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("Ws", ctypes.POINTER(Weight)), ("n_w", ctypes.c_int),
+                ("codes", ctypes.POINTER(ctypes.c_void_p)),
+                ("scales", ctypes.POINTER(ctypes.c_void_p)),
+                ("zeros", ctypes.POINTER(ctypes.c_void_p)),
+                ("s", ctypes.c_void_p), ("losses", ctypes.c_void_p), ("best", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -123,6 +135,10 @@ def lib() -> ctypes.CDLL:
         "awq_result_kernel_launches": (i32, [vp]),
         "awq_set_stage_timing": (None, [i32]),
         "awq_result_stage_ms": (st, [vp, i32, ctypes.POINTER(ctypes.c_float)]),
+        "awq_search_host_layers": (st, [ctypes.POINTER(HostLayer), i32, ctypes.POINTER(QConfig),
+                                        vp]),
+        "awq_inject_allocation_failures": (None, [i32, i32]),
+        "awq_pool_usage": (st, [ctypes.POINTER(i64), ctypes.POINTER(i64)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -259,15 +275,16 @@ def fold_scale(V: torch.Tensor, s: torch.Tensor, out: Optional[torch.Tensor] = N
 
 
 def w4a16_matvec(codes: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, N: int, K: int,
-                 x: torch.Tensor, group: int = 128) -> torch.Tensor:
-    """y [M, N] fp32 = deq(INT4 codes) x^T for x fp16 [M, K], 1 <= M <= 8."""
+                 x: torch.Tensor, group: int = 128, bits: int = 4) -> torch.Tensor:
+    """y [M, N] fp32 = deq(codes) x^T for x fp16 [M, K], 1 <= M <= 16, INT4 or
+    INT3 packed codes (awq_w4a16_matvec)."""
     _require(codes, "codes", torch.int32, 1)
     _require(x, "x", torch.float16, 2)
     if x.shape[1] != K:
         raise ValueError(f"x has K={x.shape[1]}, expected {K}")
     M = x.shape[0]
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    cfg = _cfg(4, group)
+    cfg = _cfg(bits, group)
     _check(lib().awq_w4a16_matvec(codes.data_ptr(), scales.data_ptr(), zeros.data_ptr(), N, K,
                                   ctypes.byref(cfg), x.data_ptr(), M, y.data_ptr(), _stream()))
     return y
@@ -464,12 +481,11 @@ def search_host(X: torch.Tensor, Ws: Sequence[torch.Tensor], bits: int = 4, grou
 def search_host_stream(calls: Sequence[Tuple[torch.Tensor, Sequence[torch.Tensor]]],
                        bits: int = 4, group: int = 128, n_grid: int = 20, device="cuda",
                        zero_point: bool = True) -> List[dict]:
-    """search_host over a sequence of layers ``(X, [W, ...])`` in host memory
-    (pinned for asynchronous copies), pipelined over three streams: while
-    layer i is searched, layer i+1's inputs are copied in and layer i-1's
-    results are copied out.  Device inputs are double-buffered; each result is
-    freed (stream-ordered) after its copy-out.  Returns one dict per layer,
-    as search_host does."""
+    """awq_search_host_layers over a sequence of layers ``(X, [W, ...])`` in
+    host memory (pinned for overlapped copies): the library searches layer i
+    on the current stream of ``device`` while its own streams copy layer i+1's
+    inputs in and layer i-1's results out.  Returns one dict per layer, as
+    search_host does, with the outputs in pinned host tensors."""
     calls = [(X, list(Ws)) for X, Ws in calls]
     if not calls:
         return []
@@ -479,89 +495,62 @@ def search_host_stream(calls: Sequence[Tuple[torch.Tensor, Sequence[torch.Tensor
         if not Ws or any(not isinstance(W, torch.Tensor) or W.is_cuda or W.dim() != 2
                          or W.shape[1] != X.shape[1] for W in Ws):
             raise ValueError(f"calls[{i}]: weights must be 2-D host tensors with K = {X.shape[1]}")
+        for t in (X, *Ws):
+            if t.dtype != torch.float16 or not t.is_contiguous():
+                raise TypeError(f"calls[{i}]: inputs must be contiguous float16")
     device = torch.device(device)
     if device.index is None:
         device = torch.device("cuda", torch.cuda.current_device())
-    compute = torch.cuda.current_stream(device)
-    s_in = torch.cuda.Stream(device)
-    s_out = torch.cuda.Stream(device)
-    # Two input slots sized for the largest layer, allocated on the compute
-    # stream before any copy (no allocator traffic inside the pipeline).
-    x_max = max(X.numel() for X, _ in calls)
-    w_max = max(sum(W.numel() for W in Ws) for _, Ws in calls)
+    keep = []                    # ctypes arrays referenced by the layer structs
+    layers = (HostLayer * len(calls))()
+    out: List[dict] = []
+    for i, (X, Ws) in enumerate(calls):
+        T, K = X.shape
+        gpr = groups_per_row(K, group)
+        o = {"codes": [torch.empty(packed_words(W.shape[0], K, bits), dtype=torch.int32,
+                                   pin_memory=True) for W in Ws],
+             "scales": [torch.empty((W.shape[0], gpr), dtype=torch.float16, pin_memory=True)
+                        for W in Ws],
+             "zeros": [torch.empty((W.shape[0], gpr), dtype=torch.uint8, pin_memory=True)
+                       for W in Ws],
+             "s": torch.empty(K, dtype=torch.float32, pin_memory=True),
+             "losses": np.zeros(n_grid, dtype=np.float64),
+             "best": np.zeros(1, dtype=np.int32)}
+        warr = (Weight * len(Ws))()
+        for j, W in enumerate(Ws):
+            warr[j].W = W.data_ptr()
+            warr[j].N = W.shape[0]
+        ptrs = [(ctypes.c_void_p * len(Ws))(*[t.data_ptr() for t in o[key]])
+                for key in ("codes", "scales", "zeros")]
+        keep += [warr, *ptrs]
+        L = layers[i]
+        L.X, L.T, L.K = X.data_ptr(), T, K
+        L.Ws, L.n_w = warr, len(Ws)
+        L.codes, L.scales, L.zeros = ptrs
+        L.s = o["s"].data_ptr()
+        L.losses = o["losses"].ctypes.data
+        L.best = o["best"].ctypes.data
+        out.append(o)
+    cfg = _cfg(bits, group, n_grid, zero_point)
     with torch.cuda.device(device):
-        slots = [(torch.empty(x_max, dtype=torch.float16, device=device),
-                  torch.empty(w_max, dtype=torch.float16, device=device)) for _ in range(2)]
-    slot_free = [None, None]
-    pending = []
-    out: List[dict] = [None] * len(calls)
-
-    def retire(item):
-        idx, r, done, copied, host = item
-        done.synchronize()                    # this search only, not the stream
-        try:
-            host.update(r.host_values())
-        finally:
-            compute.wait_event(copied)        # the free follows the copy-out
-            with torch.cuda.stream(compute):
-                r.free()
-        copied.synchronize()
-        out[idx] = host
-
-    try:
-        for i, (X, Ws) in enumerate(calls):
-            k = i % 2
-            xs, ws = slots[k]
-            with torch.cuda.stream(s_in):
-                if slot_free[k] is not None:
-                    s_in.wait_event(slot_free[k])
-                Xd = xs[:X.numel()].view(X.shape)
-                Xd.copy_(X, non_blocking=True)
-                Wd, off = [], 0
-                for W in Ws:
-                    Wd.append(ws[off:off + W.numel()].view(W.shape))
-                    Wd[-1].copy_(W, non_blocking=True)
-                    off += W.numel()
-                ready = torch.cuda.Event()
-                ready.record(s_in)
-            compute.wait_event(ready)
-            with torch.cuda.stream(compute):
-                r = search(Xd, Wd, bits, group, n_grid, zero_point=zero_point)
-                done = torch.cuda.Event()
-                done.record(compute)
-            slot_free[k] = done
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done)
-                v = r.device_views()
-
-                def pinned_copy(t):
-                    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                    h.copy_(t, non_blocking=True)
-                    return h
-
-                host = {
-                    "codes": [pinned_copy(t) for t in v["codes"]],
-                    "scales": [pinned_copy(t) for t in v["scales"]],
-                    "zeros": [pinned_copy(t) for t in v["zeros"]],
-                    "s": pinned_copy(v["s"]),
-                }
-                copied = torch.cuda.Event()
-                copied.record(s_out)
-            pending.append((i, r, done, copied, host))
-            if len(pending) > 1:
-                retire(pending.pop(0))
-        while pending:
-            retire(pending.pop(0))
-    except BaseException:
-        # A failed call: let the searches already enqueued finish, then free
-        # their results, so nothing is left pending on the device.
-        for _, r, done, copied, _ in pending:
-            try:
-                copied.synchronize()
-            finally:
-                r.free()
-        raise
+        _check(lib().awq_search_host_layers(layers, len(calls), ctypes.byref(cfg), _stream()))
+    for o in out:
+        o["best"] = int(o["best"][0])
+        o["alpha"] = o["best"] / n_grid
     return out
+
+
+def inject_allocation_failures(skip: int, count: int) -> None:
+    """After ``skip`` pool allocations, make the next ``count`` fail as out of
+    memory (awq_inject_allocation_failures; count 0 disarms)."""
+    lib().awq_inject_allocation_failures(int(skip), int(count))
+
+
+def pool_usage() -> Tuple[int, int]:
+    """(used, reserved) bytes of the library pool on the current device."""
+    used, reserved = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().awq_pool_usage(ctypes.byref(used), ctypes.byref(reserved)))
+    return int(used.value), int(reserved.value)
 
 
 def set_stage_timing(enable: bool) -> None:

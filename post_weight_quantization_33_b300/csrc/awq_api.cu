@@ -126,10 +126,31 @@ cudaMemPool_t pool_for_current_device(cudaError_t* err) {
   return pool;
 }
 
+// Allocation-failure injection (awq_inject_allocation_failures): the next
+// g_alloc_skip pool allocations go through, then g_alloc_fail of them report
+// cudaErrorMemoryAllocation without reaching the allocator.
+std::mutex g_inject_mu;
+int g_alloc_skip = 0, g_alloc_fail = 0;
+
+bool injected_failure() {
+  std::lock_guard<std::mutex> lock(g_inject_mu);
+  if (g_alloc_fail <= 0) return false;
+  if (g_alloc_skip > 0) {
+    --g_alloc_skip;
+    return false;
+  }
+  --g_alloc_fail;
+  return true;
+}
+
 cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t st) {
   cudaError_t e;
   cudaMemPool_t pool = pool_for_current_device(&e);
   if (pool == nullptr) return e;
+  if (injected_failure()) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
   return cudaMallocFromPoolAsync(p, bytes < 256 ? 256 : bytes, pool, st);
 }
 
@@ -341,13 +362,11 @@ awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uin
                             float* y, void* stream) {
   awq_status st;
   if ((st = check_cfg(cfg)) != AWQ_OK) return st;
-  if (cfg->bits != 4)
-    return fail(AWQ_ERR_UNSUPPORTED, "bits=%d (the W4A16 product takes INT4 codes)", cfg->bits);
-  if (N < 1 || N > (int64_t(1) << 31) || !k_fits(K, cfg) || K % 8 || K > (int64_t(1) << 31))
-    return fail(AWQ_ERR_INVALID, "N=%lld K=%lld (N >= 1; K a multiple of 8 and of the group)",
+  if (N < 1 || N > (int64_t(1) << 31) || !k_fits(K, cfg) || K % 64 || K > (int64_t(1) << 31))
+    return fail(AWQ_ERR_INVALID, "N=%lld K=%lld (N >= 1; K a multiple of 64 and of the group)",
                 static_cast<long long>(N), static_cast<long long>(K));
-  if (M < 1 || M > 8) return fail(AWQ_ERR_INVALID, "M=%d (1..8)", M);
-  if ((st = check_dev(codes, "codes", 16)) != AWQ_OK) return st;   // 16-byte code loads
+  if (M < 1 || M > 16) return fail(AWQ_ERR_INVALID, "M=%d (1..16)", M);
+  if ((st = check_dev(codes, "codes", 16)) != AWQ_OK) return st;
   if ((st = check_dev(scales, "scales", 2)) != AWQ_OK) return st;
   if ((st = check_dev(zeros, "zeros", 1)) != AWQ_OK) return st;
   if ((st = check_dev(x, "x", 16)) != AWQ_OK) return st;
@@ -355,8 +374,8 @@ awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uin
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto cleanup = [] {};
   AWQ_CUDA(launch_w4_matvec(codes, static_cast<const __half*>(scales), zeros, N, K,
-                            cfg->group_size, static_cast<const __half*>(x), M, y, s),
-           "W4A16 product kernel");
+                            cfg->group_size, cfg->bits, static_cast<const __half*>(x), M, y, s),
+           "decode product kernel");
   return ok();
 }
 
@@ -717,6 +736,28 @@ awq_status awq_release_cached_memory(void) {
   return ok();
 }
 
+void awq_inject_allocation_failures(int skip, int count) {
+  std::lock_guard<std::mutex> lock(g_inject_mu);
+  g_alloc_skip = skip > 0 ? skip : 0;
+  g_alloc_fail = count > 0 ? count : 0;
+}
+
+awq_status awq_pool_usage(int64_t* used_bytes, int64_t* reserved_bytes) {
+  if (used_bytes == nullptr || reserved_bytes == nullptr)
+    return fail(AWQ_ERR_INVALID, "used_bytes or reserved_bytes is NULL");
+  cudaError_t e;
+  cudaMemPool_t pool = pool_for_current_device(&e);
+  if (pool == nullptr) return cuda_fail(e, "pool lookup");
+  uint64_t used = 0, reserved = 0;
+  if ((e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &used)) != cudaSuccess ||
+      (e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &reserved)) !=
+          cudaSuccess)
+    return cuda_fail(e, "pool attribute");
+  *used_bytes = static_cast<int64_t>(used);
+  *reserved_bytes = static_cast<int64_t>(reserved);
+  return ok();
+}
+
 awq_status awq_selftest_bounded_wait(int64_t limit_ns) {
   if (limit_ns < 1000 || limit_ns > 5000000000ll)
     return fail(AWQ_ERR_INVALID, "limit_ns=%lld (1e3..5e9)", static_cast<long long>(limit_ns));
@@ -753,6 +794,14 @@ AWQ_HIDDEN awq_status awq_internal_fail(awq_status st, const char* fmt, ...) {
 }
 
 AWQ_HIDDEN awq_status awq_internal_ok() { return ok(); }
+
+AWQ_HIDDEN awq_status awq_internal_check_cfg(const awq_qconfig* cfg) { return check_cfg(cfg); }
+
+AWQ_HIDDEN bool awq_internal_k_fits(int64_t K, const awq_qconfig* cfg) { return k_fits(K, cfg); }
+
+AWQ_HIDDEN cudaError_t awq_internal_pool_alloc(void** p, size_t bytes, cudaStream_t st) {
+  return pool_alloc(p, bytes, st);
+}
 
 AWQ_HIDDEN awq_status awq_internal_check_dev(const void* p, const char* name, uintptr_t align) {
   return check_dev(p, name, align);

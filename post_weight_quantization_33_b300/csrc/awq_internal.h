@@ -116,12 +116,12 @@ cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_
                                    int64_t n_pad, int n_alpha, float* partials, int* status,
                                    cudaStream_t st);
 
-// ---- W4A16 product (awq_matvec.cu)
-// y[m][n] = sum_k (code - zero) * scale * x[m][k], fp32 [M][N], 1 <= M <= 8,
-// INT4 codes [N][K/8], group 64, 128 or -1.
+// ---- decode product (awq_matvec.cu)
+// y[m][n] = sum_k (code - zero) * scale * x[m][k], fp32 [M][N] (zeroed here),
+// 1 <= M <= 16, INT4 or INT3 packed codes, group 64, 128 or -1, K % 64 == 0.
 cudaError_t launch_w4_matvec(const uint32_t* codes, const __half* scales, const uint8_t* zeros,
-                             int64_t N, int64_t K, int group, const __half* x, int M, float* y,
-                             cudaStream_t st);
+                             int64_t N, int64_t K, int group, int bits, const __half* x, int M,
+                             float* y, cudaStream_t st);
 
 // ---- loss reduction (awq_reduce.cu)
 // Number of 256-row chunks of the padded row space (chunk_sums holds

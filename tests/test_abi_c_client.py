@@ -1,7 +1,8 @@
 """The C ABI from a plain C99 program (tests/abi_c/awq_client.c), compiled with
 gcc against include/awq.h and linked with libawq.so: the header is valid C,
 every declared call links, the GPU-free calls behave as documented, and on a
-B300 a search run from C gives exactly what the Python binding gives."""
+B300 a search run from C -- on device buffers, or through the host-buffer
+pipeline -- gives exactly what the Python binding gives."""
 import os
 import shutil
 import subprocess
@@ -39,7 +40,11 @@ def test_c_client_cpu_calls(tmp_path):
 
 
 @pytest.mark.gpu
-def test_c_client_search_matches_binding(tmp_path):
+@pytest.mark.parametrize("mode", ["gpu", "host"])
+def test_c_client_search_matches_binding(tmp_path, mode):
+    """mode gpu: awq_search_layer on device buffers the C program filled;
+    mode host: awq_search_host_layers from plain host buffers (three copies
+    of the layer in one call, which the program checks agree)."""
     import torch
     import workloads
     exe = _build(tmp_path)
@@ -48,7 +53,7 @@ def test_c_client_search_matches_binding(tmp_path):
     W.tofile(tmp_path / "w.bin")
     T, K = X.shape
     N = W.shape[0]
-    out = subprocess.run([exe, "gpu", str(T), str(K), str(N), str(tmp_path / "x.bin"),
+    out = subprocess.run([exe, mode, str(T), str(K), str(N), str(tmp_path / "x.bin"),
                           str(tmp_path / "w.bin"), str(tmp_path / "losses.bin"),
                           str(tmp_path / "codes.bin")], capture_output=True, text=True,
                          timeout=120)

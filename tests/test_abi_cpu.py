@@ -88,10 +88,19 @@ def test_invalid_arguments_rejected_before_launch(L):
     assert L.awq_quantize_pack(None, 0, 256, None, _cfg(), None, None, None, None) == 0
     assert L.awq_unpack_codes(None, 2, 100, 4, None, None) == INVALID
     assert L.awq_reference_output(None, 4, None, 4, 100, None, None, None) == INVALID
-    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(bits=3), None, 1, None,
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(bits=5), None, 1, None,
                               None) == UNSUPPORTED
-    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 9, None, None) == INVALID
+    # 1..16 tokens; K a multiple of 64 (the product's 64-channel unit)
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 17, None, None) == INVALID
+    assert b"M=17" in L.awq_last_error()
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 0, None, None) == INVALID
     assert L.awq_w4a16_matvec(None, None, None, 4, 200, _cfg(), None, 1, None, None) == INVALID
+    assert L.awq_w4a16_matvec(None, None, None, 4, 96, _cfg(group=-1), None, 1, None,
+                              None) == INVALID
+    # INT3 codes and 16 tokens pass the argument checks (NULL codes fail next)
+    assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(bits=3), None, 16, None,
+                              None) == INVALID
+    assert b"codes" in L.awq_last_error()
     assert L.awq_w4a16_matvec(None, None, None, 4, 256, _cfg(), None, 1, None, None) == INVALID
     # codes are read 16 bytes at a time: a 4-byte aligned pointer is refused
     assert L.awq_w4a16_matvec(ctypes.c_void_p(0x1004), None, None, 4, 256, _cfg(), None, 1, None,

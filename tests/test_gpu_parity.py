@@ -225,47 +225,73 @@ def test_fold_after_search_keeps_layer_output():
 
 
 # --------------------------------------------------------------------------
-# W4A16 product with the packed layer: within a stated fp32 rounding bound.
+# Decode product with the packed layer (W4A16 / W3A16): within a derived
+# fp32 rounding bound.
 # --------------------------------------------------------------------------
 def _matvec_bound(codes, sc, z, group, x):
-    """|y_gpu - y| <= (words + 8) * 2^-23 * sum_k |deq_k x_k|: every product is
-    exact in fp32; the per-word sums (8 terms), the scaled running sums (one
-    per word) and the 32-lane reduction each round once per step."""
+    """Every product (code - zero) * x is exact in fp32 (a 4-bit integer
+    times an fp16 value).  A group of g channels is summed in fp32 on the
+    tensor cores (at most g additions, each off by at most 2^-23 of the sum of
+    magnitudes so far), scaled once, and added to the row's running sum (one
+    addition per group), and at most two partial results meet in y.  So
+    |y - y_exact| <= (g + K/g + 4) * 2^-23 * sum_k |deq_k x_k|."""
+    K = codes.shape[1]
+    g = K if group == -1 else group
     deq = O.dequantize_scaled(codes, sc, z, group)
     mag = np.abs(x.astype(np.float64)) @ np.abs(deq).T
-    return (codes.shape[1] / 8 + 8 + 5) * 2.0 ** -23 * mag
+    return (g + K / g + 4) * 2.0 ** -23 * mag
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 8])
+@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("M", [1, 2, 8, 9, 16])
 @pytest.mark.parametrize("N,K,group", [(1, 128, 128), (37, 256, 64), (300, 1024, 128),
-                                       (129, 4096, -1), (64, 11008, 128)])
-def test_w4a16_matvec(M, N, K, group):
-    rng = workloads.weight_rng(M * 100 + N + K + group)
+                                       (129, 4096, -1), (64, 11008, 64)])
+def test_decode_product(M, N, K, group, bits):
+    rng = workloads.weight_rng(M * 100 + N + K + group + bits)
     W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
     s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
-    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), 4, group)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group)
     x = rng.standard_normal((M, K)).astype(np.float16)
-    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), group))
-    oc, osc, oz = O.quantize_groups(W, s, 4, group)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), group, bits=bits))
+    oc, osc, oz = O.quantize_groups(W, s, bits, group)
     want = O.w4a16_matvec(oc, osc, oz, group, x)
     err = np.abs(y.astype(np.float64) - want)
     assert np.all(err <= _matvec_bound(oc, osc, oz, group, x) + 1e-30), float(err.max())
 
 
-def test_w4a16_matvec_long_k_chunks():
-    """K = 28672 at M = 8 does not fit shared memory at once: x is staged in
-    chunks along K."""
-    rng = workloads.weight_rng(4242)
-    N, K, M = 40, 28672, 8
+@pytest.mark.parametrize("bits", [4, 3])
+def test_decode_product_large_and_deterministic(bits):
+    """A 70B-class MLP shape (K = 28672) at 16 tokens, where every warp's
+    range spans tile boundaries: within the bound, and identical on a
+    second run (at most two partial sums meet in an output)."""
+    rng = workloads.weight_rng(4242 + bits)
+    N, K, M = 520, 28672, 16
     W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
     s = np.ones(K, np.float32)
-    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), 4, 128)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, 128)
     x = rng.standard_normal((M, K)).astype(np.float16)
-    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), 128))
-    oc, osc, oz = O.quantize_groups(W, s, 4, 128)
+    xd = cuda(x)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, xd, 128, bits=bits))
+    y2 = host(awq.w4a16_matvec(codes, sc, z, N, K, xd, 128, bits=bits))
+    assert np.array_equal(y, y2)
+    oc, osc, oz = O.quantize_groups(W, s, bits, 128)
     want = O.w4a16_matvec(oc, osc, oz, 128, x)
     err = np.abs(y.astype(np.float64) - want)
     assert np.all(err <= _matvec_bound(oc, osc, oz, 128, x) + 1e-30)
+
+
+def test_decode_product_symmetric_codes():
+    """Symmetric codes (zero point 2^(b-1)) use the same product."""
+    rng = workloads.weight_rng(77)
+    N, K = 200, 512
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.ones(K, np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), 4, 64, zero_point=False)
+    x = rng.standard_normal((5, K)).astype(np.float16)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), 64))
+    oc, osc, oz = O.quantize_groups(W, s, 4, 64, zero_point=False)
+    want = O.w4a16_matvec(oc, osc, oz, 64, x)
+    assert np.all(np.abs(y - want) <= _matvec_bound(oc, osc, oz, 64, x) + 1e-30)
 
 
 # --------------------------------------------------------------------------
