@@ -226,12 +226,15 @@ def cpu_baseline(data, wl, rows: int, steps: int = 2) -> dict:
             "sample": oracle_sample(rows, pool) + f"; {steps} timed steps, {dt:.1f} s"}
 
 
-def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
-    """Achieved HBM bandwidth of the two HBM-bound entry points at the
-    largest workload's sizes (X 8192x8192; W 28672x8192, INT4 g128), called
-    through the C ABI with preallocated buffers, L2 flushed between launches.
-    Bytes are the algorithmic ones: 2TK for the statistic; 2NK read +
-    NK/2 codes + 3NK/128 scales and zeros written for quantize + pack."""
+def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 5) -> dict:
+    """Achieved HBM bandwidth of the HBM-bound entry points at the largest
+    workload's sizes (X 8192x8192; W 28672x8192), called through the C ABI
+    with preallocated buffers.  Each figure times calls back to back over
+    several copies of the input, each larger than L2, so no call finds its
+    input in L2 and host launch gaps are hidden; per call = elapsed / calls.
+    Bytes are the algorithmic ones: 2TK for the statistic; 2NK read + b/8 NK
+    codes + 3NK/128 scales and zeros written for quantize + pack; codes,
+    scales, zeros, x read and y written for the decode product."""
     import ctypes
     import torch
     import post_weight_quantization_33_b300 as awq
@@ -242,75 +245,152 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 10) -> dict:
     g.manual_seed(7)
     out = {}
 
-    def timed(fn):
-        ts = []
-        fn()
-        for i in range(reps):
-            flush(i)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+    def timed(fns):
+        for fn in fns:                         # warm-up pass
             fn()
-            b.record(stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+        flush(0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            for fn in fns:
+                fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / (reps * len(fns))
 
     T, K = 8192, 8192
-    X = torch.randn(T, K, generator=g, device=dev).half()
+    Xs = [torch.randn(T, K, generator=g, device=dev).half() for _ in range(6)]
     sX = torch.empty(K, dtype=torch.float64, device=dev)
-    ms = timed(lambda: awq._check(L.awq_stats(X.data_ptr(), T, K, sX.data_ptr(), st)))
+    ms = timed([lambda X=X: awq._check(L.awq_stats(X.data_ptr(), T, K, sX.data_ptr(), st))
+                for X in Xs])
     nbytes = 2 * T * K
     out["stats"] = {"shape": f"X {T}x{K} fp16", "ms": ms, "bytes": nbytes,
-                    "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
+                    "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs,
+                    "calls": f"{len(Xs)} inputs x {reps}"}
     # Context, not a denominator: a library reduction (torch.amax) reading the
-    # same bytes -- the rate a plain read-only pass reaches at this size.
-    ms = timed(lambda: torch.amax(X))
+    # same bytes the same way.
+    ms = timed([lambda X=X: torch.amax(X) for X in Xs])
     out["read_only_context"] = {"X": {"bytes": nbytes, "ms": ms, "gbs": nbytes / ms / 1e6,
                                       "kernel": "torch.amax"}}
-    del X
+    del Xs
     N, K = 28672, 8192
-    W = (torch.randn(N, K, generator=g, device=dev) * 0.015).half()
+    Ws = [(torch.randn(N, K, generator=g, device=dev) * 0.015).half() for _ in range(3)]
+    W = Ws[0]
     s = torch.rand(K, generator=g, device=dev) + 0.5
-    codes = torch.empty(N * K // 8, dtype=torch.int32, device=dev)
-    sc = torch.empty(N * K // 128, dtype=torch.float16, device=dev)
-    z = torch.empty(N * K // 128, dtype=torch.uint8, device=dev)
+    codes = [torch.empty(N * K // 8, dtype=torch.int32, device=dev) for _ in Ws]
+    sc = [torch.empty(N * K // 128, dtype=torch.float16, device=dev) for _ in Ws]
+    z = [torch.empty(N * K // 128, dtype=torch.uint8, device=dev) for _ in Ws]
     cfg = awq.QConfig(4, 128, 1, N_GRID)
-    ms = timed(lambda: awq._check(L.awq_quantize_pack(
-        W.data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg), codes.data_ptr(), sc.data_ptr(),
-        z.data_ptr(), st)))
+    ms = timed([lambda i=i: awq._check(L.awq_quantize_pack(
+        Ws[i].data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg), codes[i].data_ptr(),
+        sc[i].data_ptr(), z[i].data_ptr(), st)) for i in range(len(Ws))])
     nbytes = 2 * N * K + N * K // 2 + 3 * N * K // 128
     out["quantize_pack"] = {"shape": f"W {N}x{K} fp16 -> INT4 g128", "ms": ms, "bytes": nbytes,
-                            "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs}
-    ms = timed(lambda: torch.amax(W))
+                            "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs,
+                            "calls": f"{len(Ws)} inputs x {reps}"}
+    ms = timed([lambda W=W: torch.amax(W) for W in Ws])
     out["read_only_context"]["W"] = {"bytes": 2 * N * K, "ms": ms, "gbs": 2 * N * K / ms / 1e6,
                                      "kernel": "torch.amax"}
     # The packed layer consumed at decode: the W4A16 product for 1 and 16
     # tokens and the W3A16 product for one token, each beside a cuBLAS fp16
     # product with the dense weight of the same shape.
-    codes3 = torch.empty(N * 3 * K // 32, dtype=torch.int32, device=dev)
-    sc3 = torch.empty(N * K // 128, dtype=torch.float16, device=dev)
-    z3 = torch.empty(N * K // 128, dtype=torch.uint8, device=dev)
     cfg3 = awq.QConfig(3, 128, 1, N_GRID)
-    awq._check(L.awq_quantize_pack(W.data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg3),
-                                   codes3.data_ptr(), sc3.data_ptr(), z3.data_ptr(), st))
+    codes3 = [torch.empty(N * 3 * K // 32, dtype=torch.int32, device=dev) for _ in Ws]
+    sc3 = [torch.empty(N * K // 128, dtype=torch.float16, device=dev) for _ in Ws]
+    z3 = [torch.empty(N * K // 128, dtype=torch.uint8, device=dev) for _ in Ws]
+    for i in range(len(Ws)):
+        awq._check(L.awq_quantize_pack(Ws[i].data_ptr(), N, K, s.data_ptr(), ctypes.byref(cfg3),
+                                       codes3[i].data_ptr(), sc3[i].data_ptr(), z3[i].data_ptr(),
+                                       st))
     decode = {}
     for bits, M in ((4, 1), (4, 16), (3, 1)):
         c_, s_, z_, cf = (codes, sc, z, cfg) if bits == 4 else (codes3, sc3, z3, cfg3)
         x = torch.randn(M, K, generator=g, device=dev).half()
         y = torch.empty(M, N, dtype=torch.float32, device=dev)
-        ms = timed(lambda: awq._check(L.awq_w4a16_matvec(
-            c_.data_ptr(), s_.data_ptr(), z_.data_ptr(), N, K, ctypes.byref(cf), x.data_ptr(), M,
-            y.data_ptr(), st)))
+        ms = timed([lambda i=i: awq._check(L.awq_w4a16_matvec(
+            c_[i].data_ptr(), s_[i].data_ptr(), z_[i].data_ptr(), N, K, ctypes.byref(cf),
+            x.data_ptr(), M, y.data_ptr(), st)) for i in range(len(Ws))])
         nbytes = N * K * bits // 8 + 3 * N * K // 128 + 2 * M * K + 4 * M * N
-        dense_ms = timed(lambda: torch.matmul(x, W.t()))
+        dense_ms = timed([lambda W=W: torch.matmul(x, W.t()) for W in Ws])
         decode[f"int{bits}_m{M}"] = {
             "shape": f"W {N}x{K} INT{bits} g128, {M} token(s)", "ms": ms, "bytes": nbytes,
             "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / hbm_gbs,
             "fp16_cublas_ms": dense_ms, "speedup_vs_fp16": dense_ms / ms}
     out["decode_product"] = decode
-    del W
+    del Ws, W
     return out
+
+
+def dequant_mainloop_bound(calls, flush, stages_ms: dict, step_ms: float) -> dict:
+    """Measured lower bound on the step time of the design that dequantizes
+    packed codes inside the error GEMM's main loop and subtracts a prologue
+    reference output Y = W X^T in its epilogue (instead of this library's
+    fp16 residual pass).  That design cannot avoid (a) the prologue GEMM
+    Y = W X^T and (b) a quantize + pack pass per grid point writing the codes
+    its main loop reads; its MMA work equals this GEMM's.  Both are timed
+    here on this step's weights (this library's own tcgen05 reference GEMM
+    and quantize + pack kernels); the bound assumes the dequantization costs
+    the main loop nothing and the epilogue's reads of Y (4 N T bytes per grid
+    point) are free:  bound = step - residual pass + (a) + (b)."""
+    import ctypes
+    import torch
+    import post_weight_quantization_33_b300 as awq
+    L = awq.lib()
+    stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+    yref_ms = quant_ms = 0.0
+    for X, Ws, bits, group in calls:
+        T, K = X.shape
+        r = awq.search(X, Ws, bits, group, N_GRID)
+        r.check()
+        s_grid = r.s_grid()
+        r.free()
+        cfg = awq.QConfig(bits, group, 1, N_GRID)
+        for W in Ws:
+            N = W.shape[0]
+            Y = torch.empty(N, T, dtype=torch.float32, device=X.device)
+            status = torch.zeros(1, dtype=torch.int32, device=X.device)
+            words = awq.packed_words(N, K, bits)
+            gpr = awq.groups_per_row(K, group)
+            outs = [(torch.empty(words, dtype=torch.int32, device=X.device),
+                     torch.empty(N * gpr, dtype=torch.float16, device=X.device),
+                     torch.empty(N * gpr, dtype=torch.uint8, device=X.device))
+                    for _ in range(N_GRID)]
+
+            def yref():
+                awq._check(L.awq_reference_output(W.data_ptr(), N, X.data_ptr(), T, K,
+                                                  Y.data_ptr(), status.data_ptr(), st))
+
+            def quant_all():
+                for a in range(N_GRID):
+                    c, sc, z = outs[a]
+                    awq._check(L.awq_quantize_pack(W.data_ptr(), N, K, s_grid[a].data_ptr(),
+                                                   ctypes.byref(cfg), c.data_ptr(), sc.data_ptr(),
+                                                   z.data_ptr(), st))
+
+            for fn, which in ((yref, "y"), (quant_all, "q")):
+                fn()
+                flush(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                if which == "y":
+                    yref_ms += e0.elapsed_time(e1)
+                else:
+                    quant_ms += e0.elapsed_time(e1)
+            assert int(status.item()) == 0
+            del Y, outs
+    residual = stages_ms["residual"]
+    return {"reference_gemm_ms": yref_ms, "quantize_all_grid_points_ms": quant_ms,
+            "residual_pass_ms": residual, "step_ms": step_ms,
+            "bound_ms": step_ms - residual + yref_ms + quant_ms,
+            "note": "lower bound for dequant-in-mainloop + prologue reference GEMM: this step "
+                    "minus its residual pass plus (a) Y = W X^T and (b) quantize + pack at every "
+                    "grid point, both measured here"}
 
 
 class L2Flush:
@@ -550,6 +630,8 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
     res_ms = stage_sum["residual"] / args.steps
     res_bytes = sum(2 * wl.spec(w).rows * wl.spec(w).cols * (1 + N_GRID)
                     for c in wl.calls for w in c.ws)
+    line["dequant_mainloop_bound"] = dequant_mainloop_bound(
+        calls, flush, {k: v / args.steps for k, v in stage_sum.items()}, total_ms / args.steps)
     line["hbm_kernels"] = hbm_kernels(dev, flush, pk["hbm_gbs"])
     line["hbm_kernels"]["residual"] = {
         "shape": "this workload, every grid point", "ms": res_ms, "bytes": res_bytes,

@@ -26,11 +26,18 @@
 // permutes.  (code - zero) is formed exactly in fp16: 0x6400 | code is
 // 1024 + code, minus 1024 + zero.
 //
-// Work split.  One block per SM; the (row tile, unit) items, tile-major, are
-// cut into equal contiguous ranges, one per warp, each at least one row tile
-// long, so every SM gets the same work and at most two warps add into an
-// output (y is zeroed first; two fp32 additions onto zero commute, so the
-// result does not depend on their order).
+// Work split.  One block of 16 warps per SM.  The (row tile, unit) items,
+// tile-major, are cut into equal contiguous ranges, one per block (each at
+// least one row tile long), and a block's range into one contiguous range per
+// warp.  A warp streams its units with the codes and group parameters of the
+// next kPrefetch units in flight, across row-tile boundaries.  A row tile
+// entirely inside one warp's range is added to y at once; the partial sums of
+// the tiles at the two ends of a warp's range go to shared memory, and the
+// block adds them up in warp order before adding them to y.  y is zeroed
+// first and at most two blocks add into an output (two fp32 additions onto
+// zero commute), so the result is deterministic.  x is staged once per block
+// in shared memory when M x K fits (16-byte chunks swizzled by token, so a
+// quad-row read is conflict-free), else read through L1.
 #include <algorithm>
 
 #include "awq_internal.h"
@@ -38,9 +45,9 @@
 namespace awq {
 namespace {
 
-constexpr int kUnit = 64;        // channels per unit
-constexpr int kPrefetch = 8;     // units of codes in flight per warp
-constexpr int kMaxWarps = 12;    // per block (one block per SM)
+constexpr int kUnit = 64;          // channels per unit
+constexpr int kMaxWarps = 16;      // per block (one block per SM)
+constexpr int kXSmemMax = 192 * 1024;
 
 __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
   uint32_t v;
@@ -71,34 +78,30 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// The 16 codes of one row that thread c uses in a unit, as two 32-bit
-// fields holding codes 0..7 and 8..15 in consecutive b-bit slots.
-template <int BITS>
-struct RowCodes {
+// One unit of one row as thread c needs it: codes 16c .. 16c+15 of the unit
+// as two fields (codes 0..7 and 8..15 in consecutive b-bit slots).
+struct UnitRow {
   uint32_t lo, hi;
 };
 
-// INT4: codes 16c .. 16c+15 of the unit are words 2c, 2c+1 (8 codes each).
-// INT3: they are bits [48c, 48c+48) of the unit's 6 words.
 template <int BITS>
-__device__ __forceinline__ RowCodes<BITS> load_codes(const uint32_t* row, int64_t unit, int c) {
-  RowCodes<BITS> r;
-  if (BITS == 4) {
+__device__ __forceinline__ void load_fields(const uint32_t* row, int64_t unit, int c,
+                                            uint32_t& lo, uint32_t& hi) {
+  if (BITS == 4) {   // words 2c, 2c+1 of the unit's 8
     const uint2 v = ld_stream_u64(row + unit * 8 + 2 * c);
-    r.lo = v.x;
-    r.hi = v.y;
-  } else {
+    lo = v.x;
+    hi = v.y;
+  } else {           // bits [48c, 48c+48) of the unit's 6 words
     const uint32_t* u = row + unit * 6 + (3 * c) / 2;
     const uint32_t w0 = ld_stream_u32(u), w1 = ld_stream_u32(u + 1);
-    if (c & 1) {   // the 48 bits start at bit 16 of w0
-      r.lo = __funnelshift_r(w0, w1, 16) & 0xFFFFFFu;
-      r.hi = w1 >> 8;
+    if (c & 1) {
+      lo = __funnelshift_r(w0, w1, 16) & 0xFFFFFFu;
+      hi = w1 >> 8;
     } else {
-      r.lo = w0 & 0xFFFFFFu;
-      r.hi = __funnelshift_r(w0, w1, 24) & 0xFFFFFFu;
+      lo = w0 & 0xFFFFFFu;
+      hi = __funnelshift_r(w0, w1, 24) & 0xFFFFFFu;
     }
   }
-  return r;
 }
 
 // 1024 + code_j (low half) and 1024 + code_{j+4} (high half) of a field.
@@ -109,139 +112,216 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t f, int j) {
   return (t & 0x7u) | ((t << 4) & 0x70000u) | 0x64006400u;
 }
 
-template <int NT, int GROUP, int BITS>
-__global__ void __launch_bounds__(kMaxWarps * 32)
+template <int NT, int GROUP, int BITS, bool XSMEM>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
     k_wq_mma(const uint32_t* __restrict__ codes, const __half* __restrict__ scales,
              const uint8_t* __restrict__ zeros, int64_t N, int64_t K,
              const __half* __restrict__ x, int M, float* __restrict__ y) {
-  const int lane = threadIdx.x & 31;
+  extern __shared__ uint4 xs[];   // XSMEM: x [M][K/8] 16-byte chunks, chunk j of token t at j ^ (t & 7)
+  // Partial sums of the first and last tile of each warp's range.
+  __shared__ float part_smem[kMaxWarps][2][16 * 16];
+  __shared__ int64_t part_tile[kMaxWarps][2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t upr = K / kUnit;                        // units per row
+  const int64_t upr = K / kUnit;
   const int64_t tiles = (N + 15) / 16;
   const int64_t items = tiles * upr;
-  const int64_t i0 = w * items / warps, i1 = (w + 1) * items / warps;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
+  const int64_t b1 = (static_cast<int64_t>(blockIdx.x) + 1) * items / gridDim.x;
+  const int64_t i0 = b0 + (b1 - b0) * warp / nwarps;
+  const int64_t i1 = b0 + (b1 - b0) * (warp + 1) / nwarps;
   const int64_t words_per_row = K * BITS / 32;
   const int64_t groups = GROUP ? K / GROUP : 1;
   constexpr int kUnitsPerGroup = GROUP ? GROUP / kUnit : 1;
+  // Units of codes in flight per warp (fewer with 16 tokens: more registers
+  // per unit).
+  constexpr int kPrefetch = NT == 1 ? 8 : 5;
 
-  int64_t i = i0;
-  while (i < i1) {
-    const int64_t tile = i / upr;
-    const int64_t u0 = i - tile * upr;
-    const int64_t u1 = min(upr, u0 + (i1 - i));
-    const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-    const int64_t l0 = min(r0, N - 1), l1 = min(r1, N - 1);
-    const uint32_t* row0 = codes + l0 * words_per_row;
-    const uint32_t* row1 = codes + l1 * words_per_row;
-    float acc[NT][4], part[NT][4];
+  if constexpr (XSMEM) {
+    const int64_t cpr = K / 8;
+    for (int64_t q = threadIdx.x; q < M * cpr; q += blockDim.x) {
+      const int64_t t = q / cpr, j = q - t * cpr;
+      xs[t * cpr + (j ^ (t & 7))] = __ldg(reinterpret_cast<const uint4*>(x) + q);
+    }
+  }
+  if (lane == 0) {
+    part_tile[warp][0] = -1;
+    part_tile[warp][1] = -1;
+  }
+  __syncthreads();
+
+  // Codes of a unit: streamed from HBM, kPrefetch units ahead.  The group
+  // parameters (3 bytes per row and group) are read when the unit is used:
+  // a row's 32-byte sector of zeros or scales serves 16 to 32 groups, so they
+  // come from L1 after the row's first unit.
+  auto load_unit = [&](int64_t item, UnitRow& r0, UnitRow& r1) {
+    const int64_t tile = item / upr, unit = item - tile * upr;
+    const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+    load_fields<BITS>(codes + l0 * words_per_row, unit, c, r0.lo, r0.hi);
+    load_fields<BITS>(codes + l1 * words_per_row, unit, c, r1.lo, r1.hi);
+  };
+
+  UnitRow q0[kPrefetch], q1[kPrefetch];
+#pragma unroll
+  for (int p = 0; p < kPrefetch; ++p)
+    if (i0 + p < i1) load_unit(i0 + p, q0[p], q1[p]);
+
+  float acc[NT][4], part[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
+  int64_t cur_tile = i0 < i1 ? i0 / upr : -1;
+  int64_t tile_first = i0;   // first item of the current tile inside this range
+  float last_sf0 = 0.f, last_sf1 = 0.f;   // group scales of the last unit done
+
+  // Close the current tile: scale the group the range leaves open (per-row
+  // groups: always), then add the tile to y if it lies entirely inside this
+  // warp's range, else park it in shared memory for the block's sum.
+  auto finish_tile = [&](int64_t tile, int64_t first, int64_t end) {
+    if (GROUP == 0 || (end - tile * upr) % kUnitsPerGroup != 0) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        acc[t][0] = __fmaf_rn(last_sf0, part[t][0], acc[t][0]);
+        acc[t][1] = __fmaf_rn(last_sf0, part[t][1], acc[t][1]);
+        acc[t][2] = __fmaf_rn(last_sf1, part[t][2], acc[t][2]);
+        acc[t][3] = __fmaf_rn(last_sf1, part[t][3], acc[t][3]);
+      }
+    }
+    const bool whole = first == tile * upr && end == (tile + 1) * upr;
+    if (whole) {
+      const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int m0 = t * 8 + 2 * c;
+        if (r0 < N) {
+          if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
+          if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
+        }
+        if (r1 < N) {
+          if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
+          if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
+        }
+      }
+    } else {
+      const int slot = first == i0 ? 0 : 1;   // the range's first or last tile
+      float* ps = part_smem[warp][slot];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int m0 = t * 8 + 2 * c;
+        ps[g * 16 + m0] = acc[t][0];
+        ps[g * 16 + m0 + 1] = acc[t][1];
+        ps[(g + 8) * 16 + m0] = acc[t][2];
+        ps[(g + 8) * 16 + m0 + 1] = acc[t][3];
+      }
+      if (lane == 0) part_tile[warp][slot] = tile;
+    }
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
-    // Codes of the next kPrefetch units in flight.
-    RowCodes<BITS> q0[kPrefetch], q1[kPrefetch];
+  };
+
+  for (int64_t base = i0; base < i1; base += kPrefetch) {
 #pragma unroll
-    for (int p = 0; p < kPrefetch; ++p)
-      if (u0 + p < u1) {
-        q0[p] = load_codes<BITS>(row0, u0 + p, c);
-        q1[p] = load_codes<BITS>(row1, u0 + p, c);
+    for (int p = 0; p < kPrefetch; ++p) {
+      const int64_t it = base + p;
+      if (it >= i1) break;
+      const int64_t tile = it / upr, unit = it - tile * upr;
+      if (tile != cur_tile) {
+        finish_tile(cur_tile, tile_first, it);
+        cur_tile = tile;
+        tile_first = it;
       }
-    for (int64_t u = u0; u < u1; u += kPrefetch) {
-#pragma unroll
-      for (int p = 0; p < kPrefetch; ++p) {
-        const int64_t uu = u + p;
-        if (uu >= u1) break;
-        const RowCodes<BITS> a0 = q0[p], a1 = q1[p];
-        if (uu + kPrefetch < u1) {
-          q0[p] = load_codes<BITS>(row0, uu + kPrefetch, c);
-          q1[p] = load_codes<BITS>(row1, uu + kPrefetch, c);
-        }
-        const int64_t k0 = uu * kUnit;
-        int64_t grp = 0;
-        if constexpr (GROUP != 0) grp = k0 / GROUP;
-        // 1024 + zero of each row in both halves (exact: fp16 bits 0x6400 + z).
-        const uint32_t z0 = 0x6400u + zeros[l0 * groups + grp];
-        const uint32_t z1 = 0x6400u + zeros[l1 * groups + grp];
-        const uint32_t zp0 = z0 | (z0 << 16), zp1 = z1 | (z1 << 16);
-        // x of this thread's tokens at channels k0 + 16c .. + 15.
-        uint4 xv[NT][2];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const int tok = t * 8 + g;
-          if (tok < M) {
-            const uint4* xp = reinterpret_cast<const uint4*>(x + tok * K + k0 + 16 * c);
-            xv[t][0] = __ldg(xp);
-            xv[t][1] = __ldg(xp + 1);
-          } else {
-            xv[t][0] = xv[t][1] = make_uint4(0, 0, 0, 0);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t a[4];
-          a[0] = hsub2_u32(code_pair<BITS>(a0.lo, j), zp0);   // row g,   slots 2c, 2c+1
-          a[1] = hsub2_u32(code_pair<BITS>(a1.lo, j), zp1);   // row g+8
-          a[2] = hsub2_u32(code_pair<BITS>(a0.hi, j), zp0);   // row g,   slots 2c+8, 2c+9
-          a[3] = hsub2_u32(code_pair<BITS>(a1.hi, j), zp1);   // row g+8
-          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const uint32_t X[8] = {xv[t][0].x, xv[t][0].y, xv[t][0].z, xv[t][0].w,
-                                   xv[t][1].x, xv[t][1].y, xv[t][1].z, xv[t][1].w};
-            // x[16c + j], x[16c + j + 4]  and  x[16c + 8 + j], x[16c + 12 + j]
-            const uint32_t b0 = __byte_perm(X[j >> 1], X[(j >> 1) + 2], sel);
-            const uint32_t b1 = __byte_perm(X[4 + (j >> 1)], X[6 + (j >> 1)], sel);
-            mma_16816(part[t], a, b0, b1);
-          }
-        }
-        // End of a group (or of this warp's part of a per-row group).
-        bool group_end = uu + 1 == u1;
-        if constexpr (GROUP != 0) group_end = (uu + 1) % kUnitsPerGroup == 0;
-        if (group_end) {
-          const float s0 = __half2float(scales[l0 * groups + grp]);
-          const float s1 = __half2float(scales[l1 * groups + grp]);
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            acc[t][0] = __fmaf_rn(s0, part[t][0], acc[t][0]);
-            acc[t][1] = __fmaf_rn(s0, part[t][1], acc[t][1]);
-            acc[t][2] = __fmaf_rn(s1, part[t][2], acc[t][2]);
-            acc[t][3] = __fmaf_rn(s1, part[t][3], acc[t][3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) part[t][e] = 0.f;
-          }
-        }
-      }
-    }
-    // A range may end inside a group (g128: after its first unit): scale
-    // the partial sum of that group too.
-    if (GROUP != 0 && (u1 % kUnitsPerGroup) != 0) {
-      const int64_t grp = (u1 * kUnit - 1) / (GROUP != 0 ? GROUP : 1);
-      const float s0 = __half2float(scales[l0 * groups + grp]);
-      const float s1 = __half2float(scales[l1 * groups + grp]);
+      const UnitRow a0 = q0[p], a1 = q1[p];
+      if (it + kPrefetch < i1) load_unit(it + kPrefetch, q0[p], q1[p]);
+      const int64_t k0 = unit * kUnit;
+      int64_t grp = 0;
+      if constexpr (GROUP != 0) grp = unit / kUnitsPerGroup;
+      const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+      // 1024 + zero in both halves (exact: fp16 bits 0x6400 + z), and the scale.
+      const uint32_t z0 = 0x6400u + __ldg(zeros + l0 * groups + grp);
+      const uint32_t z1 = 0x6400u + __ldg(zeros + l1 * groups + grp);
+      const uint32_t zp0 = z0 | (z0 << 16), zp1 = z1 | (z1 << 16);
+      const float sf0 = __half2float(__ldg(scales + l0 * groups + grp));
+      const float sf1 = __half2float(__ldg(scales + l1 * groups + grp));
+      uint32_t X[NT][8];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        acc[t][0] = __fmaf_rn(s0, part[t][0], acc[t][0]);
-        acc[t][1] = __fmaf_rn(s0, part[t][1], acc[t][1]);
-        acc[t][2] = __fmaf_rn(s1, part[t][2], acc[t][2]);
-        acc[t][3] = __fmaf_rn(s1, part[t][3], acc[t][3]);
+        const int tok = t * 8 + g;
+        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+        if (tok < M) {
+          if constexpr (XSMEM) {
+            const int64_t j = (k0 + 16 * c) / 8;
+            const uint4* xrow = xs + static_cast<int64_t>(tok) * (K / 8);
+            v0 = xrow[j ^ (tok & 7)];
+            v1 = xrow[(j + 1) ^ (tok & 7)];
+          } else {
+            const uint4* xp = reinterpret_cast<const uint4*>(x + tok * K + k0 + 16 * c);
+            v0 = __ldg(xp);
+            v1 = __ldg(xp + 1);
+          }
+        }
+        X[t][0] = v0.x; X[t][1] = v0.y; X[t][2] = v0.z; X[t][3] = v0.w;
+        X[t][4] = v1.x; X[t][5] = v1.y; X[t][6] = v1.z; X[t][7] = v1.w;
       }
-    }
-    // C fragment: elements 0, 1 are row g, tokens 2c, 2c+1; 2, 3 row g+8.
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int m0 = t * 8 + 2 * c;
-      if (r0 < N) {
-        if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
-        if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a[4];
+        a[0] = hsub2_u32(code_pair<BITS>(a0.lo, j), zp0);   // row g,   slots 2c, 2c+1
+        a[1] = hsub2_u32(code_pair<BITS>(a1.lo, j), zp1);   // row g+8
+        a[2] = hsub2_u32(code_pair<BITS>(a0.hi, j), zp0);   // row g,   slots 2c+8, 2c+9
+        a[3] = hsub2_u32(code_pair<BITS>(a1.hi, j), zp1);   // row g+8
+        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          // x[16c + j], x[16c + j + 4]  and  x[16c + 8 + j], x[16c + 12 + j]
+          const uint32_t bb0 = __byte_perm(X[t][j >> 1], X[t][(j >> 1) + 2], sel);
+          const uint32_t bb1 = __byte_perm(X[t][4 + (j >> 1)], X[t][6 + (j >> 1)], sel);
+          mma_16816(part[t], a, bb0, bb1);
+        }
       }
-      if (r1 < N) {
-        if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
-        if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
+      last_sf0 = sf0;
+      last_sf1 = sf1;
+      // End of a group: scale it into the row's sum (per-row groups are
+      // scaled when their tile closes).
+      if (GROUP != 0 && (unit + 1) % kUnitsPerGroup == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);
+          acc[t][1] = __fmaf_rn(sf0, part[t][1], acc[t][1]);
+          acc[t][2] = __fmaf_rn(sf1, part[t][2], acc[t][2]);
+          acc[t][3] = __fmaf_rn(sf1, part[t][3], acc[t][3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) part[t][e] = 0.f;
+        }
       }
     }
-    i += u1 - u0;
+  }
+  if (i0 < i1) finish_tile(cur_tile, tile_first, i1);
+  __syncthreads();
+  // The parked partial sums, in warp order (equal tile ids are consecutive);
+  // thread e of the block owns element e of a tile (16 rows x 16 tokens).
+  for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x) {
+    const int row = e >> 4, tok = e & 15;
+    int64_t tile = -1;
+    float sum = 0.f;
+    for (int w = 0; w < nwarps; ++w) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int64_t t = part_tile[w][s];
+        if (t < 0) continue;
+        if (t != tile) {
+          if (tile >= 0 && tile * 16 + row < N && tok < M)
+            atomicAdd(y + tok * N + tile * 16 + row, sum);
+          tile = t;
+          sum = 0.f;
+        }
+        sum = __fadd_rn(sum, part_smem[w][s][e]);
+      }
+    }
+    if (tile >= 0 && tile * 16 + row < N && tok < M) atomicAdd(y + tok * N + tile * 16 + row, sum);
   }
 }
 
@@ -251,20 +331,30 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
                       float* y, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(M) * N, st);
   if (e != cudaSuccess) return e;
-  // One block per SM.  Warps: at most one per 16-row tile (every warp's range
-  // is then at least a tile long: at most two warps per output), at most 12.
+  // One block per SM, at most one per 16-row tile (every block's range is
+  // then at least a tile long: at most two blocks add into an output).
   const int64_t tiles = (N + 15) / 16;
-  const int sms = device_sm_count();
-  int64_t blocks = std::min<int64_t>(sms, tiles);
-  int64_t wpb = std::max<int64_t>(1, std::min<int64_t>(kMaxWarps, tiles / blocks));
+  const int64_t blocks = std::min<int64_t>(device_sm_count(), tiles);
+  const int64_t xbytes = static_cast<int64_t>(M) * K * 2;
+  const bool xsmem = xbytes <= kXSmemMax;
+  const int smem = xsmem ? static_cast<int>(xbytes) : 0;
   auto go = [&](auto kern) -> cudaError_t {
-    kern<<<static_cast<unsigned>(blocks), static_cast<unsigned>(32 * wpb), 0, st>>>(
-        codes, scales, zeros, N, K, x, M, y);
+    LaunchFacts lf;   // raises the kernel's dynamic shared memory limit once per device
+    cudaError_t err = launch_facts(reinterpret_cast<const void*>(kern), kMaxWarps * 32,
+                                   kXSmemMax, &lf);
+    if (err != cudaSuccess) return err;
+    kern<<<static_cast<unsigned>(blocks), kMaxWarps * 32, smem, st>>>(codes, scales, zeros, N, K,
+                                                                      x, M, y);
     return cudaGetLastError();
   };
-  if (group == 128) return go(k_wq_mma<NT, 128, BITS>);
-  if (group == 64) return go(k_wq_mma<NT, 64, BITS>);
-  return go(k_wq_mma<NT, 0, BITS>);
+  if (xsmem) {
+    if (group == 128) return go(k_wq_mma<NT, 128, BITS, true>);
+    if (group == 64) return go(k_wq_mma<NT, 64, BITS, true>);
+    return go(k_wq_mma<NT, 0, BITS, true>);
+  }
+  if (group == 128) return go(k_wq_mma<NT, 128, BITS, false>);
+  if (group == 64) return go(k_wq_mma<NT, 64, BITS, false>);
+  return go(k_wq_mma<NT, 0, BITS, false>);
 }
 
 }  // namespace

@@ -61,16 +61,14 @@ __device__ __forceinline__ void add_chunk(LaneSums& a, const uint4 v) {
                          v.w & 0x7FFF7FFFu};
   const f32x2 k24 = pack2(16777216.0f, 16777216.0f);
   const f32x2 c = pack2(kSplitC, kSplitC);
-  const f32x2 mc = pack2(-kSplitC, -kSplitC);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
     const f32x2 x = pack2(f.x, f.y);
     const f32x2 r = fma2(x, k24, c);                          // round(u) + C
-    const f32x2 fh = add2(r, mc);                             // round(u), exact
-    const f32x2 nfh = fh ^ 0x8000000080000000ull;             // -round(u)
+    const f32x2 nfh = sub2(c, r);                             // -round(u), exact
     a.lo[i] = add2(a.lo[i], fma2(x, k24, nfh));               // u - round(u), exact
-    a.hi[i] = add2(a.hi[i], fh);
+    a.hi[i] = sub2(a.hi[i], nfh);                             // + round(u)
   }
 }
 

@@ -22,7 +22,7 @@ BUDGET = [
     ("awq_quant.cu", r"k_quant_finalILi4E", 85, 0),
     ("awq_quant.cu", r"k_quant_finalILi3E", 85, 16),
     ("awq_stats.cu", r"k_stats_accumulate", 112, 0),   # 2 blocks of 288 threads per SM
-    ("awq_matvec.cu", r"k_wq_mma", 168, 0),   # one block of at most 12 warps per SM
+    ("awq_matvec.cu", r"k_wq_mma", 128, 0),   # one block of 16 warps per SM
     ("awq_reduce.cu", r"k_losses", 64, 0),
 ]
 
