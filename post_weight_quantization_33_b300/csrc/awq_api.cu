@@ -278,8 +278,7 @@ awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stre
   // K 64-bit sums, then the status word of the bounded waits.
   AWQ_CUDA(pool_alloc(&ws, sizeof(unsigned long long) * (K + 1), s), "scratch allocation");
   auto* acc = static_cast<unsigned long long*>(ws);
-  int* status = reinterpret_cast<int*>(acc + K);
-  AWQ_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s), "status reset");
+  int* status = reinterpret_cast<int*>(acc + K);   // zeroed with the sums
   AWQ_CUDA(launch_stats_accumulate(static_cast<const __half*>(X), T, K, acc, status, s),
            "stats kernel");
   AWQ_CUDA(launch_stats_finalize(acc, T, K, sX, status, s), "stats finalize kernel");
@@ -515,7 +514,8 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
   Carver wc;
   const size_t o_acc = wc.take<unsigned long long>(K);
   const size_t o_sx = wc.take<double>(K);
-  const size_t o_rng = wc.take<unsigned long long>(3);   // scale range [2], loss counter
+  // scale range [2], loss counter, the error GEMM's tile counter
+  const size_t o_rng = wc.take<unsigned long long>(4);
   const size_t o_r = wc.take<float>(int64_t(G) * K);
   const size_t o_d = wc.take<__half>(int64_t(G) * n_pad * K);
   const size_t o_pt = wc.take<float>(int64_t(G) * n_tiles * n_pad);
@@ -559,6 +559,7 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
   auto* gmx = reinterpret_cast<unsigned int*>(wb + o_gmx);
   auto* rsc = reinterpret_cast<double*>(wb + o_rsc);
   auto* counter = reinterpret_cast<unsigned int*>(range + 2);
+  auto* tile_counter = reinterpret_cast<unsigned int*>(range + 3);
   const __half* Xh = static_cast<const __half*>(X);
 
   AWQ_CUDA(cudaMemsetAsync(r->status, 0, sizeof(int), s), "status reset");
@@ -620,10 +621,11 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
     AWQ_CUDA(launch_gram_prepare(Xh, T, K, xt, Tp, g32, gmx, gs, rsc, r->status, s,
                                  &r->launches),
              "Gram matrix");
-    AWQ_CUDA(launch_gemm_error_gram(delta, gs, K, n_pad, G, partials, r->status, s),
+    AWQ_CUDA(launch_gemm_error_gram(delta, gs, K, n_pad, G, partials, r->status, tile_counter, s),
              "error GEMM (Gram form)");
   } else {
-    AWQ_CUDA(launch_gemm_error(delta, Xh, T, K, n_pad, G, partials, r->status, s), "error GEMM");
+    AWQ_CUDA(launch_gemm_error(delta, Xh, T, K, n_pad, G, partials, r->status, tile_counter, s),
+             "error GEMM");
   }
   r->launches += 1;
   AWQ_CUDA(mark(AWQ_STAGE_LOSS), "event record");

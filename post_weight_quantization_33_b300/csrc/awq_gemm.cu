@@ -253,6 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warps 0-3 (both)    epilogue as in k_gemm, then one arrival per thread on
 //                       the even CTA's `tempty` (256 arrivals free it).
 //
+// Tile scheduling: the even CTA's producer takes the pair's next tile from a
+// global counter (atomicAdd), so the tiles in progress on all pairs at any
+// time are about 74 consecutive ones of the tile order, however much pairs
+// drift apart over a long launch (with a fixed assignment, pair p taking
+// tiles p, p + 74, ..., the pairs drift, and the L2 reuse the tile order is
+// built for fades on the large workloads).  The id is published into a ring
+// of kTileIdSlots slots in both CTAs' shared memory (tid_full); its readers
+// -- the even CTA's MMA thread and epilogue warps, the odd CTA's producer and
+// epilogue warps -- release the slot on the even CTA's tid_empty.  Id -1 ends
+// the sequence.
+//
 // Teardown: each producer waits until every stage it filled was released
 // (so no MMA still reads its shared memory and no commit still targets its
 // barriers), then both CTAs meet at a cluster barrier before TMEM is freed and
@@ -264,10 +275,16 @@ constexpr uint32_t PA_BYTES = PM * BK * 2;        // 16 KB
 constexpr uint32_t PB_BYTES = (PN / 2) * BK * 2;  // 16 KB (this CTA's half of the tokens)
 constexpr uint32_t P_OFF_A = 0;
 constexpr uint32_t P_OFF_B = P_OFF_A + PSTAGES * PA_BYTES;
+constexpr int kTileIdSlots = 4;
+// Readers of a published tile id: the even CTA's MMA thread and 4 epilogue
+// warps, the odd CTA's producer and 4 epilogue warps.
+constexpr uint32_t kTileIdReaders = 1 + kEpilogueWarps + 1 + kEpilogueWarps;
 constexpr uint32_t P_OFF_BAR = P_OFF_B + PSTAGES * PB_BYTES;
-constexpr uint32_t P_NUM_BARS = 2 * PSTAGES + 5;   // full, empty, tfull x2, tempty x2, drain
+// full, empty, tfull x2, tempty x2, drain, tid_full, tid_empty
+constexpr uint32_t P_NUM_BARS = 2 * PSTAGES + 5 + 2 * kTileIdSlots;
 constexpr uint32_t P_OFF_MISC = P_OFF_BAR + P_NUM_BARS * 8;
-constexpr uint32_t P_SMEM_BYTES = P_OFF_MISC + 16 + 1024;
+constexpr uint32_t P_OFF_TID = P_OFF_MISC + 16;   // tile id ring (int per slot)
+constexpr uint32_t P_SMEM_BYTES = P_OFF_TID + 4 * kTileIdSlots + 1024;
 static_assert(P_SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(P_OFF_B % 1024 == 0 && PA_BYTES % 1024 == 0 && PB_BYTES % 1024 == 0,
               "swizzle atoms");
@@ -285,6 +302,7 @@ struct PairArgs {
   const __half* delta;   // Gram form: the residual [alpha][n_pad][K] (the epilogue's weights)
   int64_t K;             // Gram form: channels (columns of Gs and of delta)
   int group_rows;        // tile order: row tiles per group (see pair_group_rows)
+  unsigned int* tile_counter;   // next tile to hand out (zeroed before the launch)
 };
 
 // kGram: the B operand is Gs (K x K) instead of X, and the epilogue forms
@@ -302,14 +320,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bar_empty + 8 * PSTAGES;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_tid_full = bar_drain + 8;
+  const uint32_t bar_tid_empty = bar_tid_full + 8 * kTileIdSlots;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P_OFF_MISC + 4);
+  volatile int* tile_ids = reinterpret_cast<volatile int*>(smem + P_OFF_TID);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
-  const int pair = static_cast<int>(blockIdx.x >> 1);
-  const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PSTAGES; ++s) {
@@ -321,6 +340,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty + 8 * a, 2 * kEpilogueThreads);
     }
     mbar_init(bar_drain, 1);
+    for (int s = 0; s < kTileIdSlots; ++s) {
+      mbar_init(bar_tid_full + 8 * s, 1);
+      mbar_init(bar_tid_empty + 8 * s, kTileIdReaders);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -355,13 +378,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     nt = r2 / rows;
     mp = g * p.group_rows + (r2 - nt * rows);
   };
+  // The pair's i-th tile id (ring slot i % kTileIdSlots): published by the
+  // even CTA's producer, read here by every other role.  A reader releases
+  // the slot on the even CTA's tid_empty (one arrival per reading thread or
+  // warp).  Returns -1 at the end of the sequence, -2 if the wait gave up.
+  auto read_tile = [&](int i, bool arrive) -> int {
+    const int slot = i % kTileIdSlots;
+    if (!mbar_wait_cluster_bounded(bar_tid_full + 8 * slot,
+                                   static_cast<uint32_t>((i / kTileIdSlots) & 1), abort_flag,
+                                   p.status, kDevTimeoutTileId))
+      return -2;
+    const int t = tile_ids[slot];
+    if (arrive) mbar_arrive_cluster(map_shared(bar_tid_empty + 8 * slot, 0));
+    return t;
+  };
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int tile = pair; tile < total_tiles && ok; tile += num_pairs) {
+      for (int i = 0; ok; ++i) {
+        int tile;
+        if (leader) {
+          // Take the next tile and publish it to both CTAs once the slot's
+          // previous id has been read by all of its readers.
+          const int slot = i % kTileIdSlots;
+          if (i >= kTileIdSlots &&
+              !mbar_wait_cluster_bounded(bar_tid_empty + 8 * slot,
+                                         static_cast<uint32_t>((i / kTileIdSlots - 1) & 1),
+                                         abort_flag, p.status, kDevTimeoutTileId)) {
+            ok = false;
+            break;
+          }
+          tile = static_cast<int>(atomicAdd(p.tile_counter, 1u));
+          if (tile >= total_tiles) tile = -1;
+          const uint32_t id_addr = sbase + P_OFF_TID + 4 * slot;
+          tile_ids[slot] = tile;
+          st_shared_cluster_u32(map_shared(id_addr, 1), static_cast<uint32_t>(tile));
+          mbar_arrive_cluster(bar_tid_full + 8 * slot);                    // own CTA
+          mbar_arrive_cluster(map_shared(bar_tid_full + 8 * slot, 1));     // the odd CTA
+        } else {
+          tile = read_tile(i, true);
+          if (tile == -2) ok = false;
+        }
+        if (tile < 0) break;
         int a, nt, mp;
         decode(tile, a, nt, mp);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -399,8 +460,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (leader && lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true, issued = false;
-      int it = 0;
-      for (int tile = pair; tile < total_tiles && ok; tile += num_pairs, ++it) {
+      for (int it = 0; ok; ++it) {
+        const int tile = read_tile(it, true);
+        if (tile == -2) ok = false;
+        if (tile < 0) break;
         const uint32_t acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait_bounded(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status,
@@ -444,8 +507,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp;               // TMEM lane quarter (warps 0-3)
     const int row = q * 32 + lane;    // row within this CTA's 128
     const uint32_t tempty_leader = map_shared(bar_tempty, 0);
-    int it = 0;
-    for (int tile = pair; tile < total_tiles; tile += num_pairs, ++it) {
+    for (int it = 0;; ++it) {
+      const int tile = read_tile(it, false);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_shared(bar_tid_empty + 8 * (it % kTileIdSlots), 0));
+      if (__any_sync(0xFFFFFFFFu, tile < 0)) break;
       int a, nt, mp;
       decode(tile, a, nt, mp);
       const uint32_t acc = it & 1;
@@ -595,6 +661,9 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Pair
   if (e != cudaSuccess) return e;
   const int clusters = std::min(device_sm_count() / 2, max_clusters);
   const int pairs = static_cast<int>(std::min<int64_t>(clusters, tiles));
+  if (a.tile_counter == nullptr) return cudaErrorInvalidValue;
+  e = cudaMemsetAsync(a.tile_counter, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
   k_gemm_err_pair<kGram><<<2 * pairs, kThreads, P_SMEM_BYTES, st>>>(ta, tb, a);
   return cudaGetLastError();
 }
@@ -631,7 +700,7 @@ static int pair_group_rows(int64_t b_rows, int64_t K, int num_mp) {
 
 cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
                               int64_t n_pad, int n_alpha, float* partials, int* status,
-                              cudaStream_t st) {
+                              unsigned int* tile_counter, cudaStream_t st) {
   if (n_pad % (2 * PM) != 0) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_residual_tmap(&ta, delta, K, n_pad, n_alpha)) return cudaErrorInvalidValue;
@@ -647,12 +716,13 @@ cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, i
   a.partials = partials;
   a.status = status;
   a.group_rows = pair_group_rows(T, K, a.num_mp);
+  a.tile_counter = tile_counter;
   return launch_pair<false>(ta, tb, a, st);
 }
 
 cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_t K,
                                    int64_t n_pad, int n_alpha, float* partials, int* status,
-                                   cudaStream_t st) {
+                                   unsigned int* tile_counter, cudaStream_t st) {
   if (n_pad % (2 * PM) != 0 || K % BK != 0) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_residual_tmap(&ta, delta, K, n_pad, n_alpha)) return cudaErrorInvalidValue;
@@ -669,6 +739,7 @@ cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_
   a.delta = delta;
   a.K = K;
   a.group_rows = pair_group_rows(K, K, a.num_mp);
+  a.tile_counter = tile_counter;
   return launch_pair<true>(ta, tb, a, st);
 }
 

@@ -20,6 +20,7 @@ enum DeviceError : int {
   kDevTimeoutDrain = 6,     // in-flight copies/MMAs did not finish on abort
   kDevTimeoutSelfTest = 7,  // the self-test wait expired (expected there)
   kDevNonFinite = 8,        // a grid point's loss is not finite: X or W holds inf/NaN
+  kDevTimeoutTileId = 9,    // a tile id was never published, or its slot never released
 };
 
 constexpr int kMaxWeights = 16;
@@ -47,8 +48,9 @@ struct RowMap {
 // 2^62, and the top two bits flag channels that held an infinity or a NaN.
 constexpr int64_t kMaxStatTokens = int64_t(1) << 22;
 // acc: K 64-bit words of scratch (zeroed here, on the stream); status: a
-// device int (zeroed by the caller) that receives a code if a bounded wait
-// expired, nullable.
+// device int that receives a code if a bounded wait expired, nullable.  If
+// status is the word right after the sums (acc + K) it is zeroed here with
+// them; otherwise the caller zeroes it.
 cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
                                     unsigned long long* acc, int* status, cudaStream_t st);
 // range (nullable, 2 words zeroed by the caller): also the range of
@@ -91,9 +93,11 @@ cudaError_t launch_gemm_reference(const __half* W, int64_t N, const __half* X, i
 // partials[a][n_tile][n_pad] = sum over the tile's tokens of (delta[a] X^T)^2
 // for every grid point a (delta: fp16 [n_alpha][n_pad][K], n_pad a multiple
 // of kPairRows).
+// tile_counter: one device word of scratch (the launch zeroes it) from which
+// the CTA pairs take their tiles.
 cudaError_t launch_gemm_error(const __half* delta, const __half* X, int64_t T, int64_t K,
                               int64_t n_pad, int n_alpha, float* partials, int* status,
-                              cudaStream_t st);
+                              unsigned int* tile_counter, cudaStream_t st);
 // Self-test of the bounded wait: one CTA waits on an mbarrier nothing
 // arrives at; *status receives kDevTimeoutSelfTest after ~limit_ns.
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, int* status, cudaStream_t st);
@@ -114,6 +118,7 @@ cudaError_t launch_gram_prepare(const __half* X, int64_t T, int64_t K, __half* X
 // (delta[a] Gs)[n][j] * delta[a][n][j] (Gs fp16 [K][K], symmetric).
 cudaError_t launch_gemm_error_gram(const __half* delta, const __half* Gs, int64_t K,
                                    int64_t n_pad, int n_alpha, float* partials, int* status,
+                                   unsigned int* tile_counter,
                                    cudaStream_t st);
 
 // ---- decode product (awq_matvec.cu)

@@ -154,26 +154,50 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   // Codes of a unit: streamed from HBM, kPrefetch units ahead.  The group
   // parameters (3 bytes per row and group) are read when the unit is used:
   // a row's 32-byte sector of zeros or scales serves 16 to 32 groups, so they
-  // come from L1 after the row's first unit.
-  auto load_unit = [&](int64_t item, UnitRow& r0, UnitRow& r1) {
-    const int64_t tile = item / upr, unit = item - tile * upr;
+  // come from L1 after the row's first unit.  Items advance as (tile, unit)
+  // cursors: no division inside the loop.
+  auto load_unit = [&](int64_t tile, int64_t unit, UnitRow& r0, UnitRow& r1) {
     const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
     load_fields<BITS>(codes + l0 * words_per_row, unit, c, r0.lo, r0.hi);
     load_fields<BITS>(codes + l1 * words_per_row, unit, c, r1.lo, r1.hi);
   };
+  auto advance = [&](int64_t& tile, int64_t& unit) {
+    if (++unit == upr) {
+      unit = 0;
+      ++tile;
+    }
+  };
+  int64_t ctile = i0 / upr, cunit = i0 - ctile * upr;   // the item being computed
+  int64_t ptile = ctile, punit = cunit;                 // the next item to load
 
   UnitRow q0[kPrefetch], q1[kPrefetch];
 #pragma unroll
   for (int p = 0; p < kPrefetch; ++p)
-    if (i0 + p < i1) load_unit(i0 + p, q0[p], q1[p]);
+    if (i0 + p < i1) {
+      load_unit(ptile, punit, q0[p], q1[p]);
+      advance(ptile, punit);
+    }
 
   float acc[NT][4], part[NT][4];
 #pragma unroll
   for (int t = 0; t < NT; ++t)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
-  int64_t cur_tile = i0 < i1 ? i0 / upr : -1;
+  int64_t cur_tile = i0 < i1 ? ctile : -1;
   int64_t tile_first = i0;   // first item of the current tile inside this range
+  // Group parameters of the current tile's two rows.
+  const uint8_t* zr0 = zeros;
+  const uint8_t* zr1 = zeros;
+  const __half* sr0 = scales;
+  const __half* sr1 = scales;
+  auto set_rows = [&](int64_t tile) {
+    const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+    zr0 = zeros + l0 * groups;
+    zr1 = zeros + l1 * groups;
+    sr0 = scales + l0 * groups;
+    sr1 = scales + l1 * groups;
+  };
+  if (i0 < i1) set_rows(ctile);
   float last_sf0 = 0.f, last_sf1 = 0.f;   // group scales of the last unit done
 
   // Close the current tile: scale the group the range leaves open (per-row
@@ -228,24 +252,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     for (int p = 0; p < kPrefetch; ++p) {
       const int64_t it = base + p;
       if (it >= i1) break;
-      const int64_t tile = it / upr, unit = it - tile * upr;
+      const int64_t tile = ctile, unit = cunit;
       if (tile != cur_tile) {
         finish_tile(cur_tile, tile_first, it);
         cur_tile = tile;
         tile_first = it;
+        set_rows(tile);
       }
       const UnitRow a0 = q0[p], a1 = q1[p];
-      if (it + kPrefetch < i1) load_unit(it + kPrefetch, q0[p], q1[p]);
+      if (it + kPrefetch < i1) {
+        load_unit(ptile, punit, q0[p], q1[p]);
+        advance(ptile, punit);
+      }
+      advance(ctile, cunit);
       const int64_t k0 = unit * kUnit;
       int64_t grp = 0;
-      if constexpr (GROUP != 0) grp = unit / kUnitsPerGroup;
-      const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+      if constexpr (GROUP == 128) grp = unit >> 1;
+      if constexpr (GROUP == 64) grp = unit;
       // 1024 + zero in both halves (exact: fp16 bits 0x6400 + z), and the scale.
-      const uint32_t z0 = 0x6400u + __ldg(zeros + l0 * groups + grp);
-      const uint32_t z1 = 0x6400u + __ldg(zeros + l1 * groups + grp);
+      const uint32_t z0 = 0x6400u + __ldg(zr0 + grp);
+      const uint32_t z1 = 0x6400u + __ldg(zr1 + grp);
       const uint32_t zp0 = z0 | (z0 << 16), zp1 = z1 | (z1 << 16);
-      const float sf0 = __half2float(__ldg(scales + l0 * groups + grp));
-      const float sf1 = __half2float(__ldg(scales + l1 * groups + grp));
+      const float sf0 = __half2float(__ldg(sr0 + grp));
+      const float sf1 = __half2float(__ldg(sr1 + grp));
       uint32_t X[NT][8];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
@@ -286,7 +315,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
       last_sf1 = sf1;
       // End of a group: scale it into the row's sum (per-row groups are
       // scaled when their tile closes).
-      if (GROUP != 0 && (unit + 1) % kUnitsPerGroup == 0) {
+      if (GROUP == 64 || (GROUP == 128 && (unit & 1))) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);

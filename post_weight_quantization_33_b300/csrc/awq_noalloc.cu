@@ -24,8 +24,8 @@ namespace {
 
 constexpr int64_t kNoAllocMaxK = AWQ_STATS_NOALLOC_MAX_K;
 
-// Per-channel 64-bit sums of |x| in units of 2^-24 (see awq_stats.cu), then
-// one more word whose low half is the status of the kernel's bounded waits.
+// Per-channel 64-bit sums of |x| in units of 2^-24 (see awq_stats.cu); the
+// word after a call's K sums holds the status of its bounded waits.
 static __device__ __align__(256) unsigned long long g_stats_scratch[kNoAllocMaxK + 1];
 
 typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
@@ -112,11 +112,10 @@ extern "C" __attribute__((visibility("default"))) awq_status awq_stats_noalloc(
   cudaError_t e = scratch_for_current_context(&acc);
   if (e != cudaSuccess) return awq_internal_cuda_fail(e, "scratch address lookup");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* status = reinterpret_cast<int*>(acc + kNoAllocMaxK);
-  // The array keeps the last call's contents: the status word is cleared
-  // here and launch_stats_accumulate clears acc[0..K), both on the stream.
-  e = cudaMemsetAsync(status, 0, sizeof(int), s);
-  if (e != cudaSuccess) return awq_internal_cuda_fail(e, "status reset");
+  // The status word of this call follows its K sums.  The array keeps the
+  // last call's contents: launch_stats_accumulate clears acc[0..K] (sums and
+  // status) on the stream before accumulating.
+  int* status = reinterpret_cast<int*>(acc + K);
   e = awq::launch_stats_accumulate(static_cast<const __half*>(X), T, K, acc, status, s);
   if (e != cudaSuccess) return awq_internal_cuda_fail(e, "stats kernel");
   e = awq::launch_stats_finalize(acc, T, K, sX, status, s);

@@ -198,7 +198,12 @@ __global__ void __launch_bounds__(kStatThreads)
     if (lane != 0) return;
     prefetch_tmap(&tmap);
     int64_t issued = 0;
-    for (int64_t u = u0; u < u1; ++u, ++issued) {
+    int64_t slab = u0 / tboxes, tb = u0 - slab * tboxes;
+    for (int64_t u = u0; u < u1; ++u, ++issued, ++tb) {
+      if (tb == tboxes) {
+        tb = 0;
+        ++slab;
+      }
       const int st = static_cast<int>(issued % kStatStages);
       if (issued >= kStatStages &&
           !mbar_wait_bounded(sm.empty0 + 8 * st,
@@ -206,7 +211,6 @@ __global__ void __launch_bounds__(kStatThreads)
                              sm.abort_flag, status, kDevTimeoutEmpty))
         break;
       mbar_arrive_expect_tx(sm.full0 + 8 * st, kBoxBytes);
-      const int64_t slab = u / tboxes, tb = u - slab * tboxes;
       tma_load_2d(smem_u32(ring + st * kBoxBytes), &tmap, sm.full0 + 8 * st,
                   static_cast<int>(slab * kSlab), static_cast<int>(tb * kBoxTokens));
     }
@@ -227,20 +231,23 @@ __global__ void __launch_bounds__(kStatThreads)
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) a.hi[i] = a.lo[i] = 0ull;
+  // The unit's slab and token box, advanced without dividing (one division
+  // at the start).
   int64_t cur_slab = u0 < u1 ? u0 / tboxes : 0;
+  int64_t tb = u0 - cur_slab * tboxes;
   uint32_t round = 0;
   int in_window = 0;
-  for (int64_t u = u0, i = 0; u < u1; ++u, ++i) {
-    const int64_t slab = u / tboxes;
-    if (slab != cur_slab) {
+  int st = 0;
+  uint32_t phase = 0;
+  for (int64_t u = u0; u < u1; ++u, ++tb) {
+    if (tb == tboxes) {   // next slab
+      tb = 0;
       flush_window(a);
       in_window = 0;
       if (!flush_slab(a, cur_slab, kchunks, round++, sm, status, acc)) return;
-      cur_slab = slab;
+      ++cur_slab;
     }
-    const int st = static_cast<int>(i % kStatStages);
-    if (!mbar_wait_bounded(sm.full0 + 8 * st, static_cast<uint32_t>((i / kStatStages) & 1),
-                           sm.abort_flag, status, kDevTimeoutFull))
+    if (!mbar_wait_bounded(sm.full0 + 8 * st, phase, sm.abort_flag, status, kDevTimeoutFull))
       return;
     const uint4* box = reinterpret_cast<const uint4*>(ring + st * kBoxBytes);
 #pragma unroll
@@ -248,6 +255,10 @@ __global__ void __launch_bounds__(kStatThreads)
       add_chunk(a, box[(warp + kStatWarps * q) * 32 + lane]);
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.empty0 + 8 * st);
+    if (++st == kStatStages) {
+      st = 0;
+      phase ^= 1u;
+    }
     if (++in_window == kFlushBoxes) {
       flush_window(a);
       in_window = 0;
@@ -370,7 +381,10 @@ cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
   // One wave of resident blocks (each with a 64 KB ring), or fewer for small inputs.
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>(units, static_cast<int64_t>(lf.per_sm) * lf.sms));
-  e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long) * K, st);
+  // The sums, and the status word when it directly follows them, in one
+  // memset.
+  const bool status_next = status == reinterpret_cast<int*>(acc + K);
+  e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long) * (K + (status_next ? 1 : 0)), st);
   if (e != cudaSuccess) return e;
   k_stats_accumulate<<<static_cast<unsigned>(grid), kStatThreads, kStatSmem, st>>>(
       tmap, kchunks, tboxes, units, acc, status);
