@@ -85,15 +85,13 @@ struct UnitRow {
 };
 
 template <int BITS>
-__device__ __forceinline__ void load_fields(const uint32_t* row, int64_t unit, int c,
-                                            uint32_t& lo, uint32_t& hi) {
-  if (BITS == 4) {   // words 2c, 2c+1 of the unit's 8
-    const uint2 v = ld_stream_u64(row + unit * 8 + 2 * c);
+__device__ __forceinline__ void load_fields(const uint32_t* p, int c, uint32_t& lo, uint32_t& hi) {
+  if (BITS == 4) {   // words 2c, 2c+1 of the unit (p points at word 2c)
+    const uint2 v = ld_stream_u64(p);
     lo = v.x;
     hi = v.y;
-  } else {           // bits [48c, 48c+48) of the unit's 6 words
-    const uint32_t* u = row + unit * 6 + (3 * c) / 2;
-    const uint32_t w0 = ld_stream_u32(u), w1 = ld_stream_u32(u + 1);
+  } else {           // bits [48c, 48c+48) of the unit's 6 words (p at word 3c/2)
+    const uint32_t w0 = ld_stream_u32(p), w1 = ld_stream_u32(p + 1);
     if (c & 1) {
       lo = __funnelshift_r(w0, w1, 16) & 0xFFFFFFu;
       hi = w1 >> 8;
@@ -124,7 +122,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int64_t upr = K / kUnit;
+  const int upr = static_cast<int>(K / kUnit);          // units per row tile
   const int64_t tiles = (N + 15) / 16;
   const int64_t items = tiles * upr;
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
@@ -133,7 +131,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   const int64_t i1 = b0 + (b1 - b0) * (warp + 1) / nwarps;
   const int64_t words_per_row = K * BITS / 32;
   const int64_t groups = GROUP ? K / GROUP : 1;
-  constexpr int kUnitsPerGroup = GROUP ? GROUP / kUnit : 1;
+  constexpr int kUnitWords = BITS == 4 ? 8 : 6;          // code words per row and unit
   // Units of codes in flight per warp (fewer with 16 tokens: more registers
   // per unit).
   constexpr int kPrefetch = NT == 1 ? 8 : 5;
@@ -150,207 +148,218 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     part_tile[warp][1] = -1;
   }
   __syncthreads();
-
-  // Codes of a unit: streamed from HBM, kPrefetch units ahead.  The group
-  // parameters (3 bytes per row and group) are read when the unit is used:
-  // a row's 32-byte sector of zeros or scales serves 16 to 32 groups, so they
-  // come from L1 after the row's first unit.  Items advance as (tile, unit)
-  // cursors: no division inside the loop.
-  auto load_unit = [&](int64_t tile, int64_t unit, UnitRow& r0, UnitRow& r1) {
-    const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
-    load_fields<BITS>(codes + l0 * words_per_row, unit, c, r0.lo, r0.hi);
-    load_fields<BITS>(codes + l1 * words_per_row, unit, c, r1.lo, r1.hi);
-  };
-  auto advance = [&](int64_t& tile, int64_t& unit) {
-    if (++unit == upr) {
-      unit = 0;
-      ++tile;
-    }
-  };
-  int64_t ctile = i0 / upr, cunit = i0 - ctile * upr;   // the item being computed
-  int64_t ptile = ctile, punit = cunit;                 // the next item to load
-
-  UnitRow q0[kPrefetch], q1[kPrefetch];
-#pragma unroll
-  for (int p = 0; p < kPrefetch; ++p)
-    if (i0 + p < i1) {
-      load_unit(ptile, punit, q0[p], q1[p]);
-      advance(ptile, punit);
-    }
-
-  float acc[NT][4], part[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
-  int64_t cur_tile = i0 < i1 ? ctile : -1;
-  int64_t tile_first = i0;   // first item of the current tile inside this range
-  // Group parameters of the current tile's two rows.
-  const uint8_t* zr0 = zeros;
-  const uint8_t* zr1 = zeros;
-  const __half* sr0 = scales;
-  const __half* sr1 = scales;
-  auto set_rows = [&](int64_t tile) {
-    const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
-    zr0 = zeros + l0 * groups;
-    zr1 = zeros + l1 * groups;
-    sr0 = scales + l0 * groups;
-    sr1 = scales + l1 * groups;
-  };
-  if (i0 < i1) set_rows(ctile);
-  float last_sf0 = 0.f, last_sf1 = 0.f;   // group scales of the last unit done
-
-  // Close the current tile: scale the group the range leaves open (per-row
-  // groups: always), then add the tile to y if it lies entirely inside this
-  // warp's range, else park it in shared memory for the block's sum.
-  auto finish_tile = [&](int64_t tile, int64_t first, int64_t end) {
-    if (GROUP == 0 || (end - tile * upr) % kUnitsPerGroup != 0) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        acc[t][0] = __fmaf_rn(last_sf0, part[t][0], acc[t][0]);
-        acc[t][1] = __fmaf_rn(last_sf0, part[t][1], acc[t][1]);
-        acc[t][2] = __fmaf_rn(last_sf1, part[t][2], acc[t][2]);
-        acc[t][3] = __fmaf_rn(last_sf1, part[t][3], acc[t][3]);
+  if (i0 >= i1) goto combine;
+  {
+    // The first code word this thread reads in a row: INT4 words 2c, 2c+1 of
+    // a unit; INT3 bits [48c, 48c+48) of its 6 words.
+    const int cw = BITS == 4 ? 2 * c : (3 * c) / 2;
+    // Stream of units to load (kPrefetch ahead): tile and unit, and the two
+    // rows' code pointers at that unit.  Advanced by pointer increments; a
+    // new tile (every upr units) recomputes them.
+    int64_t ptile = i0 / upr;
+    int punit = static_cast<int>(i0 - ptile * upr);
+    const uint32_t* pc0;
+    const uint32_t* pc1;
+    auto set_load_rows = [&]() {
+      const int64_t l0 = min(ptile * 16 + g, N - 1), l1 = min(ptile * 16 + g + 8, N - 1);
+      pc0 = codes + l0 * words_per_row + static_cast<int64_t>(punit) * kUnitWords + cw;
+      pc1 = codes + l1 * words_per_row + static_cast<int64_t>(punit) * kUnitWords + cw;
+    };
+    set_load_rows();
+    auto load_next = [&](UnitRow& r0, UnitRow& r1) {
+      load_fields<BITS>(pc0, c, r0.lo, r0.hi);
+      load_fields<BITS>(pc1, c, r1.lo, r1.hi);
+      pc0 += kUnitWords;
+      pc1 += kUnitWords;
+      if (++punit == upr) {
+        punit = 0;
+        ++ptile;
+        set_load_rows();
       }
-    }
-    const bool whole = first == tile * upr && end == (tile + 1) * upr;
-    if (whole) {
-      const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+    };
+    const int n = static_cast<int>(i1 - i0);   // units of this warp
+    UnitRow q0[kPrefetch], q1[kPrefetch];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int m0 = t * 8 + 2 * c;
-        if (r0 < N) {
-          if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
-          if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
-        }
-        if (r1 < N) {
-          if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
-          if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
-        }
-      }
-    } else {
-      const int slot = first == i0 ? 0 : 1;   // the range's first or last tile
-      float* ps = part_smem[warp][slot];
+    for (int p = 0; p < kPrefetch; ++p)
+      if (p < n) load_next(q0[p], q1[p]);
+
+    // The unit being computed: its tile, its index in the tile, and the
+    // tile's group parameters and x rows.
+    int64_t tile = i0 / upr;
+    int unit = static_cast<int>(i0 - tile * upr);
+    int tile_u0 = unit;   // first unit of the current tile inside this range
+    const uint8_t* zr0;
+    const uint8_t* zr1;
+    const __half* sr0;
+    const __half* sr1;
+    auto set_rows = [&]() {
+      const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+      zr0 = zeros + l0 * groups;
+      zr1 = zeros + l1 * groups;
+      sr0 = scales + l0 * groups;
+      sr1 = scales + l1 * groups;
+    };
+    set_rows();
+    // x of this thread's tokens (t * 8 + g): 16-byte chunks 2c + 8 unit and
+    // the next, swizzled by (token & 7) = g in shared memory.
+    const uint4* xrow[NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int m0 = t * 8 + 2 * c;
-        ps[g * 16 + m0] = acc[t][0];
-        ps[g * 16 + m0 + 1] = acc[t][1];
-        ps[(g + 8) * 16 + m0] = acc[t][2];
-        ps[(g + 8) * 16 + m0 + 1] = acc[t][3];
-      }
-      if (lane == 0) part_tile[warp][slot] = tile;
+    for (int t = 0; t < NT; ++t) {
+      const int tok = t * 8 + g;
+      if constexpr (XSMEM) xrow[t] = xs + static_cast<int64_t>(min(tok, M - 1)) * (K / 8);
+      else xrow[t] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(min(tok, M - 1)) * K);
     }
+
+    float acc[NT][4], part[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
-  };
+    float last_sf0 = 0.f, last_sf1 = 0.f;   // group scales of the last unit done
 
-  for (int64_t base = i0; base < i1; base += kPrefetch) {
+    // Close the current tile at unit `end`: scale the group the range leaves
+    // open (per-row groups: always), then add the tile to y if this warp did
+    // all of it, else park it in shared memory for the block's sum.
+    auto finish_tile = [&](int end) {
+      if (GROUP == 0 || (GROUP == 128 && (end & 1))) {
 #pragma unroll
-    for (int p = 0; p < kPrefetch; ++p) {
-      const int64_t it = base + p;
-      if (it >= i1) break;
-      const int64_t tile = ctile, unit = cunit;
-      if (tile != cur_tile) {
-        finish_tile(cur_tile, tile_first, it);
-        cur_tile = tile;
-        tile_first = it;
-        set_rows(tile);
+        for (int t = 0; t < NT; ++t) {
+          acc[t][0] = __fmaf_rn(last_sf0, part[t][0], acc[t][0]);
+          acc[t][1] = __fmaf_rn(last_sf0, part[t][1], acc[t][1]);
+          acc[t][2] = __fmaf_rn(last_sf1, part[t][2], acc[t][2]);
+          acc[t][3] = __fmaf_rn(last_sf1, part[t][3], acc[t][3]);
+        }
       }
-      const UnitRow a0 = q0[p], a1 = q1[p];
-      if (it + kPrefetch < i1) {
-        load_unit(ptile, punit, q0[p], q1[p]);
-        advance(ptile, punit);
-      }
-      advance(ctile, cunit);
-      const int64_t k0 = unit * kUnit;
-      int64_t grp = 0;
-      if constexpr (GROUP == 128) grp = unit >> 1;
-      if constexpr (GROUP == 64) grp = unit;
-      // 1024 + zero in both halves (exact: fp16 bits 0x6400 + z), and the scale.
-      const uint32_t z0 = 0x6400u + __ldg(zr0 + grp);
-      const uint32_t z1 = 0x6400u + __ldg(zr1 + grp);
-      const uint32_t zp0 = z0 | (z0 << 16), zp1 = z1 | (z1 << 16);
-      const float sf0 = __half2float(__ldg(sr0 + grp));
-      const float sf1 = __half2float(__ldg(sr1 + grp));
-      uint32_t X[NT][8];
+      if (tile_u0 == 0 && end == upr) {
+        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int tok = t * 8 + g;
-        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-        if (tok < M) {
-          if constexpr (XSMEM) {
-            const int64_t j = (k0 + 16 * c) / 8;
-            const uint4* xrow = xs + static_cast<int64_t>(tok) * (K / 8);
-            v0 = xrow[j ^ (tok & 7)];
-            v1 = xrow[(j + 1) ^ (tok & 7)];
-          } else {
-            const uint4* xp = reinterpret_cast<const uint4*>(x + tok * K + k0 + 16 * c);
-            v0 = __ldg(xp);
-            v1 = __ldg(xp + 1);
+        for (int t = 0; t < NT; ++t) {
+          const int m0 = t * 8 + 2 * c;
+          if (r0 < N) {
+            if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
+            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
+          }
+          if (r1 < N) {
+            if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
+            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
           }
         }
-        X[t][0] = v0.x; X[t][1] = v0.y; X[t][2] = v0.z; X[t][3] = v0.w;
-        X[t][4] = v1.x; X[t][5] = v1.y; X[t][6] = v1.z; X[t][7] = v1.w;
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t a[4];
-        a[0] = hsub2_u32(code_pair<BITS>(a0.lo, j), zp0);   // row g,   slots 2c, 2c+1
-        a[1] = hsub2_u32(code_pair<BITS>(a1.lo, j), zp1);   // row g+8
-        a[2] = hsub2_u32(code_pair<BITS>(a0.hi, j), zp0);   // row g,   slots 2c+8, 2c+9
-        a[3] = hsub2_u32(code_pair<BITS>(a1.hi, j), zp1);   // row g+8
-        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+      } else {
+        const int slot = tile == i0 / upr ? 0 : 1;   // the range's first or last tile
+        float* ps = part_smem[warp][slot];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          // x[16c + j], x[16c + j + 4]  and  x[16c + 8 + j], x[16c + 12 + j]
-          const uint32_t bb0 = __byte_perm(X[t][j >> 1], X[t][(j >> 1) + 2], sel);
-          const uint32_t bb1 = __byte_perm(X[t][4 + (j >> 1)], X[t][6 + (j >> 1)], sel);
-          mma_16816(part[t], a, bb0, bb1);
+          const int m0 = t * 8 + 2 * c;
+          ps[g * 16 + m0] = acc[t][0];
+          ps[g * 16 + m0 + 1] = acc[t][1];
+          ps[(g + 8) * 16 + m0] = acc[t][2];
+          ps[(g + 8) * 16 + m0 + 1] = acc[t][3];
         }
+        if (lane == 0) part_tile[warp][slot] = tile;
       }
-      last_sf0 = sf0;
-      last_sf1 = sf1;
-      // End of a group: scale it into the row's sum (per-row groups are
-      // scaled when their tile closes).
-      if (GROUP == 64 || (GROUP == 128 && (unit & 1))) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
+    };
+
+    for (int base = 0; base < n; base += kPrefetch) {
+#pragma unroll
+      for (int p = 0; p < kPrefetch; ++p) {
+        if (base + p >= n) break;
+        if (unit == upr) {   // the previous unit ended a tile
+          finish_tile(upr);
+          ++tile;
+          unit = 0;
+          tile_u0 = 0;
+          set_rows();
+        }
+        const UnitRow a0 = q0[p], a1 = q1[p];
+        if (base + p + kPrefetch < n) load_next(q0[p], q1[p]);
+        int grp = 0;
+        if constexpr (GROUP == 128) grp = unit >> 1;
+        if constexpr (GROUP == 64) grp = unit;
+        // 1024 + zero in both halves (exact: fp16 bits 0x6400 + z), and the scale.
+        const uint32_t z0 = 0x6400u + __ldg(zr0 + grp);
+        const uint32_t z1 = 0x6400u + __ldg(zr1 + grp);
+        const uint32_t zp0 = z0 | (z0 << 16), zp1 = z1 | (z1 << 16);
+        const float sf0 = __half2float(__ldg(sr0 + grp));
+        const float sf1 = __half2float(__ldg(sr1 + grp));
+        uint32_t X[NT][8];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);
-          acc[t][1] = __fmaf_rn(sf0, part[t][1], acc[t][1]);
-          acc[t][2] = __fmaf_rn(sf1, part[t][2], acc[t][2]);
-          acc[t][3] = __fmaf_rn(sf1, part[t][3], acc[t][3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) part[t][e] = 0.f;
+          uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+          if (t * 8 + g < M) {
+            const int chunk = unit * 8 + 2 * c;   // 16-byte chunk of x[tok][unit*64 + 16c]
+            if constexpr (XSMEM) {
+              v0 = xrow[t][chunk ^ g];
+              v1 = xrow[t][(chunk + 1) ^ g];
+            } else {
+              v0 = __ldg(xrow[t] + chunk);
+              v1 = __ldg(xrow[t] + chunk + 1);
+            }
+          }
+          X[t][0] = v0.x; X[t][1] = v0.y; X[t][2] = v0.z; X[t][3] = v0.w;
+          X[t][4] = v1.x; X[t][5] = v1.y; X[t][6] = v1.z; X[t][7] = v1.w;
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t a[4];
+          a[0] = hsub2_u32(code_pair<BITS>(a0.lo, j), zp0);   // row g,   slots 2c, 2c+1
+          a[1] = hsub2_u32(code_pair<BITS>(a1.lo, j), zp1);   // row g+8
+          a[2] = hsub2_u32(code_pair<BITS>(a0.hi, j), zp0);   // row g,   slots 2c+8, 2c+9
+          a[3] = hsub2_u32(code_pair<BITS>(a1.hi, j), zp1);   // row g+8
+          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            // x[16c + j], x[16c + j + 4]  and  x[16c + 8 + j], x[16c + 12 + j]
+            const uint32_t bb0 = __byte_perm(X[t][j >> 1], X[t][(j >> 1) + 2], sel);
+            const uint32_t bb1 = __byte_perm(X[t][4 + (j >> 1)], X[t][6 + (j >> 1)], sel);
+            mma_16816(part[t], a, bb0, bb1);
+          }
+        }
+        last_sf0 = sf0;
+        last_sf1 = sf1;
+        // End of a group: scale it into the row's sum (per-row groups are
+        // scaled when their tile closes).
+        if (GROUP == 64 || (GROUP == 128 && (unit & 1))) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);
+            acc[t][1] = __fmaf_rn(sf0, part[t][1], acc[t][1]);
+            acc[t][2] = __fmaf_rn(sf1, part[t][2], acc[t][2]);
+            acc[t][3] = __fmaf_rn(sf1, part[t][3], acc[t][3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) part[t][e] = 0.f;
+          }
+        }
+        ++unit;
       }
     }
+    finish_tile(unit);
   }
-  if (i0 < i1) finish_tile(cur_tile, tile_first, i1);
+combine:
   __syncthreads();
   // The parked partial sums, in warp order (equal tile ids are consecutive);
   // thread e of the block owns element e of a tile (16 rows x 16 tokens).
   for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x) {
     const int row = e >> 4, tok = e & 15;
-    int64_t tile = -1;
+    int64_t tl = -1;
     float sum = 0.f;
     for (int w = 0; w < nwarps; ++w) {
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int64_t t = part_tile[w][s];
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int64_t t = part_tile[w][s2];
         if (t < 0) continue;
-        if (t != tile) {
-          if (tile >= 0 && tile * 16 + row < N && tok < M)
-            atomicAdd(y + tok * N + tile * 16 + row, sum);
-          tile = t;
+        if (t != tl) {
+          if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+          tl = t;
           sum = 0.f;
         }
-        sum = __fadd_rn(sum, part_smem[w][s][e]);
+        sum = __fadd_rn(sum, part_smem[w][s2][e]);
       }
     }
-    if (tile >= 0 && tile * 16 + row < N && tok < M) atomicAdd(y + tok * N + tile * 16 + row, sum);
+    if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
   }
 }
 
