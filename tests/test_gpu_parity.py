@@ -1,9 +1,9 @@
 """CUDA path vs the CPU oracle, element by element, through the C ABI.
 
-Bars: bit-exact for codes, packed words, zeros, fp16 scales and the exact
-channel statistic; per-grid-point loss within 1e-3 relative; the chosen alpha
-equal unless the oracle's two best losses are within 1e-3 relative; s within
-1 ulp (the fp64 pow of the two sides may differ in its last bit).
+Bars: bit-exact for codes, packed words, zeros, fp16 scales, the exact
+channel statistic and s; per-grid-point loss within 1e-3 relative; the
+chosen alpha equal unless the oracle's two best losses are within 1e-3
+relative.
 """
 import numpy as np
 import pytest
@@ -122,20 +122,24 @@ def test_search_rejects_non_finite_inputs(where):
 # --------------------------------------------------------------------------
 # Scales.
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("K", [1, 100, 4096, 11008])
-def test_scales_match_oracle(K):
+@pytest.mark.parametrize("n_grid", [5, 20, 64])
+@pytest.mark.parametrize("K", [1, 100, 4096, 11008, 65536])
+def test_scales_match_oracle(K, n_grid):
+    """s equal, bit for bit, to the oracle's fp32 rounding of its fp64 power,
+    at every grid point: both sides stay far within half an fp32 ulp of the
+    exact value (the GPU's log/exp recurrence to about 2^-47 relative), so
+    they round alike except within ~2^-23 of a rounding boundary -- measured
+    on a B300: no value differs in 21.5 million (these inputs and two more
+    seeds)."""
     rng = workloads.weight_rng(K)
     sX = np.exp(rng.uniform(-3, 5, K))
     if K > 4:
         sX[:3] = [0.0, 1e-7, 1e-4]
-    s = host(awq.scales(cuda(sX), 20))
+    s = host(awq.scales(cuda(sX), n_grid))
     assert np.all(s[0] == 1.0)
-    same = 0
-    for i, a in enumerate(O.alpha_grid(20)):
+    for i, a in enumerate(O.alpha_grid(n_grid)):
         want = O.scale_vector(sX, a)
-        np.testing.assert_array_max_ulp(s[i], want, maxulp=1)
-        same += int(np.sum(s[i] == want))
-    assert same >= 0.999 * 20 * K
+        assert np.array_equal(s[i], want), (i, int(np.sum(s[i] != want)))
 
 
 # --------------------------------------------------------------------------
@@ -336,7 +340,7 @@ def _compare_search(X, Ws, bits, group, n_grid=20, rows_rtol=LOSS_RTOL, zero_poi
     assert res.alpha == res.best / n_grid
     s_best = host(res.s())
     s_grid = host(res.s_grid())
-    np.testing.assert_array_max_ulp(s_grid, ref["s_grid"], maxulp=1)
+    assert np.array_equal(s_grid, ref["s_grid"])
     assert np.array_equal(s_best, s_grid[res.best])
     rl = host(res.row_losses())
     off = 0
