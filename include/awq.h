@@ -193,7 +193,8 @@ awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float
  *            awq_quantize_pack (INT4 [N][K/8] or INT3 [N][3K/32]), 16-byte
  *            aligned.
  *   scales : device fp16 [N][K/group] ([N][1] for group_size -1).
- *   zeros  : device uint8, same shape.
+ *   zeros  : device uint8, same shape (integers in [0, 2^bits - 1], as the
+ *            search and awq_quantize_pack write them).
  *   cfg    : the configuration the codes were made with (bits 3 or 4,
  *            group_size; zero_point and n_grid are not used).
  *   x      : device fp16 [M][K], 1 <= M <= 16, 16-byte aligned: activations
@@ -205,7 +206,9 @@ awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float
  *            (mma.sync, fp16 operands), and each group's sum is scaled in fp32.
  *            Deterministic: run-to-run identical.
  * K % 64 == 0 and K % group == 0.  Allocates nothing (y is zeroed on the
- * stream, then accumulated). */
+ * stream, then accumulated).  K % 128 == 0 streams the codes through TMA
+ * (a device wait bounded at 2 s: if one expires, the outputs of the rows
+ * concerned read NaN); other K read them with plain loads. */
 awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uint8_t* zeros,
                             int64_t N, int64_t K, const awq_qconfig* cfg, const void* x, int M,
                             float* y, void* stream);

@@ -11,22 +11,36 @@
 // HBM-bound: per weight b/8 byte of codes plus 3 bytes per group.  The
 // multiply-adds run on the tensor cores (mma.sync m16n8k16, fp16 operands,
 // fp32 accumulation): A is a 16-row tile of the weight as exact fp16
-// (code - zero) values built in registers, B holds 8 tokens of x.  A warp
-// reads 16 rows x 64 channels (a "unit") per step and issues 4 MMAs per 8
-// tokens; at each group's end the fp32 sums are scaled by the group's fp16
-// scale (in fp32) and added to the row's accumulator.
+// (code - zero) values built in registers, B holds 8 tokens of x.  At each
+// group's end the fp32 sums are scaled by the group's fp16 scale (in fp32)
+// and added to the row's accumulator.
 //
-// Channel order.  The dot product over a group does not depend on the order
-// of its channels, so each thread of a quad takes 16 consecutive codes of its
-// two rows (one 8-byte load per row for INT4) and feeds them to the four
-// MMAs of the unit: in step j, thread c supplies channels 16c+j, 16c+j+4,
-// 16c+8+j and 16c+12+j in the slots the fragment layout gives it (2c, 2c+1,
-// 2c+8, 2c+9).  The B fragment of thread (token t, c) holds x at the same
-// channels, taken from its own 32-byte load of x[t][16c .. 16c+15] by byte
-// permutes.  (code - zero) is formed exactly in fp16: 0x6400 | code is
-// 1024 + code, minus 1024 + zero.
+// Units.  A warp step (a "unit") covers 16 rows x 128 channels when
+// K % 128 == 0, else 16 rows x 64 channels, in halves of 64 channels; a half
+// is four MMAs per 8 tokens.  In a half, each thread of a quad takes 16
+// consecutive codes of its two rows (INT4: one 8-byte load per row; INT3:
+// two 4-byte loads) and feeds them to the four MMAs: in MMA j, thread c
+// supplies channels 16c+j, 16c+j+4, 16c+8+j and 16c+12+j in the k slots the
+// fragment layout gives it (2c, 2c+1, 2c+8, 2c+9).  A group's dot product
+// does not depend on the order of its channels, and the two halves of a unit
+// never share an MMA, so 64-channel groups stay apart.
 //
-// Work split.  One block of 16 warps per SM.  The (row tile, unit) items,
+// (code - zero) in fp16, exactly.  A code masked into the low mantissa bits
+// of 1024 (0x6400 | code) is 1024 + code; minus 1024 + zero (HSUB2) is
+// code - zero.  A code masked in place at bit offset 4 is 1024 + 16 code; one
+// HFMA2 with 1/16 and -(64 + zero) gives code - zero (the product and the sum
+// are exact in fp16).  So the eight INT4 codes of a word cost one shift, four
+// LOP3s and four HSUB2/HFMA2s; INT3 codes sit at offsets 0, 3, 6, 9 (factors
+// 1, 1/8, 1/64, and a shift for the last).
+//
+// x.  When M x K fp16 fits in shared memory the block stages x once,
+// permuted so that a thread's B fragments for the four MMAs of a half are two
+// 16-byte loads (no byte permutes in the loop); for odd tokens the two
+// 64-byte halves of the staged 128 bytes are swapped, so the quads of a warp
+// (8 tokens) spread over all 32 banks.  Otherwise x is read through L1 and
+// its B fragments are formed by byte permutes.
+//
+// Work split.  One block of 16 warps per SM (8 for 16 tokens read through L1).  The (row tile, unit) items,
 // tile-major, are cut into equal contiguous ranges, one per block (each at
 // least one row tile long), and a block's range into one contiguous range per
 // warp.  A warp streams its units with the codes and group parameters of the
@@ -35,19 +49,20 @@
 // the tiles at the two ends of a warp's range go to shared memory, and the
 // block adds them up in warp order before adding them to y.  y is zeroed
 // first and at most two blocks add into an output (two fp32 additions onto
-// zero commute), so the result is deterministic.  x is staged once per block
-// in shared memory when M x K fits (16-byte chunks swizzled by token, so a
-// quad-row read is conflict-free), else read through L1.
+// zero commute), so the result is deterministic.
 #include <algorithm>
+#include <type_traits>
 
 #include "awq_internal.h"
+#include "awq_ptx.cuh"
 
 namespace awq {
 namespace {
 
-constexpr int kUnit = 64;          // channels per unit
+constexpr int kHalf = 64;          // channels per half unit (four MMAs)
 constexpr int kMaxWarps = 16;      // per block (one block per SM)
 constexpr int kXSmemMax = 192 * 1024;
+constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
 
 __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
   uint32_t v;
@@ -78,51 +93,114 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// One unit of one row as thread c needs it: codes 16c .. 16c+15 of the unit
-// as two fields (codes 0..7 and 8..15 in consecutive b-bit slots).
-struct UnitRow {
-  uint32_t lo, hi;
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// fp16 pairs made from a row's zero point z (an integer in [0, 2^b - 1]):
+// p = 1024 + z, and q1, q2 = -(1024/m + z) for the in-place factors m
+// (INT4: 16; INT3: 8 and 64).  Each is exact: 1024/m + z stays inside one
+// binade whose spacing is 1/m.
+struct ZeroPairs {
+  uint32_t p, q1, q2;
 };
 
 template <int BITS>
-__device__ __forceinline__ void load_fields(const uint32_t* p, int c, uint32_t& lo, uint32_t& hi) {
-  if (BITS == 4) {   // words 2c, 2c+1 of the unit (p points at word 2c)
-    const uint2 v = ld_stream_u64(p);
-    lo = v.x;
-    hi = v.y;
-  } else {           // bits [48c, 48c+48) of the unit's 6 words (p at word 3c/2)
-    const uint32_t w0 = ld_stream_u32(p), w1 = ld_stream_u32(p + 1);
-    if (c & 1) {
-      lo = __funnelshift_r(w0, w1, 16) & 0xFFFFFFu;
-      hi = w1 >> 8;
-    } else {
-      lo = w0 & 0xFFFFFFu;
-      hi = __funnelshift_r(w0, w1, 24) & 0xFFFFFFu;
-    }
+__device__ __forceinline__ ZeroPairs zero_pairs(uint32_t z) {
+  ZeroPairs r;
+  r.p = z * 0x00010001u + kMagic;                 // 1024 + z (spacing 1)
+  if (BITS == 4) {
+    r.q1 = z * 0x00100010u + 0xD400D400u;         // -(64 + z)  (spacing 1/16)
+    r.q2 = 0;
+  } else {
+    r.q1 = z * 0x00080008u + 0xD800D800u;         // -(128 + z) (spacing 1/8)
+    r.q2 = z * 0x00400040u + 0xCC00CC00u;         // -(16 + z)  (spacing 1/64)
+  }
+  return r;
+}
+
+// (code - zero) of codes j and j + 4 of a field of 8 codes, as an fp16 pair,
+// for j = 0..3.  INT4: code i at bits 4i.  INT3: code i at bits 3i (bits
+// above 24 are ignored).
+// (f & mask) | magic in one LOP3: the mask is the instruction's immediate and
+// `magic` (fp16 1024 in both halves) a register.  The kernels take magic as
+// an argument so that it stays in a register instead of being folded into a
+// second immediate (which would take a second LOP3).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t mask_or(uint32_t f, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(f), "n"(MASK), "r"(magic));
+  return d;
+}
+
+template <int BITS>
+__device__ __forceinline__ void dequant_field(uint32_t f, const ZeroPairs& z, uint32_t magic,
+                                              uint32_t (&d)[4]) {
+  if (BITS == 4) {
+    d[0] = hsub2_u32(mask_or<0x000F000Fu>(f, magic), z.p);
+    d[1] = hfma2_u32(mask_or<0x00F000F0u>(f, magic), 0x2C002C00u, z.q1);   // x 1/16
+    const uint32_t t = f >> 8;
+    d[2] = hsub2_u32(mask_or<0x000F000Fu>(t, magic), z.p);
+    d[3] = hfma2_u32(mask_or<0x00F000F0u>(t, magic), 0x2C002C00u, z.q1);
+  } else {
+    // Codes 0..3 stay at bits 0..11, codes 4..7 move to bits 16..27 (bits
+    // 12..15 and 28..31 are left over and never masked in).
+    const uint32_t w = (f & 0x00000FFFu) | ((f << 4) & 0xFFFFF000u);
+    d[0] = hsub2_u32(mask_or<0x00070007u>(w, magic), z.p);
+    d[1] = hfma2_u32(mask_or<0x00380038u>(w, magic), 0x30003000u, z.q1);   // x 1/8
+    d[2] = hfma2_u32(mask_or<0x01C001C0u>(w, magic), 0x24002400u, z.q2);   // x 1/64
+    d[3] = hsub2_u32(mask_or<0x00070007u>(w >> 9, magic), z.p);
   }
 }
 
-// 1024 + code_j (low half) and 1024 + code_{j+4} (high half) of a field.
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t f, int j) {
-  if (BITS == 4) return ((f >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-  const uint32_t t = f >> (3 * j);
-  return (t & 0x7u) | ((t << 4) & 0x70000u) | 0x64006400u;
+// Raw code words of one unit for the two rows of a thread, and the packed
+// group parameters of the unit (one or two zeros and fp16 scales per row).
+template <int H>
+struct UnitWords {
+  uint32_t r0[2 * H], r1[2 * H];
+  uint32_t z0, z1, s0, s1;
+};
+
+// Warps per block: 16, or 8 with twice the registers each when 16 tokens
+// are read through L1.
+template <int NT, bool XPERM>
+__host__ __device__ constexpr int block_warps() {
+  return NT == 2 && !XPERM ? 8 : kMaxWarps;
 }
 
-template <int NT, int GROUP, int BITS, bool XSMEM>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+template <int NT, int GROUP, int BITS, bool XPERM, int H>
+__global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
     k_wq_mma(const uint32_t* __restrict__ codes, const __half* __restrict__ scales,
              const uint8_t* __restrict__ zeros, int64_t N, int64_t K,
-             const __half* __restrict__ x, int M, float* __restrict__ y) {
-  extern __shared__ uint4 xs[];   // XSMEM: x [M][K/8] 16-byte chunks, chunk j of token t at j ^ (t & 7)
+             const __half* __restrict__ x, int M, float* __restrict__ y, uint32_t magic) {
+  // XPERM: x permuted, 8 chunks of 16 bytes per token and half (see above).
+  extern __shared__ uint4 xs[];
   // Partial sums of the first and last tile of each warp's range.
   __shared__ float part_smem[kMaxWarps][2][16 * 16];
   __shared__ int64_t part_tile[kMaxWarps][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int upr = static_cast<int>(K / kUnit);          // units per row tile
+  constexpr int kUnitCh = kHalf * H;
+  constexpr int kHalfWords = 2 * BITS;              // code words per row and half
+  constexpr int kUnitWords = kHalfWords * H;
+  constexpr int kGroupsPerUnit = GROUP == 64 ? H : 1;
+  // Units in flight per warp: as many as the registers allow (16 tokens, x
+  // read through L1, and two groups per unit each take more per unit; 16
+  // tokens with x read through L1 run 8 warps with twice the registers).
+  constexpr int kPrefetch =
+      (H == 2 ? (NT == 1 ? (XPERM ? 4 : (BITS == 4 ? 3 : 2)) : (XPERM ? 3 : 5))
+              : (NT == 1 ? (XPERM ? 6 : 5) : (XPERM ? 4 : 8))) -
+      (GROUP == 64 ? 1 : 0);
+  const int upr = static_cast<int>(K / kUnitCh);   // units per row tile
+  const int hcs = static_cast<int>(K / kHalf);     // halves per row
   const int64_t tiles = (N + 15) / 16;
   const int64_t items = tiles * upr;
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
@@ -131,16 +209,30 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   const int64_t i1 = b0 + (b1 - b0) * (warp + 1) / nwarps;
   const int64_t words_per_row = K * BITS / 32;
   const int64_t groups = GROUP ? K / GROUP : 1;
-  constexpr int kUnitWords = BITS == 4 ? 8 : 6;          // code words per row and unit
-  // Units of codes in flight per warp (fewer with 16 tokens: more registers
-  // per unit).
-  constexpr int kPrefetch = NT == 1 ? 8 : 5;
 
-  if constexpr (XSMEM) {
-    const int64_t cpr = K / 8;
-    for (int64_t q = threadIdx.x; q < M * cpr; q += blockDim.x) {
-      const int64_t t = q / cpr, j = q - t * cpr;
-      xs[t * cpr + (j ^ (t & 7))] = __ldg(reinterpret_cast<const uint4*>(x) + q);
+  if constexpr (XPERM) {
+    // Item q: token t, half hc, quad slot cc (channels 64 hc + 16 cc .. + 15).
+    // Chunk i of the slot holds the B words of MMAs 2i and 2i + 1:
+    // {x[j], x[j+4]} and {x[8+j], x[12+j]} of the slot's 16 channels.
+    const int per_tok = hcs * 4;
+    for (int q = threadIdx.x; q < M * per_tok; q += blockDim.x) {
+      const int t = q / per_tok, r = q - t * per_tok;
+      const int hc = r >> 2, cc = r & 3;
+      const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K +
+                                                        hc * kHalf + cc * 16);
+      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const uint32_t X[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+        o[2 * j] = __byte_perm(X[j >> 1], X[(j >> 1) + 2], sel);
+        o[2 * j + 1] = __byte_perm(X[4 + (j >> 1)], X[6 + (j >> 1)], sel);
+      }
+      const int odd4 = (t & 1) * 4;
+      uint4* dst = xs + (static_cast<int64_t>(t) * hcs + hc) * 8;
+      dst[cc ^ odd4] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[(4 + cc) ^ odd4] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
   if (lane == 0) {
@@ -150,25 +242,69 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   __syncthreads();
   if (i0 >= i1) goto combine;
   {
-    // The first code word this thread reads in a row: INT4 words 2c, 2c+1 of
-    // a unit; INT3 bits [48c, 48c+48) of its 6 words.
+    // The first code word of this thread in a half: INT4 words 2c, 2c+1;
+    // INT3 bits [48c, 48c+48) of the half's 6 words (c odd: from bit 16 of
+    // word (3c)/2).
     const int cw = BITS == 4 ? 2 * c : (3 * c) / 2;
+    const bool odd = c & 1;
     // Stream of units to load (kPrefetch ahead): tile and unit, and the two
-    // rows' code pointers at that unit.  Advanced by pointer increments; a
-    // new tile (every upr units) recomputes them.
+    // rows' code and group-parameter pointers at that unit.  Advanced by
+    // pointer increments; a new tile (every upr units) recomputes them.
     int64_t ptile = i0 / upr;
     int punit = static_cast<int>(i0 - ptile * upr);
     const uint32_t* pc0;
     const uint32_t* pc1;
+    const uint8_t* pz0 = nullptr;
+    const uint8_t* pz1 = nullptr;
+    const __half* ps0 = nullptr;
+    const __half* ps1 = nullptr;
     auto set_load_rows = [&]() {
       const int64_t l0 = min(ptile * 16 + g, N - 1), l1 = min(ptile * 16 + g + 8, N - 1);
       pc0 = codes + l0 * words_per_row + static_cast<int64_t>(punit) * kUnitWords + cw;
       pc1 = codes + l1 * words_per_row + static_cast<int64_t>(punit) * kUnitWords + cw;
+      if constexpr (GROUP != 0) {
+        const int64_t gi = static_cast<int64_t>(punit) * kGroupsPerUnit;
+        pz0 = zeros + l0 * groups + gi;
+        pz1 = zeros + l1 * groups + gi;
+        ps0 = scales + l0 * groups + gi;
+        ps1 = scales + l1 * groups + gi;
+      }
     };
     set_load_rows();
-    auto load_next = [&](UnitRow& r0, UnitRow& r1) {
-      load_fields<BITS>(pc0, c, r0.lo, r0.hi);
-      load_fields<BITS>(pc1, c, r1.lo, r1.hi);
+    auto load_next = [&](UnitWords<H>& u) {
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        if constexpr (BITS == 4) {
+          const uint2 v0 = ld_stream_u64(pc0 + h * kHalfWords);
+          const uint2 v1 = ld_stream_u64(pc1 + h * kHalfWords);
+          u.r0[2 * h] = v0.x;
+          u.r0[2 * h + 1] = v0.y;
+          u.r1[2 * h] = v1.x;
+          u.r1[2 * h + 1] = v1.y;
+        } else {
+          u.r0[2 * h] = ld_stream_u32(pc0 + h * kHalfWords);
+          u.r0[2 * h + 1] = ld_stream_u32(pc0 + h * kHalfWords + 1);
+          u.r1[2 * h] = ld_stream_u32(pc1 + h * kHalfWords);
+          u.r1[2 * h + 1] = ld_stream_u32(pc1 + h * kHalfWords + 1);
+        }
+      }
+      if constexpr (GROUP != 0) {
+        if constexpr (kGroupsPerUnit == 2) {   // two groups: 2 zeros, 2 scales per row
+          u.z0 = __ldg(reinterpret_cast<const unsigned short*>(pz0));
+          u.z1 = __ldg(reinterpret_cast<const unsigned short*>(pz1));
+          u.s0 = __ldg(reinterpret_cast<const unsigned int*>(ps0));
+          u.s1 = __ldg(reinterpret_cast<const unsigned int*>(ps1));
+        } else {
+          u.z0 = __ldg(pz0);
+          u.z1 = __ldg(pz1);
+          u.s0 = __ldg(reinterpret_cast<const unsigned short*>(ps0));
+          u.s1 = __ldg(reinterpret_cast<const unsigned short*>(ps1));
+        }
+        pz0 += kGroupsPerUnit;
+        pz1 += kGroupsPerUnit;
+        ps0 += kGroupsPerUnit;
+        ps1 += kGroupsPerUnit;
+      }
       pc0 += kUnitWords;
       pc1 += kUnitWords;
       if (++punit == upr) {
@@ -178,36 +314,44 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
       }
     };
     const int n = static_cast<int>(i1 - i0);   // units of this warp
-    UnitRow q0[kPrefetch], q1[kPrefetch];
+    UnitWords<H> q[kPrefetch];
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p)
-      if (p < n) load_next(q0[p], q1[p]);
+      if (p < n) load_next(q[p]);
 
-    // The unit being computed: its tile, its index in the tile, and the
-    // tile's group parameters and x rows.
+    // The unit being computed: its tile, its index in the tile, and (groups
+    // of a whole row) the tile's group parameters.
     int64_t tile = i0 / upr;
     int unit = static_cast<int>(i0 - tile * upr);
     int tile_u0 = unit;   // first unit of the current tile inside this range
-    const uint8_t* zr0;
-    const uint8_t* zr1;
-    const __half* sr0;
-    const __half* sr1;
+    ZeroPairs rz0{}, rz1{};
+    float rsf0 = 0.f, rsf1 = 0.f;
     auto set_rows = [&]() {
-      const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
-      zr0 = zeros + l0 * groups;
-      zr1 = zeros + l1 * groups;
-      sr0 = scales + l0 * groups;
-      sr1 = scales + l1 * groups;
+      if constexpr (GROUP == 0) {
+        const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+        rz0 = zero_pairs<BITS>(__ldg(zeros + l0));
+        rz1 = zero_pairs<BITS>(__ldg(zeros + l1));
+        rsf0 = __half2float(__ldg(scales + l0));
+        rsf1 = __half2float(__ldg(scales + l1));
+      }
     };
     set_rows();
-    // x of this thread's tokens (t * 8 + g): 16-byte chunks 2c + 8 unit and
-    // the next, swizzled by (token & 7) = g in shared memory.
-    const uint4* xrow[NT];
+    // x of this thread's tokens (t * 8 + g, tokens past M read token M - 1;
+    // their output columns are never written).  XPERM: the two chunks of
+    // half 0 (add 8 chunks per half); else 16-byte chunk 2c of half 0.
+    const uint4* xa[NT];
+    const uint4* xb[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const int tok = t * 8 + g;
-      if constexpr (XSMEM) xrow[t] = xs + static_cast<int64_t>(min(tok, M - 1)) * (K / 8);
-      else xrow[t] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(min(tok, M - 1)) * K);
+      const int tok = min(t * 8 + g, M - 1);
+      if constexpr (XPERM) {
+        const int odd4 = (tok & 1) * 4;
+        xa[t] = xs + static_cast<int64_t>(tok) * hcs * 8 + (c ^ odd4);
+        xb[t] = xs + static_cast<int64_t>(tok) * hcs * 8 + ((4 + c) ^ odd4);
+      } else {
+        xa[t] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * K) + 2 * c;
+        xb[t] = xa[t] + 1;
+      }
     }
 
     float acc[NT][4], part[NT][4];
@@ -215,19 +359,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
-    float last_sf0 = 0.f, last_sf1 = 0.f;   // group scales of the last unit done
 
-    // Close the current tile at unit `end`: scale the group the range leaves
-    // open (per-row groups: always), then add the tile to y if this warp did
-    // all of it, else park it in shared memory for the block's sum.
+    // Close the current tile at unit `end`: scale the sums of a whole-row
+    // group, then add the tile to y if this warp did all of it, else park it
+    // in shared memory for the block's sum.
     auto finish_tile = [&](int end) {
-      if (GROUP == 0 || (GROUP == 128 && (end & 1))) {
+      if constexpr (GROUP == 0) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          acc[t][0] = __fmaf_rn(last_sf0, part[t][0], acc[t][0]);
-          acc[t][1] = __fmaf_rn(last_sf0, part[t][1], acc[t][1]);
-          acc[t][2] = __fmaf_rn(last_sf1, part[t][2], acc[t][2]);
-          acc[t][3] = __fmaf_rn(last_sf1, part[t][3], acc[t][3]);
+          acc[t][0] = __fmaf_rn(rsf0, part[t][0], acc[t][0]);
+          acc[t][1] = __fmaf_rn(rsf0, part[t][1], acc[t][1]);
+          acc[t][2] = __fmaf_rn(rsf1, part[t][2], acc[t][2]);
+          acc[t][3] = __fmaf_rn(rsf1, part[t][3], acc[t][3]);
         }
       }
       if (tile_u0 == 0 && end == upr) {
@@ -274,63 +417,84 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
           tile_u0 = 0;
           set_rows();
         }
-        const UnitRow a0 = q0[p], a1 = q1[p];
-        if (base + p + kPrefetch < n) load_next(q0[p], q1[p]);
-        int grp = 0;
-        if constexpr (GROUP == 128) grp = unit >> 1;
-        if constexpr (GROUP == 64) grp = unit;
-        // 1024 + zero in both halves (exact: fp16 bits 0x6400 + z), and the scale.
-        const uint32_t z0 = 0x6400u + __ldg(zr0 + grp);
-        const uint32_t z1 = 0x6400u + __ldg(zr1 + grp);
-        const uint32_t zp0 = z0 | (z0 << 16), zp1 = z1 | (z1 << 16);
-        const float sf0 = __half2float(__ldg(sr0 + grp));
-        const float sf1 = __half2float(__ldg(sr1 + grp));
-        uint32_t X[NT][8];
+        const UnitWords<H> u = q[p];
+        if (base + p + kPrefetch < n) load_next(q[p]);
+        // Group parameters of group k of the unit (whole-row groups: the tile's).
+        ZeroPairs z0, z1;
+        float sf0 = 0.f, sf1 = 0.f;
+        auto group_params = [&](int k) {
+          if constexpr (GROUP == 0) {
+            z0 = rz0;
+            z1 = rz1;
+          } else {
+            z0 = zero_pairs<BITS>((u.z0 >> (8 * k)) & 0xFFu);
+            z1 = zero_pairs<BITS>((u.z1 >> (8 * k)) & 0xFFu);
+            sf0 = half_bits_to_float(u.s0 >> (16 * k));
+            sf1 = half_bits_to_float(u.s1 >> (16 * k));
+          }
+        };
+        group_params(0);
+        const int hc0 = unit * H;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-          if (t * 8 + g < M) {
-            const int chunk = unit * 8 + 2 * c;   // 16-byte chunk of x[tok][unit*64 + 16c]
-            if constexpr (XSMEM) {
-              v0 = xrow[t][chunk ^ g];
-              v1 = xrow[t][(chunk + 1) ^ g];
+        for (int h = 0; h < H; ++h) {
+          if (kGroupsPerUnit == 2 && h == 1) group_params(1);
+          // B fragments: MMA j takes words 2j and 2j + 1.
+          uint32_t B[NT][8];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int off = (hc0 + h) * 8;
+            if constexpr (XPERM) {
+              const uint4 v0 = xa[t][off], v1 = xb[t][off];
+              B[t][0] = v0.x; B[t][1] = v0.y; B[t][2] = v0.z; B[t][3] = v0.w;
+              B[t][4] = v1.x; B[t][5] = v1.y; B[t][6] = v1.z; B[t][7] = v1.w;
             } else {
-              v0 = __ldg(xrow[t] + chunk);
-              v1 = __ldg(xrow[t] + chunk + 1);
+              const uint4 v0 = __ldg(xa[t] + off), v1 = __ldg(xb[t] + off);
+              const uint32_t X[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+                B[t][2 * j] = __byte_perm(X[j >> 1], X[(j >> 1) + 2], sel);
+                B[t][2 * j + 1] = __byte_perm(X[4 + (j >> 1)], X[6 + (j >> 1)], sel);
+              }
             }
           }
-          X[t][0] = v0.x; X[t][1] = v0.y; X[t][2] = v0.z; X[t][3] = v0.w;
-          X[t][4] = v1.x; X[t][5] = v1.y; X[t][6] = v1.z; X[t][7] = v1.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t a[4];
-          a[0] = hsub2_u32(code_pair<BITS>(a0.lo, j), zp0);   // row g,   slots 2c, 2c+1
-          a[1] = hsub2_u32(code_pair<BITS>(a1.lo, j), zp1);   // row g+8
-          a[2] = hsub2_u32(code_pair<BITS>(a0.hi, j), zp0);   // row g,   slots 2c+8, 2c+9
-          a[3] = hsub2_u32(code_pair<BITS>(a1.hi, j), zp1);   // row g+8
-          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            // x[16c + j], x[16c + j + 4]  and  x[16c + 8 + j], x[16c + 12 + j]
-            const uint32_t bb0 = __byte_perm(X[t][j >> 1], X[t][(j >> 1) + 2], sel);
-            const uint32_t bb1 = __byte_perm(X[t][4 + (j >> 1)], X[t][6 + (j >> 1)], sel);
-            mma_16816(part[t], a, bb0, bb1);
+          // The fields (codes 0..7 and 8..15 of this thread's 16) of both rows.
+          uint32_t lo0, hi0, lo1, hi1;
+          if constexpr (BITS == 4) {
+            lo0 = u.r0[2 * h];
+            hi0 = u.r0[2 * h + 1];
+            lo1 = u.r1[2 * h];
+            hi1 = u.r1[2 * h + 1];
+          } else {
+            const int sl = odd ? 16 : 0, sh = odd ? 8 : 24;
+            lo0 = __funnelshift_r(u.r0[2 * h], u.r0[2 * h + 1], sl);
+            hi0 = __funnelshift_r(odd ? u.r0[2 * h + 1] : u.r0[2 * h], u.r0[2 * h + 1], sh);
+            lo1 = __funnelshift_r(u.r1[2 * h], u.r1[2 * h + 1], sl);
+            hi1 = __funnelshift_r(odd ? u.r1[2 * h + 1] : u.r1[2 * h], u.r1[2 * h + 1], sh);
           }
-        }
-        last_sf0 = sf0;
-        last_sf1 = sf1;
-        // End of a group: scale it into the row's sum (per-row groups are
-        // scaled when their tile closes).
-        if (GROUP == 64 || (GROUP == 128 && (unit & 1))) {
+          uint32_t dl0[4], dl1[4], dh0[4], dh1[4];
+          dequant_field<BITS>(lo0, z0, magic, dl0);   // row g,   slots 2c, 2c+1
+          dequant_field<BITS>(lo1, z1, magic, dl1);   // row g+8
+          dequant_field<BITS>(hi0, z0, magic, dh0);   // row g,   slots 2c+8, 2c+9
+          dequant_field<BITS>(hi1, z1, magic, dh1);   // row g+8
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);
-            acc[t][1] = __fmaf_rn(sf0, part[t][1], acc[t][1]);
-            acc[t][2] = __fmaf_rn(sf1, part[t][2], acc[t][2]);
-            acc[t][3] = __fmaf_rn(sf1, part[t][3], acc[t][3]);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a[4] = {dl0[j], dl1[j], dh0[j], dh1[j]};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) part[t][e] = 0.f;
+            for (int t = 0; t < NT; ++t) mma_16816(part[t], a, B[t][2 * j], B[t][2 * j + 1]);
+          }
+          // End of a group: scale it into the row's sum (whole-row groups
+          // are scaled when their tile closes).
+          if (GROUP == 64 || (GROUP == 128 && h == H - 1)) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);
+              acc[t][1] = __fmaf_rn(sf0, part[t][1], acc[t][1]);
+              acc[t][2] = __fmaf_rn(sf1, part[t][2], acc[t][2]);
+              acc[t][3] = __fmaf_rn(sf1, part[t][3], acc[t][3]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) part[t][e] = 0.f;
+            }
           }
         }
         ++unit;
@@ -363,6 +527,577 @@ combine:
   }
 }
 
+// ---------------------------------------------------------------- TMA ring
+// K % 128 == 0: each warp streams its units through its own ring of S
+// shared-memory stages filled by TMA.  A stage is up to 4 units (512
+// channels) of 16 rows in two 2-D boxes of 2 units each (INT4 16 x 128 bytes
+// in the 128-byte swizzle, 16-byte chunk j of row r at j ^ (r & 7), so the
+// quads' 8-byte reads of 8 rows hit distinct banks; INT3 16 x 96 bytes).
+// Stages end at multiples of 4 units of a tile (and at the ends of a warp's
+// range), so most are 4 whole units.  Lane 0 issues a stage's two copies and
+// their transaction count on the stage's mbarrier; the warp waits on it
+// (bounded), reads the codes with shared loads and feeds the MMAs, and lane
+// 0 refills the slot with the stage S ahead once every lane has read it.
+// Group parameters of a stage are read one stage ahead, with one vector load
+// per row when the stage is whole and aligned.  The zero's fp16 pairs come
+// from one byte permute (0x64 | z in both halves is 1024 + z) and fp16
+// subtractions.  A group's first MMA starts from a zero accumulator.
+constexpr int kStageUnits = 4;        // 128-channel units per stage
+constexpr int kBoxBytes = 2048;       // one box: 16 rows x (INT4 128, INT3 96) bytes
+constexpr int kSlotBytes = 2 * kBoxBytes;
+constexpr int kMaxStages = 6;
+constexpr int kDecodeSmemMax = 227 * 1024;
+
+template <int BITS>
+__host__ __device__ constexpr int box_row_bytes() {
+  return BITS == 4 ? 128 : 96;
+}
+
+// Dynamic shared memory of the TMA kernel, in this order: the rings
+// (1024-byte aligned), x (staged), the parked partial sums, their tile ids,
+// the mbarriers, the abort flag.
+__host__ __device__ constexpr int64_t tma_smem_bytes(int nwarps, int S, int64_t xbytes, int NT) {
+  return 1024 + static_cast<int64_t>(nwarps) * S * kSlotBytes + xbytes +
+         static_cast<int64_t>(nwarps) * 2 * 16 * 8 * NT * 4 + nwarps * 2 * 8 +
+         static_cast<int64_t>(nwarps) * S * 8 + 16;
+}
+
+// D = A B with a zero accumulator input.
+__device__ __forceinline__ void mma_16816_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1) {
+  const float z = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
+// The zero's fp16 pairs from p = 1024 + z (both halves): q1, q2 by exact fp16
+// subtractions (960 - p = -(64 + z); 896 - p = -(128 + z); 1008 - p = -(16 + z)).
+template <int BITS>
+__device__ __forceinline__ ZeroPairs zero_pairs_from_p(uint32_t p) {
+  ZeroPairs r;
+  r.p = p;
+  if (BITS == 4) {
+    r.q1 = hsub2_u32(0x63806380u, p);   // 960
+    r.q2 = 0;
+  } else {
+    r.q1 = hsub2_u32(0x63006300u, p);   // 896
+    r.q2 = hsub2_u32(0x63E063E0u, p);   // 1008
+  }
+  return r;
+}
+
+// 1024 + (byte b of w) in both fp16 halves: bytes {w.b, 0x64, w.b, 0x64}.
+__device__ __forceinline__ uint32_t magic_pair_of_byte(uint32_t w, int b) {
+  return __byte_perm(w, 0x64646464u, static_cast<uint32_t>(b | 0x40 | (b << 8) | 0x4000));
+}
+
+// Group parameters of one stage for rows g and g + 8: GS = 4 (groups of 128)
+// or 8 (groups of 64) zeros (bytes) and fp16 scales per row.
+template <int GS>
+struct StageParams {
+  uint32_t z0[GS / 4], z1[GS / 4];
+  uint32_t s0[GS / 2], s1[GS / 2];
+};
+
+// Warps per block of the TMA kernel: 16, or 8 with twice the registers each
+// for 16 tokens or x read through L1.
+template <int NT, bool XPERM>
+__host__ __device__ constexpr int tma_warps() {
+  return NT == 2 || !XPERM ? 8 : kMaxWarps;
+}
+
+template <int NT, int GROUP, int BITS, bool XPERM>
+__global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
+    k_wq_tma(const __grid_constant__ CUtensorMap tmap, const __half* __restrict__ scales,
+             const uint8_t* __restrict__ zeros, int64_t N, int64_t K,
+             const __half* __restrict__ x, int M, float* __restrict__ y, int S, int vec,
+             uint32_t magic) {
+  extern __shared__ uint8_t dsmem[];
+  const uint32_t raw_base = smem_u32(dsmem);
+  uint8_t* const sm = dsmem + (((raw_base + 1023u) & ~1023u) - raw_base);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  constexpr int kRowBytes = box_row_bytes<BITS>();
+  constexpr int kUnitBytes = 16 * BITS;               // bytes of a row per 128-channel unit
+  constexpr int kTok = 8 * NT;
+  constexpr int kGPU = GROUP == 64 ? 2 : 1;           // groups per unit
+  constexpr int GS = kStageUnits * kGPU;              // groups per stage
+  const int upr = static_cast<int>(K / 128);
+  const int hcs = static_cast<int>(K / kHalf);
+  const int64_t tiles = (N + 15) / 16;
+  const int64_t items = tiles * upr;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
+  const int64_t b1 = (static_cast<int64_t>(blockIdx.x) + 1) * items / gridDim.x;
+  const int64_t i0 = b0 + (b1 - b0) * warp / nwarps;
+  const int64_t i1 = b0 + (b1 - b0) * (warp + 1) / nwarps;
+  const int64_t groups = GROUP ? K / GROUP : 1;
+
+  uint8_t* const ring = sm;
+  uint4* const xs = reinterpret_cast<uint4*>(ring + static_cast<int64_t>(nwarps) * S * kSlotBytes);
+  float* const part_all =
+      reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + (XPERM ? int64_t(M) * K * 2 : 0));
+  int64_t* const part_tile = reinterpret_cast<int64_t*>(part_all + nwarps * 2 * 16 * kTok);
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(part_tile + nwarps * 2);
+  int* const abort_flag = reinterpret_cast<int*>(bars + nwarps * S);
+
+  const uint32_t bar_w = smem_u32(bars + warp * S);
+  const uint32_t ring_w = smem_u32(ring) + static_cast<uint32_t>(warp * S * kSlotBytes);
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bar_w + 8 * s, 1);
+    part_tile[2 * warp] = -1;
+    part_tile[2 * warp + 1] = -1;
+  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  fence_barrier_init();
+  __syncwarp();
+
+  // Units of the stage that starts at `unit` with `left` units of the range
+  // to go: to the next multiple of 4, the tile's end or the range's end.
+  auto stage_units = [&](int unit, int left) {
+    return min(min(kStageUnits - (unit & (kStageUnits - 1)), upr - unit), left);
+  };
+  // Producer cursor (every lane keeps it; lane 0 issues the copies).
+  int64_t ptile = i0 / upr;
+  int punit = static_cast<int>(i0 - ptile * upr);
+  int pleft = static_cast<int>(i1 - i0);
+  int issued = 0;
+  auto produce = [&](int slot) {
+    if (lane == 0) {
+      const uint32_t bar = bar_w + 8 * slot;
+      const uint32_t dst = ring_w + slot * kSlotBytes;
+      const int xw = punit * (kUnitBytes / 4), yr = static_cast<int>(ptile * 16);
+      mbar_arrive_expect_tx(bar, 2 * 16 * kRowBytes);
+      tma_load_2d(dst, &tmap, bar, xw, yr);
+      tma_load_2d(dst + kBoxBytes, &tmap, bar, xw + 2 * kUnitBytes / 4, yr);
+    }
+    const int nu = stage_units(punit, pleft);
+    punit += nu;
+    pleft -= nu;
+    if (punit == upr) {
+      punit = 0;
+      ++ptile;
+    }
+    ++issued;
+  };
+  // The first S stages go out before x is staged.
+  for (int s = 0; s < S && pleft > 0; ++s) produce(s);
+
+  if constexpr (XPERM) {
+    // Staged x: for token t and half hc, 8 chunks of 16 bytes; chunk i*4 + cc
+    // (stored at (i*4 + cc) ^ ((t & 1) * 4)) holds the B words of MMAs 2i and
+    // 2i + 1 of quad slot cc: {x[j], x[j+4]} and {x[8+j], x[12+j]} of the
+    // slot's 16 channels 64 hc + 16 cc + (0..15).  One chunk per thread,
+    // consecutive threads writing consecutive chunks.
+    const int per_tok = hcs * 8;
+    for (int q = threadIdx.x; q < M * per_tok; q += blockDim.x) {
+      const int t = q / per_tok, r = q - t * per_tok;
+      const int hc = r >> 3, pos = r & 7;
+      const int within = pos ^ ((t & 1) * 4);
+      const int i = within >> 2, cc = within & 3;
+      const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K +
+                                                        hc * kHalf + cc * 16);
+      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const uint32_t a0 = i ? v0.y : v0.x, a2 = i ? v0.w : v0.z;
+      const uint32_t c0 = i ? v1.y : v1.x, c2 = i ? v1.w : v1.z;
+      xs[q] = make_uint4(__byte_perm(a0, a2, 0x5410u), __byte_perm(c0, c2, 0x5410u),
+                         __byte_perm(a0, a2, 0x7632u), __byte_perm(c0, c2, 0x7632u));
+    }
+  }
+  __syncthreads();
+  bool failed = false;
+  if (i0 < i1) {
+    // Group parameters: row pointers of one tile (cached) and the loads of a
+    // stage.
+    int64_t prow_tile = -1;
+    const uint8_t* zr0 = zeros;
+    const uint8_t* zr1 = zeros;
+    const __half* sr0 = scales;
+    const __half* sr1 = scales;
+    auto load_params = [&](StageParams<GS>& p, int64_t T, int U, int nu) {
+      if constexpr (GROUP != 0) {
+        if (T != prow_tile) {
+          prow_tile = T;
+          const int64_t l0 = min(T * 16 + g, N - 1), l1 = min(T * 16 + g + 8, N - 1);
+          zr0 = zeros + l0 * groups;
+          zr1 = zeros + l1 * groups;
+          sr0 = scales + l0 * groups;
+          sr1 = scales + l1 * groups;
+        }
+        const int64_t gi = static_cast<int64_t>(U) * kGPU;
+        if (nu == kStageUnits && vec) {   // aligned: one load per row and array
+          if constexpr (GS == 4) {
+            p.z0[0] = __ldg(reinterpret_cast<const unsigned int*>(zr0 + gi));
+            p.z1[0] = __ldg(reinterpret_cast<const unsigned int*>(zr1 + gi));
+            const uint2 a = __ldg(reinterpret_cast<const uint2*>(sr0 + gi));
+            const uint2 b = __ldg(reinterpret_cast<const uint2*>(sr1 + gi));
+            p.s0[0] = a.x; p.s0[1] = a.y; p.s1[0] = b.x; p.s1[1] = b.y;
+          } else {
+            const uint2 za = __ldg(reinterpret_cast<const uint2*>(zr0 + gi));
+            const uint2 zb = __ldg(reinterpret_cast<const uint2*>(zr1 + gi));
+            p.z0[0] = za.x; p.z0[1] = za.y; p.z1[0] = zb.x; p.z1[1] = zb.y;
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(sr0 + gi));
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(sr1 + gi));
+            p.s0[0] = a.x; p.s0[1] = a.y; p.s0[2] = a.z; p.s0[3] = a.w;
+            p.s1[0] = b.x; p.s1[1] = b.y; p.s1[2] = b.z; p.s1[3] = b.w;
+          }
+        } else {   // element by element (groups past the stage repeat its first)
+          const int ng = nu * kGPU;
+#pragma unroll
+          for (int k = 0; k < GS / 4; ++k) p.z0[k] = p.z1[k] = 0;
+#pragma unroll
+          for (int k = 0; k < GS / 2; ++k) p.s0[k] = p.s1[k] = 0;
+#pragma unroll
+          for (int k = 0; k < GS; ++k) {
+            const int kk = k < ng ? k : 0;
+            p.z0[k >> 2] |= static_cast<uint32_t>(__ldg(zr0 + gi + kk)) << (8 * (k & 3));
+            p.z1[k >> 2] |= static_cast<uint32_t>(__ldg(zr1 + gi + kk)) << (8 * (k & 3));
+            p.s0[k >> 1] |= static_cast<uint32_t>(__half_as_ushort(__ldg(sr0 + gi + kk)))
+                            << (16 * (k & 1));
+            p.s1[k >> 1] |= static_cast<uint32_t>(__half_as_ushort(__ldg(sr1 + gi + kk)))
+                            << (16 * (k & 1));
+          }
+        }
+      } else {
+        (void)p; (void)T; (void)U; (void)nu;
+      }
+    };
+
+    // The stage being computed, and (whole-row groups) the tile's parameters.
+    int64_t tile = i0 / upr;
+    int unit = static_cast<int>(i0 - tile * upr);
+    int tile_u0 = unit;
+    int left = static_cast<int>(i1 - i0);
+    ZeroPairs rz0{}, rz1{};
+    float rsf0 = 0.f, rsf1 = 0.f;
+    auto set_rows = [&]() {
+      if constexpr (GROUP == 0) {
+        const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+        rz0 = zero_pairs_from_p<BITS>(magic_pair_of_byte(__ldg(zeros + l0), 0));
+        rz1 = zero_pairs_from_p<BITS>(magic_pair_of_byte(__ldg(zeros + l1), 0));
+        rsf0 = __half2float(__ldg(scales + l0));
+        rsf1 = __half2float(__ldg(scales + l1));
+      }
+    };
+    set_rows();
+    const uint4* xa[NT];
+    const uint4* xb[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int tok = min(t * 8 + g, M - 1);
+      if constexpr (XPERM) {
+        const int odd4 = (tok & 1) * 4;
+        xa[t] = xs + static_cast<int64_t>(tok) * hcs * 8 + (c ^ odd4);
+        xb[t] = xs + static_cast<int64_t>(tok) * hcs * 8 + ((4 + c) ^ odd4);
+      } else {
+        xa[t] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * K) + 2 * c;
+        xb[t] = xa[t] + 1;
+      }
+    }
+    // Byte offsets of this thread's code words in a box, for row g (row
+    // g + 8 is 8 rows further), per (unit of the box, half): INT4, its 8
+    // bytes in the swizzled layout; INT3, the first of its two words.
+    uint32_t coff[4];
+#pragma unroll
+    for (int uh = 0; uh < 4; ++uh) {
+      if constexpr (BITS == 4) {
+        const uint32_t chunk = ((static_cast<uint32_t>(uh) ^ (g >> 1)) << 1) | ((c >> 1) ^ (g & 1));
+        coff[uh] = g * kRowBytes + chunk * 16 + (c & 1) * 8;
+      } else {
+        coff[uh] = g * kRowBytes + (uh >> 1) * kUnitBytes + (uh & 1) * 24 + 4 * ((3 * c) / 2);
+      }
+    }
+    const bool odd = c & 1;
+
+    float acc[NT][4], part[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
+
+    auto finish_tile = [&](int end) {
+      if constexpr (GROUP == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          acc[t][0] = __fmaf_rn(rsf0, part[t][0], acc[t][0]);
+          acc[t][1] = __fmaf_rn(rsf0, part[t][1], acc[t][1]);
+          acc[t][2] = __fmaf_rn(rsf1, part[t][2], acc[t][2]);
+          acc[t][3] = __fmaf_rn(rsf1, part[t][3], acc[t][3]);
+        }
+      }
+      if (tile_u0 == 0 && end == upr) {
+        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int m0 = t * 8 + 2 * c;
+          if (r0 < N) {
+            if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
+            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
+          }
+          if (r1 < N) {
+            if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
+            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
+          }
+        }
+      } else {
+        const int slot = tile == i0 / upr ? 0 : 1;   // the range's first or last tile
+        float* ps = part_all + (warp * 2 + slot) * 16 * kTok;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int m0 = t * 8 + 2 * c;
+          ps[g * kTok + m0] = acc[t][0];
+          ps[g * kTok + m0 + 1] = acc[t][1];
+          ps[(g + 8) * kTok + m0] = acc[t][2];
+          ps[(g + 8) * kTok + m0 + 1] = acc[t][3];
+        }
+        if (lane == 0) part_tile[2 * warp + slot] = tile;
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[t][e] = part[t][e] = 0.f;
+    };
+
+    // One stage from slot address sl: FULL (4 units, compiled without
+    // per-unit guards) or the first nu units.
+    auto run_stage = [&](auto full_tag, uint32_t sl, const StageParams<GS>& pc, int nu) {
+      constexpr bool FULL = decltype(full_tag)::value;
+#pragma unroll
+      for (int uu = 0; uu < kStageUnits; ++uu) {
+        if (!FULL && uu >= nu) break;
+        ZeroPairs z0, z1;
+        float sf0 = 0.f, sf1 = 0.f;
+        auto group_params = [&](int k) {   // group k of the stage
+          if constexpr (GROUP == 0) {
+            z0 = rz0;
+            z1 = rz1;
+          } else {
+            z0 = zero_pairs_from_p<BITS>(magic_pair_of_byte(pc.z0[k >> 2], k & 3));
+            z1 = zero_pairs_from_p<BITS>(magic_pair_of_byte(pc.z1[k >> 2], k & 3));
+            sf0 = half_bits_to_float(pc.s0[k >> 1] >> (16 * (k & 1)));
+            sf1 = half_bits_to_float(pc.s1[k >> 1] >> (16 * (k & 1)));
+          }
+        };
+        group_params(uu * kGPU);
+        const int hc0 = (unit + uu) * 2;
+        const uint32_t box = sl + (uu >> 1) * kBoxBytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (kGPU == 2 && h == 1) group_params(uu * 2 + 1);
+          uint32_t B[NT][8];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int off = (hc0 + h) * 8;
+            if constexpr (XPERM) {
+              const uint4 v0 = xa[t][off], v1 = xb[t][off];
+              B[t][0] = v0.x; B[t][1] = v0.y; B[t][2] = v0.z; B[t][3] = v0.w;
+              B[t][4] = v1.x; B[t][5] = v1.y; B[t][6] = v1.z; B[t][7] = v1.w;
+            } else {
+              const uint4 v0 = __ldg(xa[t] + off), v1 = __ldg(xb[t] + off);
+              const uint32_t X[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+                B[t][2 * j] = __byte_perm(X[j >> 1], X[(j >> 1) + 2], sel);
+                B[t][2 * j + 1] = __byte_perm(X[4 + (j >> 1)], X[6 + (j >> 1)], sel);
+              }
+            }
+          }
+          uint32_t lo0, hi0, lo1, hi1;
+          const uint32_t a0 = box + coff[(uu & 1) * 2 + h];
+          if constexpr (BITS == 4) {
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo0), "=r"(hi0) : "r"(a0));
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(lo1), "=r"(hi1)
+                         : "r"(a0 + 8 * kRowBytes));
+          } else {
+            uint32_t w0, w1, v0, v1;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(a0));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(a0 + 4));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v0) : "r"(a0 + 8 * kRowBytes));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v1) : "r"(a0 + 8 * kRowBytes + 4));
+            const int sl16 = odd ? 16 : 0, sh = odd ? 8 : 24;
+            lo0 = __funnelshift_r(w0, w1, sl16);
+            hi0 = __funnelshift_r(odd ? w1 : w0, w1, sh);
+            lo1 = __funnelshift_r(v0, v1, sl16);
+            hi1 = __funnelshift_r(odd ? v1 : v0, v1, sh);
+          }
+          uint32_t dl0[4], dl1[4], dh0[4], dh1[4];
+          dequant_field<BITS>(lo0, z0, magic, dl0);
+          dequant_field<BITS>(lo1, z1, magic, dl1);
+          dequant_field<BITS>(hi0, z0, magic, dh0);
+          dequant_field<BITS>(hi1, z1, magic, dh1);
+          // A group's first MMA starts from zero (whole-row groups keep
+          // their sum until the tile closes).
+          constexpr bool kFresh = GROUP != 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a[4] = {dl0[j], dl1[j], dh0[j], dh1[j]};
+            const bool first = kFresh && j == 0 && (GROUP == 64 || h == 0);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              if (first) mma_16816_first(part[t], a, B[t][2 * j], B[t][2 * j + 1]);
+              else mma_16816(part[t], a, B[t][2 * j], B[t][2 * j + 1]);
+            }
+          }
+          if (GROUP == 64 || (GROUP == 128 && h == 1)) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              acc[t][0] = __fmaf_rn(sf0, part[t][0], acc[t][0]);
+              acc[t][1] = __fmaf_rn(sf0, part[t][1], acc[t][1]);
+              acc[t][2] = __fmaf_rn(sf1, part[t][2], acc[t][2]);
+              acc[t][3] = __fmaf_rn(sf1, part[t][3], acc[t][3]);
+            }
+          }
+        }
+      }
+    };
+
+    StageParams<GS> pcur{}, pnext{};
+    int nu = stage_units(unit, left);
+    load_params(pcur, tile, unit, nu);
+    int slot = 0;
+    uint32_t phase = 0;
+    int consumed = 0;
+    while (true) {
+      // The next stage: its position and (one stage ahead) its parameters.
+      int nunit = unit + nu;
+      const int nleft = left - nu;
+      int64_t ntile = tile;
+      if (nunit == upr) {
+        nunit = 0;
+        ++ntile;
+      }
+      const int nnu = nleft > 0 ? stage_units(nunit, nleft) : 0;
+      if (nleft > 0) load_params(pnext, ntile, nunit, nnu);
+      if (!mbar_wait_bounded(bar_w + 8 * slot, phase, abort_flag, nullptr, 0)) {
+        failed = true;
+        break;
+      }
+      const uint32_t sl = ring_w + slot * kSlotBytes;
+      if (nu == kStageUnits) run_stage(std::true_type{}, sl, pcur, nu);
+      else run_stage(std::false_type{}, sl, pcur, nu);
+      // Every lane has read the slot (its loads fed the MMAs above): refill it.
+      __syncwarp();
+      ++consumed;
+      if (pleft > 0) produce(slot);
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1;
+      }
+      if (nleft == 0) {
+        finish_tile(unit + nu);
+        break;
+      }
+      if (ntile != tile) {
+        finish_tile(upr);
+        tile = ntile;
+        tile_u0 = 0;
+        set_rows();
+      }
+      unit = nunit;
+      left = nleft;
+      nu = nnu;
+      pcur = pnext;
+    }
+    if (failed) {
+      // Let the copies still in flight land before the block can exit.
+      for (int k = consumed; k < issued; ++k) {
+        mbar_wait_bounded(bar_w + 8 * slot, phase, nullptr, nullptr, 0, kDrainLimitNs);
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 16 * kTok; e += blockDim.x) {
+    const int row = e / kTok, tok = e - row * kTok;
+    int64_t tl = -1;
+    float sum = 0.f;
+    for (int w = 0; w < nwarps; ++w) {
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int64_t t = part_tile[2 * w + s2];
+        if (t < 0) continue;
+        if (t != tl) {
+          if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+          tl = t;
+          sum = 0.f;
+        }
+        sum = __fadd_rn(sum, part_all[(w * 2 + s2) * 16 * kTok + e]);
+      }
+    }
+    if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+  }
+  if (*abort_flag) {
+    // A wait expired: every output of the block's rows reads NaN.
+    __syncthreads();
+    const int64_t r0 = (b0 / upr) * 16, r1 = min(N, ((b1 + upr - 1) / upr) * 16);
+    for (int64_t q = threadIdx.x; q < (r1 - r0) * M; q += blockDim.x) {
+      const int64_t m = q / (r1 - r0), r = r0 + (q - m * (r1 - r0));
+      y[m * N + r] = __int_as_float(0x7FC00000);
+    }
+  }
+}
+
+template <int NT, int BITS, bool XPERM, int H>
+cudaError_t launch_wq_h(int group, int64_t blocks, int smem, const uint32_t* codes,
+                        const __half* scales, const uint8_t* zeros, int64_t N, int64_t K,
+                        const __half* x, int M, float* y, cudaStream_t st) {
+  auto go = [&](auto kern) -> cudaError_t {
+    LaunchFacts lf;   // raises the kernel's dynamic shared memory limit once per device
+    constexpr int threads = block_warps<NT, XPERM>() * 32;
+    cudaError_t err = launch_facts(reinterpret_cast<const void*>(kern), threads, kXSmemMax, &lf);
+    if (err != cudaSuccess) return err;
+    kern<<<static_cast<unsigned>(blocks), threads, smem, st>>>(codes, scales, zeros, N, K, x, M,
+                                                               y, kMagic);
+    return cudaGetLastError();
+  };
+  if (group == 64) return go(k_wq_mma<NT, 64, BITS, XPERM, H>);
+  if (group == 128) return cudaErrorInvalidValue;   // 64-channel units: K % 128 != 0
+  return go(k_wq_mma<NT, 0, BITS, XPERM, H>);
+}
+
+template <int NT, int BITS, bool XPERM>
+cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, const uint32_t* codes,
+                       const __half* scales, const uint8_t* zeros, int64_t N, int64_t K,
+                       const __half* x, int M, float* y, cudaStream_t st) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // The codes as a 2-D tensor of 32-bit words [N][K b / 32]; boxes of 16
+  // rows x two units (INT4 128 bytes, 128-byte swizzle; INT3 96 bytes).
+  // Rows past N and words past a row's end read as zeros.
+  CUtensorMap tmap;
+  const int64_t words = K * BITS / 32;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(words), static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(words) * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_row_bytes<BITS>() / 4), 16};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(codes), dims, strides,
+          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  auto go = [&](auto kern) -> cudaError_t {
+    LaunchFacts lf;   // raises the kernel's dynamic shared memory limit once per device
+    constexpr int threads = tma_warps<NT, XPERM>() * 32;
+    cudaError_t err = launch_facts(reinterpret_cast<const void*>(kern), threads, kDecodeSmemMax,
+                                   &lf);
+    if (err != cudaSuccess) return err;
+    kern<<<static_cast<unsigned>(blocks), threads, static_cast<size_t>(smem), st>>>(
+        tmap, scales, zeros, N, K, x, M, y, S, vec, kMagic);
+    return cudaGetLastError();
+  };
+  if (group == 128) return go(k_wq_tma<NT, 128, BITS, XPERM>);
+  if (group == 64) return go(k_wq_tma<NT, 64, BITS, XPERM>);
+  return go(k_wq_tma<NT, 0, BITS, XPERM>);
+}
+
 template <int NT, int BITS>
 cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
                       const uint8_t* zeros, int64_t N, int64_t K, const __half* x, int M,
@@ -374,25 +1109,33 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
   const int64_t tiles = (N + 15) / 16;
   const int64_t blocks = std::min<int64_t>(device_sm_count(), tiles);
   const int64_t xbytes = static_cast<int64_t>(M) * K * 2;
-  const bool xsmem = xbytes <= kXSmemMax;
-  const int smem = xsmem ? static_cast<int>(xbytes) : 0;
-  auto go = [&](auto kern) -> cudaError_t {
-    LaunchFacts lf;   // raises the kernel's dynamic shared memory limit once per device
-    cudaError_t err = launch_facts(reinterpret_cast<const void*>(kern), kMaxWarps * 32,
-                                   kXSmemMax, &lf);
-    if (err != cudaSuccess) return err;
-    kern<<<static_cast<unsigned>(blocks), kMaxWarps * 32, smem, st>>>(codes, scales, zeros, N, K,
-                                                                      x, M, y);
-    return cudaGetLastError();
-  };
-  if (xsmem) {
-    if (group == 128) return go(k_wq_mma<NT, 128, BITS, true>);
-    if (group == 64) return go(k_wq_mma<NT, 64, BITS, true>);
-    return go(k_wq_mma<NT, 0, BITS, true>);
+  if (K % 128 == 0) {
+    // Stage x when it leaves room for 2 stages per warp; the rest of the
+    // shared memory is ring (at most kMaxStages stages per warp).
+    const bool xperm = tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes, NT) <= kDecodeSmemMax;
+    const int nw = xperm ? tma_warps<NT, true>() : tma_warps<NT, false>();
+    const int64_t xb = xperm ? xbytes : 0;
+    int S = 1;
+    while (S < kMaxStages && tma_smem_bytes(nw, S + 1, xb, NT) <= kDecodeSmemMax) ++S;
+    const int64_t smem = tma_smem_bytes(nw, S, xb, NT);
+    // Whole aligned stages read their groups' zeros and scales with one
+    // vector load per row (4 or 8 groups) when the arrays allow it.
+    const int gs = kStageUnits * (group == 64 ? 2 : 1);
+    const int64_t groups = group > 0 ? K / group : 1;
+    const int vec = group > 0 && groups % gs == 0 &&
+                    reinterpret_cast<uintptr_t>(zeros) % gs == 0 &&
+                    reinterpret_cast<uintptr_t>(scales) % (2 * gs) == 0;
+    return xperm ? launch_tma<NT, BITS, true>(group, blocks, S, smem, vec, codes, scales, zeros, N,
+                                              K, x, M, y, st)
+                 : launch_tma<NT, BITS, false>(group, blocks, S, smem, vec, codes, scales, zeros,
+                                               N, K, x, M, y, st);
   }
-  if (group == 128) return go(k_wq_mma<NT, 128, BITS, false>);
-  if (group == 64) return go(k_wq_mma<NT, 64, BITS, false>);
-  return go(k_wq_mma<NT, 0, BITS, false>);
+  const bool xperm = xbytes <= kXSmemMax;
+  const int smem = xperm ? static_cast<int>(xbytes) : 0;
+  return xperm ? launch_wq_h<NT, BITS, true, 1>(group, blocks, smem, codes, scales, zeros, N, K, x,
+                                                M, y, st)
+               : launch_wq_h<NT, BITS, false, 1>(group, blocks, smem, codes, scales, zeros, N, K, x,
+                                                 M, y, st);
 }
 
 }  // namespace
@@ -400,7 +1143,7 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
 cudaError_t launch_w4_matvec(const uint32_t* codes, const __half* scales, const uint8_t* zeros,
                              int64_t N, int64_t K, int group, int bits, const __half* x, int M,
                              float* y, cudaStream_t st) {
-  if (M < 1 || M > 16 || K % kUnit) return cudaErrorInvalidValue;
+  if (M < 1 || M > 16 || K % kHalf) return cudaErrorInvalidValue;
   if (bits == 4)
     return M <= 8 ? launch_wq<1, 4>(group, codes, scales, zeros, N, K, x, M, y, st)
                   : launch_wq<2, 4>(group, codes, scales, zeros, N, K, x, M, y, st);

@@ -249,7 +249,9 @@ def _matvec_bound(codes, sc, z, group, x):
 @pytest.mark.parametrize("bits", [4, 3])
 @pytest.mark.parametrize("M", [1, 2, 8, 9, 16])
 @pytest.mark.parametrize("N,K,group", [(1, 128, 128), (37, 256, 64), (300, 1024, 128),
-                                       (129, 4096, -1), (64, 11008, 64)])
+                                       (129, 4096, -1), (64, 11008, 64), (50, 1408, 128),
+                                       # K % 128 == 64: 64-channel units
+                                       (45, 704, 64), (33, 192, -1)])
 def test_decode_product(M, N, K, group, bits):
     rng = workloads.weight_rng(M * 100 + N + K + group + bits)
     W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
@@ -282,6 +284,52 @@ def test_decode_product_large_and_deterministic(bits):
     want = O.w4a16_matvec(oc, osc, oz, 128, x)
     err = np.abs(y.astype(np.float64) - want)
     assert np.all(err <= _matvec_bound(oc, osc, oz, 128, x) + 1e-30)
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("M,N,K,group", [(8, 50, 12416, 64), (8, 40, 12352, 64),
+                                         (16, 30, 6208, -1), (5, 20, 40064, 128)])
+def test_decode_product_x_through_l1(M, N, K, group, bits):
+    """M x K fp16 above the 192 KiB staged in shared memory: x is read
+    through L1 and permuted in registers (128- and 64-channel units, 8 and
+    16 tokens)."""
+    rng = workloads.weight_rng(M + N + K + bits)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, cuda(x), group, bits=bits))
+    oc, osc, oz = O.quantize_groups(W, s, bits, group)
+    want = O.w4a16_matvec(oc, osc, oz, group, x)
+    err = np.abs(y.astype(np.float64) - want)
+    assert np.all(err <= _matvec_bound(oc, osc, oz, group, x) + 1e-30), float(err.max())
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+def test_decode_product_unaligned_group_parameters(bits):
+    """Zeros at an odd address and scales at 2 mod 4 (slices of larger
+    buffers): 64-channel groups are then read one at a time (64-channel
+    units, so another split of the work and another fp32 rounding order than
+    from aligned copies): within the bound, and deterministic."""
+    rng = workloads.weight_rng(515 + bits)
+    N, K, M = 70, 1024, 3
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, 64)
+    zbuf = torch.zeros(z.numel() + 1, dtype=z.dtype, device=z.device)
+    zbuf[1:] = z.reshape(-1)
+    sbuf = torch.zeros(sc.numel() + 1, dtype=sc.dtype, device=sc.device)
+    sbuf[1:] = sc.reshape(-1)
+    zu, su = zbuf[1:], sbuf[1:]
+    assert zu.data_ptr() % 2 == 1 and su.data_ptr() % 4 == 2
+    x = cuda(rng.standard_normal((M, K)).astype(np.float16))
+    y_un = host(awq.w4a16_matvec(codes, su, zu, N, K, x, 64, bits=bits))
+    assert np.array_equal(y_un, host(awq.w4a16_matvec(codes, su, zu, N, K, x, 64, bits=bits)))
+    oc, osc, oz = O.quantize_groups(W, s, bits, 64)
+    xh = x.cpu().numpy()
+    want = O.w4a16_matvec(oc, osc, oz, 64, xh)
+    err = np.abs(y_un.astype(np.float64) - want)
+    assert np.all(err <= _matvec_bound(oc, osc, oz, 64, xh) + 1e-30), float(err.max())
 
 
 def test_decode_product_symmetric_codes():

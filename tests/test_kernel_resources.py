@@ -22,7 +22,14 @@ BUDGET = [
     ("awq_quant.cu", r"k_quant_finalILi4E", 85, 0),
     ("awq_quant.cu", r"k_quant_finalILi3E", 85, 16),
     ("awq_stats.cu", r"k_stats_accumulate", 112, 0),   # 2 blocks of 288 threads per SM
-    ("awq_matvec.cu", r"k_wq_mma", 128, 0),   # one block of 16 warps per SM
+    # Decode product: one block of 16 warps per SM, or of 8 warps (255
+    # registers each) for 16 tokens with x read through L1 (NT 2, XPERM false).
+    ("awq_matvec.cu", r"k_wq_mmaILi1E|k_wq_mmaILi2ELi-?\d+ELi\dELb1E", 128, 0),
+    ("awq_matvec.cu", r"k_wq_mmaILi2ELi-?\d+ELi\dELb0E", 255, 0),
+    # TMA ring: 16 warps per SM for x staged in shared memory and up to 8
+    # tokens, else 8 (255 registers each).
+    ("awq_matvec.cu", r"k_wq_tmaILi1ELi-?\d+ELi\dELb1E", 128, 0),
+    ("awq_matvec.cu", r"k_wq_tmaILi2E|k_wq_tmaILi1ELi-?\d+ELi\dELb0E", 255, 0),
     ("awq_reduce.cu", r"k_losses", 64, 0),
 ]
 
