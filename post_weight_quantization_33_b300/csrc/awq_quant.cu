@@ -341,8 +341,11 @@ __global__ void __launch_bounds__(kQuantThreads)
         raw_to_f32(raw, w[r]);
       }
       __syncwarp();   // the slot is refilled at the next row pair
+      // Where this row pair's residual goes at the tile's first grid point
+      // (advanced by one slab per grid point).
+      __half* dst = delta + static_cast<int64_t>(a0) * slab + (row_off + row0) * K + lw.k0;
 #pragma unroll 1
-      for (int a = 0; a < na; ++a) {
+      for (int a = 0; a < na; ++a, dst += slab) {
         float sv[kPerLane], rv[kPerLane];
 #pragma unroll
         for (int q = 0; q < kPerLane / 4; ++q) {
@@ -401,18 +404,29 @@ __global__ void __launch_bounds__(kQuantThreads)
           const f32x2 rcp2 = pack2(g.rcp, g.rcp);
           const f32x2 magic2 = pack2(kMagic, kMagic), nmagic2 = pack2(-kMagic, -kMagic);
           float d[kPerLane];
+          // The two loops differ only in the lower clamp, needed only where
+          // some group of the warp is all negative (a warp-uniform branch
+          // around the loop, so the common one has one min per weight).
+          if (low) {
 #pragma unroll
-          for (int i = 0; i < kPerLane; i += 2) {
-            const f32x2 ws2 = mul2_again(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
-            const f32x2 t = mul2(ws2, rcp2);
-            float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
-            if (low) {
-              t0 = fmaxf(t0, lo);
-              t1 = fmaxf(t1, lo);
+            for (int i = 0; i < kPerLane; i += 2) {
+              const f32x2 ws2 = mul2_again(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+              const f32x2 t = mul2(ws2, rcp2);
+              const float t0 = fmaxf(fminf(lo2(t), hi), lo), t1 = fmaxf(fminf(hi2(t), hi), lo);
+              const f32x2 m = add2(add2(pack2(t0, t1), magic2), nmagic2);
+              d[i] = lo2(m);
+              d[i + 1] = hi2(m);
             }
-            const f32x2 m = add2(add2(pack2(t0, t1), magic2), nmagic2);
-            d[i] = lo2(m);
-            d[i + 1] = hi2(m);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kPerLane; i += 2) {
+              const f32x2 ws2 = mul2_again(pack2(w[r][i], w[r][i + 1]), pack2(sv[i], sv[i + 1]));
+              const f32x2 t = mul2(ws2, rcp2);
+              const float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
+              const f32x2 m = add2(add2(pack2(t0, t1), magic2), nmagic2);
+              d[i] = lo2(m);
+              d[i + 1] = hi2(m);
+            }
           }
           uint32_t o[kPerLane / 2];
 #pragma unroll
@@ -423,8 +437,7 @@ __global__ void __launch_bounds__(kQuantThreads)
             const __half2 hv = __floats2half2_rn(lo2(e), hi2(e));
             o[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-          const int64_t row = row0 + r;
-          if (lw.active && row < N) st_v8(delta + ga * slab + (row_off + row) * K + lw.k0, o);
+          if (lw.active && row0 + r < N) st_v8(dst + r * K, o);
         }
       }
     }
@@ -550,17 +563,27 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
       const float lo = -g.z, hi = L - g.z;
       const f32x2 rcp2 = pack2(g.rcp, g.rcp), magic2 = pack2(kMagic, kMagic);
       uint32_t b[kPerLane];
+      // The lower clamp only where some group of the warp is all negative (a
+      // warp-uniform branch around the loop: the common one has one min per
+      // weight).
+      if (low) {
 #pragma unroll
-      for (int i = 0; i < kPerLane; i += 2) {
-        const f32x2 t = mul2(pack2(ws[r][i], ws[r][i + 1]), rcp2);
-        float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
-        if (low) {
-          t0 = fmaxf(t0, lo);
-          t1 = fmaxf(t1, lo);
+        for (int i = 0; i < kPerLane; i += 2) {
+          const f32x2 t = mul2(pack2(ws[r][i], ws[r][i + 1]), rcp2);
+          const float t0 = fmaxf(fminf(lo2(t), hi), lo), t1 = fmaxf(fminf(hi2(t), hi), lo);
+          const f32x2 m = add2(pack2(t0, t1), magic2);
+          b[i] = static_cast<uint32_t>(m);
+          b[i + 1] = static_cast<uint32_t>(m >> 32);
         }
-        const f32x2 m = add2(pack2(t0, t1), magic2);
-        b[i] = static_cast<uint32_t>(m);
-        b[i + 1] = static_cast<uint32_t>(m >> 32);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kPerLane; i += 2) {
+          const f32x2 t = mul2(pack2(ws[r][i], ws[r][i + 1]), rcp2);
+          const float t0 = fminf(lo2(t), hi), t1 = fminf(hi2(t), hi);
+          const f32x2 m = add2(pack2(t0, t1), magic2);
+          b[i] = static_cast<uint32_t>(m);
+          b[i + 1] = static_cast<uint32_t>(m >> 32);
+        }
       }
       const bool store = lw.active && row < N;
       uint32_t* crow = codes + row * words;
