@@ -538,8 +538,8 @@ combine:
 // their transaction count on the stage's mbarrier; the warp waits on it
 // (bounded), reads the codes with shared loads and feeds the MMAs, and lane
 // 0 refills the slot with the stage S ahead once every lane has read it.
-// Group parameters of a stage are read one stage ahead, with one vector load
-// per row when the stage is whole and aligned.  The zero's fp16 pairs come
+// Group parameters of a stage are read at its start (before its wait), with
+// one vector load per row when the stage is whole and aligned.  The zero's fp16 pairs come
 // from one byte permute (0x64 | z in both halves is 1024 + z) and fp16
 // subtractions.  A group's first MMA starts from a zero accumulator.
 constexpr int kStageUnits = 4;        // 128-channel units per stage
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     return min(min(kStageUnits - (unit & (kStageUnits - 1)), upr - unit), left);
   };
   // Producer cursor (every lane keeps it; lane 0 issues the copies).
-  int64_t ptile = i0 / upr;
+  int ptile = static_cast<int>(i0 / upr);
   int punit = static_cast<int>(i0 - ptile * upr);
   int pleft = static_cast<int>(i1 - i0);
   int issued = 0;
@@ -712,16 +712,17 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
   if (i0 < i1) {
     // Group parameters: row pointers of one tile (cached) and the loads of a
     // stage.
-    int64_t prow_tile = -1;
+    int prow_tile = -1;
     const uint8_t* zr0 = zeros;
     const uint8_t* zr1 = zeros;
     const __half* sr0 = scales;
     const __half* sr1 = scales;
-    auto load_params = [&](StageParams<GS>& p, int64_t T, int U, int nu) {
+    auto load_params = [&](StageParams<GS>& p, int T, int U, int nu) {
       if constexpr (GROUP != 0) {
         if (T != prow_tile) {
           prow_tile = T;
-          const int64_t l0 = min(T * 16 + g, N - 1), l1 = min(T * 16 + g + 8, N - 1);
+          const int64_t l0 = min(static_cast<int64_t>(T) * 16 + g, N - 1);
+          const int64_t l1 = min(static_cast<int64_t>(T) * 16 + g + 8, N - 1);
           zr0 = zeros + l0 * groups;
           zr1 = zeros + l1 * groups;
           sr0 = scales + l0 * groups;
@@ -767,15 +768,16 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     };
 
     // The stage being computed, and (whole-row groups) the tile's parameters.
-    int64_t tile = i0 / upr;
-    int unit = static_cast<int>(i0 - tile * upr);
+    int tile = static_cast<int>(i0 / upr);
+    int unit = static_cast<int>(i0 - static_cast<int64_t>(tile) * upr);
     int tile_u0 = unit;
     int left = static_cast<int>(i1 - i0);
     ZeroPairs rz0{}, rz1{};
     float rsf0 = 0.f, rsf1 = 0.f;
     auto set_rows = [&]() {
       if constexpr (GROUP == 0) {
-        const int64_t l0 = min(tile * 16 + g, N - 1), l1 = min(tile * 16 + g + 8, N - 1);
+        const int64_t l0 = min(static_cast<int64_t>(tile) * 16 + g, N - 1);
+        const int64_t l1 = min(static_cast<int64_t>(tile) * 16 + g + 8, N - 1);
         rz0 = zero_pairs_from_p<BITS>(magic_pair_of_byte(__ldg(zeros + l0), 0));
         rz1 = zero_pairs_from_p<BITS>(magic_pair_of_byte(__ldg(zeros + l1), 0));
         rsf0 = __half2float(__ldg(scales + l0));
@@ -829,7 +831,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         }
       }
       if (tile_u0 == 0 && end == upr) {
-        const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+        const int64_t r0 = static_cast<int64_t>(tile) * 16 + g, r1 = r0 + 8;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int m0 = t * 8 + 2 * c;
@@ -956,23 +958,22 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       }
     };
 
-    StageParams<GS> pcur{}, pnext{};
+    StageParams<GS> pcur{};
     int nu = stage_units(unit, left);
-    load_params(pcur, tile, unit, nu);
     int slot = 0;
     uint32_t phase = 0;
     int consumed = 0;
     while (true) {
-      // The next stage: its position and (one stage ahead) its parameters.
+      // The next stage's position.
       int nunit = unit + nu;
       const int nleft = left - nu;
-      int64_t ntile = tile;
+      int ntile = tile;
       if (nunit == upr) {
         nunit = 0;
         ++ntile;
       }
       const int nnu = nleft > 0 ? stage_units(nunit, nleft) : 0;
-      if (nleft > 0) load_params(pnext, ntile, nunit, nnu);
+      load_params(pcur, tile, unit, nu);
       if (!mbar_wait_bounded(bar_w + 8 * slot, phase, abort_flag, nullptr, 0)) {
         failed = true;
         break;
@@ -1001,7 +1002,6 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       unit = nunit;
       left = nleft;
       nu = nnu;
-      pcur = pnext;
     }
     if (failed) {
       // Let the copies still in flight land before the block can exit.
