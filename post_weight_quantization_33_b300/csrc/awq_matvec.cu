@@ -545,7 +545,10 @@ combine:
 constexpr int kStageUnits = 4;        // 128-channel units per stage
 constexpr int kBoxBytes = 2048;       // one box: 16 rows x (INT4 128, INT3 96) bytes
 constexpr int kSlotBytes = 2 * kBoxBytes;
-constexpr int kMaxStages = 6;
+// Stages per warp: measured at one token on W 28672 x 8192 INT4, 2 stages
+// (37.3 us) beat 3 (40.1 us; the shared memory they take is the L1 the
+// per-stage group-parameter loads then miss) and 1 (39.4 us).
+constexpr int kMaxStages = 2;
 constexpr int kDecodeSmemMax = 227 * 1024;
 
 template <int BITS>
