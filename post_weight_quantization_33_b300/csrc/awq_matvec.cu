@@ -556,11 +556,18 @@ __host__ __device__ constexpr int box_row_bytes() {
   return BITS == 4 ? 128 : 96;
 }
 
+// With the group parameters loaded by TMA as well, a stage also holds two
+// boxes of 16 rows: 16 zeros (bytes) and 8 fp16 scales per row, placed so
+// that they cover the stage's groups.
+constexpr int kParamSlotBytes = 512;
+
 // Dynamic shared memory of the TMA kernel, in this order: the rings
-// (1024-byte aligned), x (staged), the parked partial sums, their tile ids,
-// the mbarriers, the abort flag.
-__host__ __device__ constexpr int64_t tma_smem_bytes(int nwarps, int S, int64_t xbytes, int NT) {
-  return 1024 + static_cast<int64_t>(nwarps) * S * kSlotBytes + xbytes +
+// (1024-byte aligned), the parameter boxes (with pt), x (staged), the parked
+// partial sums, their tile ids, the mbarriers, the abort flag.
+__host__ __device__ constexpr int64_t tma_smem_bytes(int nwarps, int S, int64_t xbytes, int NT,
+                                                     bool pt) {
+  return 1024 + static_cast<int64_t>(nwarps) * S * (kSlotBytes + (pt ? kParamSlotBytes : 0)) +
+         xbytes +
          static_cast<int64_t>(nwarps) * 2 * 16 * 8 * NT * 4 + nwarps * 2 * 8 +
          static_cast<int64_t>(nwarps) * S * 8 + 16;
 }
@@ -612,9 +619,10 @@ __host__ __device__ constexpr int tma_warps() {
   return NT == 2 || !XPERM ? 8 : kMaxWarps;
 }
 
-template <int NT, int GROUP, int BITS, bool XPERM>
+template <int NT, int GROUP, int BITS, bool XPERM, bool PT>
 __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
-    k_wq_tma(const __grid_constant__ CUtensorMap tmap, const __half* __restrict__ scales,
+    k_wq_tma(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_z,
+             const __grid_constant__ CUtensorMap tmap_s, const __half* __restrict__ scales,
              const uint8_t* __restrict__ zeros, int64_t N, int64_t K,
              const __half* __restrict__ x, int M, float* __restrict__ y, int S, int vec,
              uint32_t magic) {
@@ -640,7 +648,9 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
   const int64_t groups = GROUP ? K / GROUP : 1;
 
   uint8_t* const ring = sm;
-  uint4* const xs = reinterpret_cast<uint4*>(ring + static_cast<int64_t>(nwarps) * S * kSlotBytes);
+  uint8_t* const pring = ring + static_cast<int64_t>(nwarps) * S * kSlotBytes;   // PT
+  uint4* const xs =
+      reinterpret_cast<uint4*>(pring + (PT ? static_cast<int64_t>(nwarps) * S * kParamSlotBytes : 0));
   float* const part_all =
       reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + (XPERM ? int64_t(M) * K * 2 : 0));
   int64_t* const part_tile = reinterpret_cast<int64_t*>(part_all + nwarps * 2 * 16 * kTok);
@@ -649,6 +659,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
 
   const uint32_t bar_w = smem_u32(bars + warp * S);
   const uint32_t ring_w = smem_u32(ring) + static_cast<uint32_t>(warp * S * kSlotBytes);
+  const uint32_t pring_w = smem_u32(pring) + static_cast<uint32_t>(warp * S * kParamSlotBytes);
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(bar_w + 8 * s, 1);
     part_tile[2 * warp] = -1;
@@ -673,9 +684,17 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       const uint32_t bar = bar_w + 8 * slot;
       const uint32_t dst = ring_w + slot * kSlotBytes;
       const int xw = punit * (kUnitBytes / 4), yr = static_cast<int>(ptile * 16);
-      mbar_arrive_expect_tx(bar, 2 * 16 * kRowBytes);
+      mbar_arrive_expect_tx(bar, 2 * 16 * kRowBytes + (PT ? kParamSlotBytes : 0));
       tma_load_2d(dst, &tmap, bar, xw, yr);
       tma_load_2d(dst + kBoxBytes, &tmap, bar, xw + 2 * kUnitBytes / 4, yr);
+      if constexpr (PT) {
+        // The 16 zeros and 8 scales per row whose blocks hold the stage's
+        // groups (a stage never crosses a multiple of 4 units).
+        const int gz = punit * kGPU;
+        const uint32_t pdst = pring_w + slot * kParamSlotBytes;
+        tma_load_2d(pdst, &tmap_z, bar, gz & ~15, yr);
+        tma_load_2d(pdst + kParamSlotBytes / 2, &tmap_s, bar, gz & ~7, yr);
+      }
     }
     const int nu = stage_units(punit, pleft);
     punit += nu;
@@ -961,6 +980,57 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       }
     };
 
+    // PT: the stage's group parameters from its parameter boxes (rows g and
+    // g + 8; box rows of 16 bytes: zeros of groups (gz & ~15) + 0..15, scales
+    // of groups (gz & ~7) + 0..7).
+    auto smem_params = [&](StageParams<GS>& p, int slot, int U, int n) {
+      if constexpr (PT && GROUP != 0) {
+        const uint32_t pz = pring_w + slot * kParamSlotBytes, ps = pz + kParamSlotBytes / 2;
+        const int gz = U * kGPU, bz = gz & 15, bs = gz & 7;
+        const uint32_t rz0 = pz + g * 16, rz1 = pz + (g + 8) * 16;
+        const uint32_t rs0 = ps + g * 16, rs1 = ps + (g + 8) * 16;
+        if (n == kStageUnits) {
+          if constexpr (GS == 4) {
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(p.z0[0]) : "r"(rz0 + bz));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(p.z1[0]) : "r"(rz1 + bz));
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(p.s0[0]), "=r"(p.s0[1]) : "r"(rs0 + 2 * bs));
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(p.s1[0]), "=r"(p.s1[1]) : "r"(rs1 + 2 * bs));
+          } else {
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(p.z0[0]), "=r"(p.z0[1]) : "r"(rz0 + bz));
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(p.z1[0]), "=r"(p.z1[1]) : "r"(rz1 + bz));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(p.s0[0]), "=r"(p.s0[1]), "=r"(p.s0[2]), "=r"(p.s0[3]) : "r"(rs0));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(p.s1[0]), "=r"(p.s1[1]), "=r"(p.s1[2]), "=r"(p.s1[3]) : "r"(rs1));
+          }
+        } else {   // element by element (groups past the stage repeat its first)
+          const int ng = n * kGPU;
+#pragma unroll
+          for (int k = 0; k < GS / 4; ++k) p.z0[k] = p.z1[k] = 0;
+#pragma unroll
+          for (int k = 0; k < GS / 2; ++k) p.s0[k] = p.s1[k] = 0;
+#pragma unroll
+          for (int k = 0; k < GS; ++k) {
+            const int kk = k < ng ? k : 0;
+            uint32_t a, b, cs, d;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(a) : "r"(rz0 + bz + kk));
+            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b) : "r"(rz1 + bz + kk));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(cs) : "r"(rs0 + 2 * (bs + kk)));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(d) : "r"(rs1 + 2 * (bs + kk)));
+            p.z0[k >> 2] |= a << (8 * (k & 3));
+            p.z1[k >> 2] |= b << (8 * (k & 3));
+            p.s0[k >> 1] |= cs << (16 * (k & 1));
+            p.s1[k >> 1] |= d << (16 * (k & 1));
+          }
+        }
+      } else {
+        (void)p; (void)slot; (void)U; (void)n;
+      }
+    };
     StageParams<GS> pcur{};
     int nu = stage_units(unit, left);
     int slot = 0;
@@ -976,11 +1046,12 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         ++ntile;
       }
       const int nnu = nleft > 0 ? stage_units(nunit, nleft) : 0;
-      load_params(pcur, tile, unit, nu);
+      if constexpr (!PT) load_params(pcur, tile, unit, nu);
       if (!mbar_wait_bounded(bar_w + 8 * slot, phase, abort_flag, nullptr, 0)) {
         failed = true;
         break;
       }
+      if constexpr (PT) smem_params(pcur, slot, unit, nu);
       const uint32_t sl = ring_w + slot * kSlotBytes;
       if (nu == kStageUnits) run_stage(std::true_type{}, sl, pcur, nu);
       else run_stage(std::false_type{}, sl, pcur, nu);
@@ -1067,15 +1138,15 @@ cudaError_t launch_wq_h(int group, int64_t blocks, int smem, const uint32_t* cod
 }
 
 template <int NT, int BITS, bool XPERM>
-cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, const uint32_t* codes,
-                       const __half* scales, const uint8_t* zeros, int64_t N, int64_t K,
-                       const __half* x, int M, float* y, cudaStream_t st) {
+cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, bool pt,
+                       const uint32_t* codes, const __half* scales, const uint8_t* zeros, int64_t N,
+                       int64_t K, const __half* x, int M, float* y, cudaStream_t st) {
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   // The codes as a 2-D tensor of 32-bit words [N][K b / 32]; boxes of 16
   // rows x two units (INT4 128 bytes, 128-byte swizzle; INT3 96 bytes).
   // Rows past N and words past a row's end read as zeros.
-  CUtensorMap tmap;
+  CUtensorMap tmap, tmap_z, tmap_s;
   const int64_t words = K * BITS / 32;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(words), static_cast<cuuint64_t>(N)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(words) * 4};
@@ -1086,6 +1157,24 @@ cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, 
           BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  tmap_z = tmap;
+  tmap_s = tmap;
+  if (pt) {
+    // zeros [N][groups] bytes, boxes of 16 rows x 16 groups; scales [N][groups]
+    // fp16, boxes of 16 rows x 8 groups (row strides multiples of 16 bytes).
+    const int64_t groups = K / group;
+    const cuuint64_t gd[2] = {static_cast<cuuint64_t>(groups), static_cast<cuuint64_t>(N)};
+    const cuuint64_t zs[1] = {static_cast<cuuint64_t>(groups)};
+    const cuuint64_t ss[1] = {static_cast<cuuint64_t>(groups) * 2};
+    const cuuint32_t zb[2] = {16, 16}, sb[2] = {8, 16};
+    if (enc(&tmap_z, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(zeros), gd, zs, zb,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(scales), gd, ss, sb,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   auto go = [&](auto kern) -> cudaError_t {
     LaunchFacts lf;   // raises the kernel's dynamic shared memory limit once per device
     constexpr int threads = tma_warps<NT, XPERM>() * 32;
@@ -1093,12 +1182,14 @@ cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, 
                                    &lf);
     if (err != cudaSuccess) return err;
     kern<<<static_cast<unsigned>(blocks), threads, static_cast<size_t>(smem), st>>>(
-        tmap, scales, zeros, N, K, x, M, y, S, vec, kMagic);
+        tmap, tmap_z, tmap_s, scales, zeros, N, K, x, M, y, S, vec, kMagic);
     return cudaGetLastError();
   };
-  if (group == 128) return go(k_wq_tma<NT, 128, BITS, XPERM>);
-  if (group == 64) return go(k_wq_tma<NT, 64, BITS, XPERM>);
-  return go(k_wq_tma<NT, 0, BITS, XPERM>);
+  if (group == 128)
+    return pt ? go(k_wq_tma<NT, 128, BITS, XPERM, true>) : go(k_wq_tma<NT, 128, BITS, XPERM, false>);
+  if (group == 64)
+    return pt ? go(k_wq_tma<NT, 64, BITS, XPERM, true>) : go(k_wq_tma<NT, 64, BITS, XPERM, false>);
+  return go(k_wq_tma<NT, 0, BITS, XPERM, false>);
 }
 
 template <int NT, int BITS>
@@ -1115,23 +1206,29 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
   if (K % 128 == 0) {
     // Stage x when it leaves room for 2 stages per warp; the rest of the
     // shared memory is ring (at most kMaxStages stages per warp).
-    const bool xperm = tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes, NT) <= kDecodeSmemMax;
+    // Group parameters by TMA with the codes when their rows are whole
+    // multiples of 16 bytes (and the arrays 16-byte aligned); else loaded by
+    // the warps, with one vector load per row on whole aligned stages when
+    // the arrays allow it.
+    const int64_t groups = group > 0 ? K / group : 1;
+    const bool pt = group > 0 && groups % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(zeros) % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(scales) % 16 == 0;
+    const bool xperm =
+        tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes, NT, pt) <= kDecodeSmemMax;
     const int nw = xperm ? tma_warps<NT, true>() : tma_warps<NT, false>();
     const int64_t xb = xperm ? xbytes : 0;
     int S = 1;
-    while (S < kMaxStages && tma_smem_bytes(nw, S + 1, xb, NT) <= kDecodeSmemMax) ++S;
-    const int64_t smem = tma_smem_bytes(nw, S, xb, NT);
-    // Whole aligned stages read their groups' zeros and scales with one
-    // vector load per row (4 or 8 groups) when the arrays allow it.
+    while (S < kMaxStages && tma_smem_bytes(nw, S + 1, xb, NT, pt) <= kDecodeSmemMax) ++S;
+    const int64_t smem = tma_smem_bytes(nw, S, xb, NT, pt);
     const int gs = kStageUnits * (group == 64 ? 2 : 1);
-    const int64_t groups = group > 0 ? K / group : 1;
     const int vec = group > 0 && groups % gs == 0 &&
                     reinterpret_cast<uintptr_t>(zeros) % gs == 0 &&
                     reinterpret_cast<uintptr_t>(scales) % (2 * gs) == 0;
-    return xperm ? launch_tma<NT, BITS, true>(group, blocks, S, smem, vec, codes, scales, zeros, N,
-                                              K, x, M, y, st)
-                 : launch_tma<NT, BITS, false>(group, blocks, S, smem, vec, codes, scales, zeros,
-                                               N, K, x, M, y, st);
+    return xperm ? launch_tma<NT, BITS, true>(group, blocks, S, smem, vec, pt, codes, scales, zeros,
+                                              N, K, x, M, y, st)
+                 : launch_tma<NT, BITS, false>(group, blocks, S, smem, vec, pt, codes, scales,
+                                               zeros, N, K, x, M, y, st);
   }
   const bool xperm = xbytes <= kXSmemMax;
   const int smem = xperm ? static_cast<int>(xbytes) : 0;

@@ -250,6 +250,8 @@ def _matvec_bound(codes, sc, z, group, x):
 @pytest.mark.parametrize("M", [1, 2, 8, 9, 16])
 @pytest.mark.parametrize("N,K,group", [(1, 128, 128), (37, 256, 64), (300, 1024, 128),
                                        (129, 4096, -1), (64, 11008, 64), (50, 1408, 128),
+                                       # 16 groups per row: parameters by TMA
+                                       (300, 2048, 128), (40, 1024, 64),
                                        # K % 128 == 64: 64-channel units
                                        (45, 704, 64), (33, 192, -1)])
 def test_decode_product(M, N, K, group, bits):
