@@ -25,13 +25,6 @@ __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// The same product as mul2, never merged with an identical earlier one
-// (recomputing a value can be cheaper than keeping it in registers).
-__device__ __forceinline__ f32x2 mul2_again(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
   f32x2 d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
