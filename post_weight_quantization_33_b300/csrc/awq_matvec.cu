@@ -87,6 +87,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch: y is zeroed by k_zero_y, which lets the
+// product kernel start at once; the product waits for it (all of its writes
+// visible) before its first access to y.
+__device__ __forceinline__ void wait_for_zeroed_y() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__global__ void k_zero_y(float* __restrict__ y, int64_t n) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    y[i] = 0.f;
+}
+
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a),
                             *reinterpret_cast<const __half2*>(&b));
@@ -240,6 +254,7 @@ __global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
     part_tile[warp][1] = -1;
   }
   __syncthreads();
+  wait_for_zeroed_y();
   if (i0 >= i1) goto combine;
   {
     // The first code word of this thread in a half: INT4 words 2c, 2c+1;
@@ -730,6 +745,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     }
   }
   __syncthreads();
+  wait_for_zeroed_y();
   bool failed = false;
   if (i0 < i1) {
     // Group parameters: row pointers of one tile (cached) and the loads of a
@@ -1119,6 +1135,25 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
   }
 }
 
+// Launches kern after the stream's previous kernel (k_zero_y) with
+// programmatic stream serialization: kern may start before k_zero_y ends and
+// waits for it (griddepcontrol.wait) before touching y.
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(Kern kern, int64_t blocks, int threads, int64_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int NT, int BITS, bool XPERM, int H>
 cudaError_t launch_wq_h(int group, int64_t blocks, int smem, const uint32_t* codes,
                         const __half* scales, const uint8_t* zeros, int64_t N, int64_t K,
@@ -1128,9 +1163,8 @@ cudaError_t launch_wq_h(int group, int64_t blocks, int smem, const uint32_t* cod
     constexpr int threads = block_warps<NT, XPERM>() * 32;
     cudaError_t err = launch_facts(reinterpret_cast<const void*>(kern), threads, kXSmemMax, &lf);
     if (err != cudaSuccess) return err;
-    kern<<<static_cast<unsigned>(blocks), threads, smem, st>>>(codes, scales, zeros, N, K, x, M,
-                                                               y, kMagic);
-    return cudaGetLastError();
+    return launch_dependent(kern, blocks, threads, smem, st, codes, scales, zeros, N, K, x, M, y,
+                            kMagic);
   };
   if (group == 64) return go(k_wq_mma<NT, 64, BITS, XPERM, H>);
   if (group == 128) return cudaErrorInvalidValue;   // 64-channel units: K % 128 != 0
@@ -1181,9 +1215,8 @@ cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, 
     cudaError_t err = launch_facts(reinterpret_cast<const void*>(kern), threads, kDecodeSmemMax,
                                    &lf);
     if (err != cudaSuccess) return err;
-    kern<<<static_cast<unsigned>(blocks), threads, static_cast<size_t>(smem), st>>>(
-        tmap, tmap_z, tmap_s, scales, zeros, N, K, x, M, y, S, vec, kMagic);
-    return cudaGetLastError();
+    return launch_dependent(kern, blocks, threads, smem, st, tmap, tmap_z, tmap_s, scales, zeros,
+                            N, K, x, M, y, S, vec, kMagic);
   };
   if (group == 128)
     return pt ? go(k_wq_tma<NT, 128, BITS, XPERM, true>) : go(k_wq_tma<NT, 128, BITS, XPERM, false>);
@@ -1196,7 +1229,11 @@ template <int NT, int BITS>
 cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
                       const uint8_t* zeros, int64_t N, int64_t K, const __half* x, int M,
                       float* y, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(M) * N, st);
+  // y is zeroed by a kernel that lets the product start behind it.
+  const int64_t ny = static_cast<int64_t>(M) * N;
+  k_zero_y<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(ny, 256), 4 * device_sm_count())),
+             256, 0, st>>>(y, ny);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // One block per SM, at most one per 16-row tile (every block's range is
   // then at least a tile long: at most two blocks add into an output).
