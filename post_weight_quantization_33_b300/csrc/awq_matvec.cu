@@ -90,12 +90,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // Programmatic dependent launch: y is zeroed by k_zero_y, which lets the
 // product kernel start at once; the product waits for it (all of its writes
 // visible) before its first access to y.
-__device__ __forceinline__ void wait_for_zeroed_y() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
+__device__ __forceinline__ void wait_for_zeroed_y() { grid_dependency_wait(); }
 
 __global__ void k_zero_y(float* __restrict__ y, int64_t n) {
-  asm volatile("griddepcontrol.launch_dependents;");
+  grid_dependents_launch();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     y[i] = 0.f;
@@ -1133,25 +1131,6 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       y[m * N + r] = __int_as_float(0x7FC00000);
     }
   }
-}
-
-// Launches kern after the stream's previous kernel (k_zero_y) with
-// programmatic stream serialization: kern may start before k_zero_y ends and
-// waits for it (griddepcontrol.wait) before touching y.
-template <typename Kern, typename... Args>
-cudaError_t launch_dependent(Kern kern, int64_t blocks, int threads, int64_t smem,
-                             cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(static_cast<unsigned>(threads));
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int NT, int BITS, bool XPERM, int H>

@@ -24,6 +24,20 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may start before
+// the stream's previous kernel ends; grid_dependency_wait() waits until that
+// kernel has completed and its writes are visible (a no-op for a kernel
+// launched without that attribute).  grid_dependents_launch() lets the
+// stream's next kernel, if launched that way, start.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -76,7 +90,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if ((it & 31u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns || clock64() - c0 > cycle_limit) {
-        if (status != nullptr) atomicCAS(status, 0, code);
+        if (status != nullptr) {
+          grid_dependency_wait();   // the status word may be zeroed by the previous kernel
+          atomicCAS(status, 0, code);
+        }
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }
@@ -261,7 +278,10 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
     if ((it & 31u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns || clock64() - c0 > cycle_limit) {
-        if (status != nullptr) atomicCAS(status, 0, code);
+        if (status != nullptr) {
+          grid_dependency_wait();   // the status word may be zeroed by the previous kernel
+          atomicCAS(status, 0, code);
+        }
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }

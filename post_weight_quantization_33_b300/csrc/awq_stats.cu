@@ -131,6 +131,8 @@ __device__ __forceinline__ bool flush_slab(LaneSums& a, int64_t slab, int64_t kc
   if (warp != 0) return true;
   if (!mbar_wait_bounded(sm.red_full, round & 1u, sm.abort_flag, status, kDevTimeoutFull))
     return false;
+  // The sums were zeroed by the previous kernel, which this one may overlap.
+  if (round == 0) grid_dependency_wait();
   const int64_t chunk = slab * 32 + lane;
   if (chunk < kchunks) {
     uint32_t f = 0;
@@ -189,6 +191,7 @@ __global__ void __launch_bounds__(kStatThreads)
     mbar_init(sm.red_free, 1);
     *sm.abort_flag = 0;
     fence_barrier_init();
+    grid_dependents_launch();   // the finalize kernel may start (it waits for this one)
   }
   __syncthreads();
   const int64_t G = gridDim.x;
@@ -306,6 +309,7 @@ __global__ void k_stats_finalize(const unsigned long long* __restrict__ acc, int
                                  int64_t K, double* __restrict__ sX,
                                  unsigned long long* __restrict__ range,
                                  const int* __restrict__ status) {
+  grid_dependency_wait();   // the accumulation, which this kernel may overlap, is complete
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   double v = 0.0;
   if (k < K) {
@@ -316,6 +320,15 @@ __global__ void k_stats_finalize(const unsigned long long* __restrict__ acc, int
     sX[k] = v;
   }
   if (range != nullptr) block_range(fmax(v, 1e-4), k < K, range);
+}
+
+// Zeroes the sums (and the word after them) and lets the accumulation start
+// behind it.
+__global__ void k_zero_sums(unsigned long long* __restrict__ acc, int64_t n) {
+  grid_dependents_launch();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    acc[i] = 0ull;
 }
 
 __global__ void k_sx_range(const double* __restrict__ sX, int64_t K,
@@ -381,22 +394,25 @@ cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
   // One wave of resident blocks (each with a 64 KB ring), or fewer for small inputs.
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>(units, static_cast<int64_t>(lf.per_sm) * lf.sms));
-  // The sums, and the status word when it directly follows them, in one
-  // memset.
+  // The sums, and the status word when it directly follows them, zeroed by
+  // a kernel the accumulation is launched behind (it waits before its first
+  // atomic add).
   const bool status_next = status == reinterpret_cast<int*>(acc + K);
-  e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long) * (K + (status_next ? 1 : 0)), st);
+  const int64_t nz = K + (status_next ? 1 : 0);
+  k_zero_sums<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(nz, 256), 4 * lf.sms)), 256, 0,
+                st>>>(acc, nz);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_stats_accumulate<<<static_cast<unsigned>(grid), kStatThreads, kStatSmem, st>>>(
-      tmap, kchunks, tboxes, units, acc, status);
-  return cudaGetLastError();
+  return launch_dependent(k_stats_accumulate, grid, kStatThreads, kStatSmem, st, tmap, kchunks,
+                          tboxes, units, acc, status);
 }
 
 cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int64_t K,
                                   double* sX, const int* status, cudaStream_t st,
                                   unsigned long long* range) {
-  k_stats_finalize<<<static_cast<unsigned>(ceil_div(K, 256)), 256, 0, st>>>(acc, T, K, sX,
-                                                                            range, status);
-  return cudaGetLastError();
+  // Launched behind the accumulation, which lets it start early; it waits.
+  return launch_dependent(k_stats_finalize, ceil_div(K, 256), 256, 0, st,
+                          static_cast<const unsigned long long*>(acc), T, K, sX, range, status);
 }
 
 cudaError_t launch_sx_range(const double* sX, int64_t K, unsigned long long* range,
