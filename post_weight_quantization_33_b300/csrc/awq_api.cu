@@ -594,7 +594,7 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
     AWQ_CUDA(launch_stats_accumulate(Xh, T, K, acc, r->status, s), "stats kernel");
     AWQ_CUDA(launch_stats_finalize(acc, T, K, sx_ws, r->status, s, range),
              "stats finalize kernel");
-    r->launches += 2;
+    r->launches += 3;   // zeroing, accumulation, finalize
     sxp = sx_ws;
   }
   AWQ_CUDA(mark(AWQ_STAGE_SCALES), "event record");
