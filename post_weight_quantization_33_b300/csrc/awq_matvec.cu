@@ -40,11 +40,13 @@
 // (8 tokens) spread over all 32 banks.  Otherwise x is read through L1 and
 // its B fragments are formed by byte permutes.
 //
-// Work split.  One block of 16 warps per SM (8 for 16 tokens read through L1).  The (row tile, unit) items,
-// tile-major, are cut into equal contiguous ranges, one per block (each at
-// least one row tile long), and a block's range into one contiguous range per
-// warp.  A warp streams its units with the codes and group parameters of the
-// next kPrefetch units in flight, across row-tile boundaries.  A row tile
+// Work split.  One block of 16 warps per SM (8 for 16 tokens, or x read
+// through L1).  The (row tile, unit) items, tile-major, are cut into equal
+// contiguous ranges, one per block (each at least one row tile long), and a
+// block's range into one contiguous range per warp.  A warp streams its units
+// across row-tile boundaries: K % 128 == 0 through a TMA ring in shared
+// memory (k_wq_tma below), else with the codes and group parameters of the
+// next kPrefetch 64-channel units held in registers (k_wq_mma).  A row tile
 // entirely inside one warp's range is added to y at once; the partial sums of
 // the tiles at the two ends of a warp's range go to shared memory, and the
 // block adds them up in warp order before adding them to y.  y is zeroed
@@ -551,10 +553,16 @@ combine:
 // their transaction count on the stage's mbarrier; the warp waits on it
 // (bounded), reads the codes with shared loads and feeds the MMAs, and lane
 // 0 refills the slot with the stage S ahead once every lane has read it.
-// Group parameters of a stage are read at its start (before its wait), with
-// one vector load per row when the stage is whole and aligned.  The zero's fp16 pairs come
-// from one byte permute (0x64 | z in both halves is 1024 + z) and fp16
-// subtractions.  A group's first MMA starts from a zero accumulator.
+// When a row's group count is a multiple of 16, a stage also carries two
+// small boxes of 16 rows with the group zeros (16 per row) and fp16 scales (8
+// per row) whose blocks hold the stage's groups; otherwise the warp reads
+// them at the stage's start (before its wait), with one vector load per row
+// when the stage is whole and aligned.  The zero's fp16 pairs come from one
+// byte permute (0x64 | z in both halves is 1024 + z) and fp16 subtractions.
+// A group's first MMA starts from a zero accumulator.  y is zeroed by
+// k_zero_y, which the product is launched behind (programmatic dependent
+// launch: the product stages x and issues its first copies at once, and
+// waits for the zeroing only before its main loop).
 constexpr int kStageUnits = 4;        // 128-channel units per stage
 constexpr int kBoxBytes = 2048;       // one box: 16 rows x (INT4 128, INT3 96) bytes
 constexpr int kSlotBytes = 2 * kBoxBytes;
