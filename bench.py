@@ -231,7 +231,8 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 5) -> dict:
     workload's sizes (X 8192x8192; W 28672x8192), called through the C ABI
     with preallocated buffers.  Each figure times calls back to back over
     several copies of the input, each larger than L2, so no call finds its
-    input in L2 and host launch gaps are hidden; per call = elapsed / calls.
+    input in L2; the calls are queued behind a device-side wait, so host
+    launch gaps are hidden; per call = elapsed / calls.
     Bytes are the algorithmic ones: 2TK for the statistic; 2NK read + b/8 NK
     codes + 3NK/128 scales and zeros written for quantize + pack; codes,
     scales, zeros, x read and y written for the decode product."""
@@ -249,6 +250,11 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 5) -> dict:
         for fn in fns:                         # warm-up pass
             fn()
         flush(0)
+        # A device-side wait (about 2 ms) while the host queues every timed
+        # call: the calls then run back to back on the GPU, so the figure is
+        # their device time, not the host's launch rate (a call's host work,
+        # about 20 us for the statistic, can exceed its device time).
+        torch.cuda._sleep(4_000_000)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)

@@ -640,7 +640,7 @@ __host__ __device__ constexpr int tma_warps() {
   return NT == 2 || !XPERM ? 8 : kMaxWarps;
 }
 
-template <int NT, int GROUP, int BITS, bool XPERM, bool PT>
+template <int NT, int GROUP, int BITS, bool XPERM, bool PT, bool SPLIT>
 __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     k_wq_tma(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_z,
              const __grid_constant__ CUtensorMap tmap_s, const __half* __restrict__ scales,
@@ -658,12 +658,21 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
   constexpr int kTok = 8 * NT;
   constexpr int kGPU = GROUP == 64 ? 2 : 1;           // groups per unit
   constexpr int GS = kStageUnits * kGPU;              // groups per stage
-  const int upr = static_cast<int>(K / 128);
-  const int hcs = static_cast<int>(K / kHalf);
+  // SPLIT: block b of the grid's two equal parts takes the part's channels
+  // [part K/2, (part + 1) K/2), over whole row tiles, so each output gets
+  // one sum per part.
+  constexpr int kp = SPLIT ? 2 : 1;
+  const int bpp = static_cast<int>(gridDim.x) / kp;
+  const int part = SPLIT ? static_cast<int>(blockIdx.x) / bpp : 0;
+  const int64_t bb = static_cast<int64_t>(blockIdx.x) - static_cast<int64_t>(part) * bpp;
+  const int64_t kpart = K / kp;
+  const int upr = static_cast<int>(kpart / 128);     // units per row of the part
+  const int ubase = part * upr;                      // the part's first unit of a row
+  const int hcs = static_cast<int>(kpart / kHalf);
   const int64_t tiles = (N + 15) / 16;
   const int64_t items = tiles * upr;
-  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
-  const int64_t b1 = (static_cast<int64_t>(blockIdx.x) + 1) * items / gridDim.x;
+  const int64_t b0 = SPLIT ? bb * tiles / bpp * upr : bb * items / bpp;
+  const int64_t b1 = SPLIT ? (bb + 1) * tiles / bpp * upr : (bb + 1) * items / bpp;
   const int64_t i0 = b0 + (b1 - b0) * warp / nwarps;
   const int64_t i1 = b0 + (b1 - b0) * (warp + 1) / nwarps;
   const int64_t groups = GROUP ? K / GROUP : 1;
@@ -673,7 +682,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
   uint4* const xs =
       reinterpret_cast<uint4*>(pring + (PT ? static_cast<int64_t>(nwarps) * S * kParamSlotBytes : 0));
   float* const part_all =
-      reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + (XPERM ? int64_t(M) * K * 2 : 0));
+      reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + (XPERM ? int64_t(M) * kpart * 2 : 0));
   int64_t* const part_tile = reinterpret_cast<int64_t*>(part_all + nwarps * 2 * 16 * kTok);
   uint64_t* const bars = reinterpret_cast<uint64_t*>(part_tile + nwarps * 2);
   int* const abort_flag = reinterpret_cast<int*>(bars + nwarps * S);
@@ -704,14 +713,14 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     if (lane == 0) {
       const uint32_t bar = bar_w + 8 * slot;
       const uint32_t dst = ring_w + slot * kSlotBytes;
-      const int xw = punit * (kUnitBytes / 4), yr = static_cast<int>(ptile * 16);
+      const int xw = (ubase + punit) * (kUnitBytes / 4), yr = static_cast<int>(ptile * 16);
       mbar_arrive_expect_tx(bar, 2 * 16 * kRowBytes + (PT ? kParamSlotBytes : 0));
       tma_load_2d(dst, &tmap, bar, xw, yr);
       tma_load_2d(dst + kBoxBytes, &tmap, bar, xw + 2 * kUnitBytes / 4, yr);
       if constexpr (PT) {
         // The 16 zeros and 8 scales per row whose blocks hold the stage's
         // groups (a stage never crosses a multiple of 4 units).
-        const int gz = punit * kGPU;
+        const int gz = (ubase + punit) * kGPU;
         const uint32_t pdst = pring_w + slot * kParamSlotBytes;
         tma_load_2d(pdst, &tmap_z, bar, gz & ~15, yr);
         tma_load_2d(pdst + kParamSlotBytes / 2, &tmap_s, bar, gz & ~7, yr);
@@ -742,7 +751,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       const int within = pos ^ ((t & 1) * 4);
       const int i = within >> 2, cc = within & 3;
       const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K +
-                                                        hc * kHalf + cc * 16);
+                                                        part * kpart + hc * kHalf + cc * 16);
       const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
       const uint32_t a0 = i ? v0.y : v0.x, a2 = i ? v0.w : v0.z;
       const uint32_t c0 = i ? v1.y : v1.x, c2 = i ? v1.w : v1.z;
@@ -772,7 +781,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
           sr0 = scales + l0 * groups;
           sr1 = scales + l1 * groups;
         }
-        const int64_t gi = static_cast<int64_t>(U) * kGPU;
+        const int64_t gi = static_cast<int64_t>(ubase + U) * kGPU;
         if (nu == kStageUnits && vec) {   // aligned: one load per row and array
           if constexpr (GS == 4) {
             p.z0[0] = __ldg(reinterpret_cast<const unsigned int*>(zr0 + gi));
@@ -839,7 +848,8 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         xa[t] = xs + static_cast<int64_t>(tok) * hcs * 8 + (c ^ odd4);
         xb[t] = xs + static_cast<int64_t>(tok) * hcs * 8 + ((4 + c) ^ odd4);
       } else {
-        xa[t] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * K) + 2 * c;
+        xa[t] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * K + part * kpart) +
+                2 * c;
         xb[t] = xa[t] + 1;
       }
     }
@@ -1008,7 +1018,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     auto smem_params = [&](StageParams<GS>& p, int slot, int U, int n) {
       if constexpr (PT && GROUP != 0) {
         const uint32_t pz = pring_w + slot * kParamSlotBytes, ps = pz + kParamSlotBytes / 2;
-        const int gz = U * kGPU, bz = gz & 15, bs = gz & 7;
+        const int gz = (ubase + U) * kGPU, bz = gz & 15, bs = gz & 7;
         const uint32_t rz0 = pz + g * 16, rz1 = pz + (g + 8) * 16;
         const uint32_t rs0 = ps + g * 16, rs1 = ps + (g + 8) * 16;
         if (n == kStageUnits) {
@@ -1160,7 +1170,7 @@ cudaError_t launch_wq_h(int group, int64_t blocks, int smem, const uint32_t* cod
 
 template <int NT, int BITS, bool XPERM>
 cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, bool pt,
-                       const uint32_t* codes, const __half* scales, const uint8_t* zeros, int64_t N,
+                       bool split, const uint32_t* codes, const __half* scales, const uint8_t* zeros, int64_t N,
                        int64_t K, const __half* x, int M, float* y, cudaStream_t st) {
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -1205,11 +1215,24 @@ cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, 
     return launch_dependent(kern, blocks, threads, smem, st, tmap, tmap_z, tmap_s, scales, zeros,
                             N, K, x, M, y, S, vec, kMagic);
   };
+  // The K split is compiled for up to 8 tokens with x staged only.
+  constexpr bool kCanSplit = NT == 1 && XPERM;
+  if (kCanSplit && split) {
+    if (group == 128)
+      return pt ? go(k_wq_tma<NT, 128, BITS, XPERM, true, kCanSplit>)
+                : go(k_wq_tma<NT, 128, BITS, XPERM, false, kCanSplit>);
+    if (group == 64)
+      return pt ? go(k_wq_tma<NT, 64, BITS, XPERM, true, kCanSplit>)
+                : go(k_wq_tma<NT, 64, BITS, XPERM, false, kCanSplit>);
+    return go(k_wq_tma<NT, 0, BITS, XPERM, false, kCanSplit>);
+  }
   if (group == 128)
-    return pt ? go(k_wq_tma<NT, 128, BITS, XPERM, true>) : go(k_wq_tma<NT, 128, BITS, XPERM, false>);
+    return pt ? go(k_wq_tma<NT, 128, BITS, XPERM, true, false>)
+              : go(k_wq_tma<NT, 128, BITS, XPERM, false, false>);
   if (group == 64)
-    return pt ? go(k_wq_tma<NT, 64, BITS, XPERM, true>) : go(k_wq_tma<NT, 64, BITS, XPERM, false>);
-  return go(k_wq_tma<NT, 0, BITS, XPERM, false>);
+    return pt ? go(k_wq_tma<NT, 64, BITS, XPERM, true, false>)
+              : go(k_wq_tma<NT, 64, BITS, XPERM, false, false>);
+  return go(k_wq_tma<NT, 0, BITS, XPERM, false, false>);
 }
 
 template <int NT, int BITS>
@@ -1225,7 +1248,7 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
   // One block per SM, at most one per 16-row tile (every block's range is
   // then at least a tile long: at most two blocks add into an output).
   const int64_t tiles = (N + 15) / 16;
-  const int64_t blocks = std::min<int64_t>(device_sm_count(), tiles);
+  int64_t blocks = std::min<int64_t>(device_sm_count(), tiles);
   const int64_t xbytes = static_cast<int64_t>(M) * K * 2;
   if (K % 128 == 0) {
     // Stage x when it leaves room for 2 stages per warp; the rest of the
@@ -1238,10 +1261,21 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
     const bool pt = group > 0 && groups % 16 == 0 &&
                     reinterpret_cast<uintptr_t>(zeros) % 16 == 0 &&
                     reinterpret_cast<uintptr_t>(scales) % 16 == 0;
-    const bool xperm =
-        tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes, NT, pt) <= kDecodeSmemMax;
+    bool xperm = tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes, NT, pt) <= kDecodeSmemMax;
+    // Up to 8 tokens, when x does not fit but half of it does (K a multiple
+    // of 1024, so a half starts on a 4-unit stage boundary): half the blocks
+    // take the first K/2 channels and half the rest, each over whole row
+    // tiles, so every output gets exactly two sums (deterministic).  (For 9
+    // to 16 tokens x read through L1 measured faster.)
+    int kp = 1;
+    if (NT == 1 && !xperm && K % 1024 == 0 && tiles >= 2 &&
+        tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes / 2, NT, pt) <= kDecodeSmemMax) {
+      kp = 2;
+      xperm = true;
+      blocks = 2 * std::min<int64_t>(device_sm_count() / 2, tiles);
+    }
     const int nw = xperm ? tma_warps<NT, true>() : tma_warps<NT, false>();
-    const int64_t xb = xperm ? xbytes : 0;
+    const int64_t xb = xperm ? xbytes / kp : 0;
     int S = 1;
     while (S < kMaxStages && tma_smem_bytes(nw, S + 1, xb, NT, pt) <= kDecodeSmemMax) ++S;
     const int64_t smem = tma_smem_bytes(nw, S, xb, NT, pt);
@@ -1249,10 +1283,10 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
     const int vec = group > 0 && groups % gs == 0 &&
                     reinterpret_cast<uintptr_t>(zeros) % gs == 0 &&
                     reinterpret_cast<uintptr_t>(scales) % (2 * gs) == 0;
-    return xperm ? launch_tma<NT, BITS, true>(group, blocks, S, smem, vec, pt, codes, scales, zeros,
-                                              N, K, x, M, y, st)
-                 : launch_tma<NT, BITS, false>(group, blocks, S, smem, vec, pt, codes, scales,
-                                               zeros, N, K, x, M, y, st);
+    return xperm ? launch_tma<NT, BITS, true>(group, blocks, S, smem, vec, pt, kp == 2, codes,
+                                              scales, zeros, N, K, x, M, y, st)
+                 : launch_tma<NT, BITS, false>(group, blocks, S, smem, vec, pt, kp == 2, codes,
+                                               scales, zeros, N, K, x, M, y, st);
   }
   const bool xperm = xbytes <= kXSmemMax;
   const int smem = xperm ? static_cast<int>(xbytes) : 0;

@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kStatThreads)
   if (warp == kStatWarps) {
     if (lane != 0) return;
     prefetch_tmap(&tmap);
+    // X may be written by the kernel before the zeroing kernel: its first
+    // load waits for that chain to complete.
+    grid_dependency_wait();
     int64_t issued = 0;
     int64_t slab = u0 / tboxes, tb = u0 - slab * tboxes;
     for (int64_t u = u0; u < u1; ++u, ++issued, ++tb) {
@@ -323,9 +326,11 @@ __global__ void k_stats_finalize(const unsigned long long* __restrict__ acc, int
 }
 
 // Zeroes the sums (and the word after them) and lets the accumulation start
-// behind it.
+// behind it.  Launched behind the stream's previous kernel (which may still
+// read the memory it zeroes), it waits for that kernel before writing.
 __global__ void k_zero_sums(unsigned long long* __restrict__ acc, int64_t n) {
   grid_dependents_launch();
+  grid_dependency_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     acc[i] = 0ull;
@@ -395,13 +400,13 @@ cudaError_t launch_stats_accumulate(const __half* X, int64_t T, int64_t K,
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>(units, static_cast<int64_t>(lf.per_sm) * lf.sms));
   // The sums, and the status word when it directly follows them, zeroed by
-  // a kernel the accumulation is launched behind (it waits before its first
-  // atomic add).
+  // a kernel the accumulation is launched behind; that kernel is itself
+  // launched behind the stream's previous kernel, so the chain's launches
+  // overlap the kernels before them.
   const bool status_next = status == reinterpret_cast<int*>(acc + K);
   const int64_t nz = K + (status_next ? 1 : 0);
-  k_zero_sums<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(nz, 256), 4 * lf.sms)), 256, 0,
-                st>>>(acc, nz);
-  e = cudaGetLastError();
+  e = launch_dependent(k_zero_sums, std::min<int64_t>(ceil_div(nz, 256), 4 * lf.sms), 256, 0, st,
+                       acc, nz);
   if (e != cudaSuccess) return e;
   return launch_dependent(k_stats_accumulate, grid, kStatThreads, kStatSmem, st, tmap, kchunks,
                           tboxes, units, acc, status);
@@ -411,7 +416,8 @@ cudaError_t launch_stats_finalize(const unsigned long long* acc, int64_t T, int6
                                   double* sX, const int* status, cudaStream_t st,
                                   unsigned long long* range) {
   // Launched behind the accumulation, which lets it start early; it waits.
-  return launch_dependent(k_stats_finalize, ceil_div(K, 256), 256, 0, st,
+  // 64-thread blocks spread the fp64 divisions over as many SMs as possible.
+  return launch_dependent(k_stats_finalize, ceil_div(K, 64), 64, 0, st,
                           static_cast<const unsigned long long*>(acc), T, K, sX, range, status);
 }
 

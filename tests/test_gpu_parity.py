@@ -308,6 +308,37 @@ def test_decode_product_x_through_l1(M, N, K, group, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("M,N,K,group,unaligned", [
+    (8, 300, 8192, 128, False), (6, 2048, 8192, 64, False), (7, 37, 8192, -1, False),
+    (5, 520, 12288, 128, False), (8, 17, 8192, 128, False), (8, 100, 9216, 128, False),
+    (8, 70, 8192, 64, True)])
+def test_decode_product_split_k(M, N, K, group, unaligned, bits):
+    """Up to 8 tokens, M x K fp16 too large for shared memory but half of it
+    fits (K a multiple of 1024): half the blocks take the first K/2 channels,
+    half the rest, over whole row tiles (2 row tiles upwards, ragged N; parameters by
+    TMA, by vector loads (72 groups per row), one by one (unaligned arrays),
+    and whole-row groups): within the bound, and identical on a second run."""
+    rng = workloads.weight_rng(M * 7 + N + K + group + bits)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group)
+    if unaligned:
+        zbuf = torch.zeros(z.numel() + 1, dtype=z.dtype, device=z.device)
+        zbuf[1:] = z.reshape(-1)
+        sbuf = torch.zeros(sc.numel() + 1, dtype=sc.dtype, device=sc.device)
+        sbuf[1:] = sc.reshape(-1)
+        z, sc = zbuf[1:], sbuf[1:]
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    xd = cuda(x)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, xd, group, bits=bits))
+    assert np.array_equal(y, host(awq.w4a16_matvec(codes, sc, z, N, K, xd, group, bits=bits)))
+    oc, osc, oz = O.quantize_groups(W, s, bits, group)
+    want = O.w4a16_matvec(oc, osc, oz, group, x)
+    err = np.abs(y.astype(np.float64) - want)
+    assert np.all(err <= _matvec_bound(oc, osc, oz, group, x) + 1e-30), float(err.max())
+
+
+@pytest.mark.parametrize("bits", [4, 3])
 def test_decode_product_unaligned_group_parameters(bits):
     """Zeros at an odd address and scales at 2 mod 4 (slices of larger
     buffers): 64-channel groups are then read one at a time (64-channel
@@ -560,7 +591,7 @@ def test_stage_timing_and_launch_count():
         ms = r.stage_ms()
         assert set(ms) == set(awq.STAGES) and all(v >= 0 for v in ms.values())
         assert ms["error_gemm"] > 0
-        assert r.kernel_launches == 7   # 2 stats, 1 scales, 1 residual, 1 GEMM, 1 loss, 1 final
+        assert r.kernel_launches == 8   # 3 stats, 1 scales, 1 residual, 1 GEMM, 1 loss, 1 final
         r.free()
     finally:
         awq.set_stage_timing(False)
