@@ -339,6 +339,28 @@ def test_decode_product_split_k(M, N, K, group, unaligned, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("N,K,group", [(18981, 1024, 128), (19000, 1152, 64),
+                                       (20000, 1280, -1)])
+def test_decode_product_many_tiles(M, N, K, group, bits):
+    """About 1200 row tiles of 16 over the SMs (ragged N; 8, 9 and 10 units
+    per row, so ranges start and end mid-tile; three group layouts, x staged
+    or split in halves): within the bound, and identical on a second run."""
+    rng = workloads.weight_rng(M * 11 + N + K + group + bits)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W), cuda(s), bits, group)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    xd = cuda(x)
+    y = host(awq.w4a16_matvec(codes, sc, z, N, K, xd, group, bits=bits))
+    assert np.array_equal(y, host(awq.w4a16_matvec(codes, sc, z, N, K, xd, group, bits=bits)))
+    oc, osc, oz = O.quantize_groups(W, s, bits, group)
+    want = O.w4a16_matvec(oc, osc, oz, group, x)
+    err = np.abs(y.astype(np.float64) - want)
+    assert np.all(err <= _matvec_bound(oc, osc, oz, group, x) + 1e-30), float(err.max())
+
+
+@pytest.mark.parametrize("bits", [4, 3])
 def test_decode_product_unaligned_group_parameters(bits):
     """Zeros at an odd address and scales at 2 mod 4 (slices of larger
     buffers): 64-channel groups are then read one at a time (64-channel
