@@ -259,6 +259,7 @@ int64_t awq_packed_words(int64_t N, int64_t K, int bits) {
 }
 
 awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stream) {
+  NvtxScope nvtx("awq_stats");
   if (T < 1) return fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
   if (T > kMaxStatTokens)
     return fail(AWQ_ERR_INVALID,
@@ -287,6 +288,7 @@ awq_status awq_stats(const void* X, int64_t T, int64_t K, double* sX, void* stre
 }
 
 awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s_out, void* stream) {
+  NvtxScope nvtx("awq_scales");
   if (K < 1 || K > (int64_t(1) << 31))
     return fail(AWQ_ERR_INVALID, "K=%lld", static_cast<long long>(K));
   if (n_grid < 1 || n_grid > kMaxGrid)
@@ -310,6 +312,7 @@ awq_status awq_scales(const double* sX, int64_t K, int n_grid, float* s_out, voi
 awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s_vec,
                              const awq_qconfig* cfg, uint32_t* codes, void* scales,
                              uint8_t* zeros, void* stream) {
+  NvtxScope nvtx("awq_quantize_pack");
   awq_status st;
   if ((st = check_cfg(cfg)) != AWQ_OK) return st;
   if (N < 0) return fail(AWQ_ERR_INVALID, "N=%lld", static_cast<long long>(N));
@@ -343,6 +346,7 @@ awq_status awq_quantize_pack(const void* W, int64_t N, int64_t K, const float* s
 
 awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bits, uint8_t* q,
                             void* stream) {
+  NvtxScope nvtx("awq_unpack_codes");
   if (awq_packed_words(N, K, bits) < 0)
     return fail(AWQ_ERR_INVALID, "invalid shape N=%lld K=%lld bits=%d",
                 static_cast<long long>(N), static_cast<long long>(K), bits);
@@ -359,6 +363,7 @@ awq_status awq_unpack_codes(const uint32_t* codes, int64_t N, int64_t K, int bit
 awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uint8_t* zeros,
                             int64_t N, int64_t K, const awq_qconfig* cfg, const void* x, int M,
                             float* y, void* stream) {
+  NvtxScope nvtx("awq_w4a16_matvec");
   awq_status st;
   if ((st = check_cfg(cfg)) != AWQ_OK) return st;
   if (N < 1 || N > (int64_t(1) << 31) || !k_fits(K, cfg) || K % 64 || K > (int64_t(1) << 31))
@@ -380,6 +385,7 @@ awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uin
 
 awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float* s_vec,
                           void* out, void* stream) {
+  NvtxScope nvtx("awq_fold_scale");
   if (rows < 1 || cols < 1 || rows > (int64_t(1) << 40) / cols)
     return fail(AWQ_ERR_INVALID, "rows=%lld cols=%lld (both >= 1)", static_cast<long long>(rows),
                 static_cast<long long>(cols));
@@ -397,6 +403,7 @@ awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float
 
 awq_status awq_reference_output(const void* W, int64_t N, const void* X, int64_t T, int64_t K,
                                 float* Y, int* status_dev, void* stream) {
+  NvtxScope nvtx("awq_reference_output");
   if (N < 1 || T < 1 || K < 64 || K % 64)
     return fail(AWQ_ERR_INVALID, "N=%lld T=%lld K=%lld (N, T >= 1; K a positive multiple of 64)",
                 static_cast<long long>(N), static_cast<long long>(T), static_cast<long long>(K));
@@ -583,7 +590,14 @@ static awq_status search_impl(const void* X, int64_t T, int64_t K, const double*
       AWQ_CUDA(cudaEventCreate(&r->ev[e]), "event creation");
     r->timed = true;
   }
+  // Each stage is also an NVTX range (stats, scales, residual, error_gemm,
+  // loss, final).
+  NvtxStages nvtx_stage;
+  static const char* const kStageNames[AWQ_NUM_STAGES] = {"stats", "scales", "residual",
+                                                          "error_gemm", "loss", "final"};
   auto mark = [&](int e) -> cudaError_t {
+    if (e < AWQ_NUM_STAGES) nvtx_stage.next(kStageNames[e]);
+    else nvtx_stage.close();
     return r->timed ? cudaEventRecord(r->ev[e], s) : cudaSuccess;
   };
   AWQ_CUDA(mark(AWQ_STAGE_STATS), "event record");
@@ -666,12 +680,14 @@ extern "C" {
 awq_status awq_search_layer(const void* X, int64_t T, int64_t K, const double* sX,
                             const awq_weight* Ws, int n_w, const awq_qconfig* cfg, void* stream,
                             awq_result** out) {
+  NvtxScope nvtx("awq_search_layer");
   return search_impl(X, T, K, sX, Ws, n_w, cfg, stream, out, false);
 }
 
 awq_status awq_search_layer_gram(const void* X, int64_t T, int64_t K, const double* sX,
                                  const awq_weight* Ws, int n_w, const awq_qconfig* cfg,
                                  void* stream, awq_result** out) {
+  NvtxScope nvtx("awq_search_layer_gram");
   return search_impl(X, T, K, sX, Ws, n_w, cfg, stream, out, true);
 }
 

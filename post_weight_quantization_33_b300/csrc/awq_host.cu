@@ -80,6 +80,7 @@ struct InFlight {
 
 extern "C" __attribute__((visibility("default"))) awq_status awq_search_host_layers(
     const awq_host_layer* layers, int n_layers, const awq_qconfig* cfg, void* stream) {
+  awq::NvtxScope nvtx("awq_search_host_layers");
   if (n_layers < 0 || (n_layers > 0 && layers == nullptr))
     return awq_internal_fail(AWQ_ERR_INVALID, "n_layers=%d with layers %s", n_layers,
                              layers ? "set" : "NULL");

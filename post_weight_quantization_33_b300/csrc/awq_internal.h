@@ -2,12 +2,49 @@
 // translation units.  Not part of the public interface.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace awq {
+
+// NVTX ranges on the host thread that enqueues the library's work: a tool
+// (Nsight Compute with --nvtx) attributes each kernel to the ranges open at
+// its launch, e.g. awq_search_layer/error_gemm.  With no tool attached a push
+// or pop does nothing.
+class NvtxScope {
+ public:
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
+
+// Sibling ranges in sequence: next() closes the open one and opens another.
+class NvtxStages {
+ public:
+  NvtxStages() = default;
+  ~NvtxStages() {
+    if (open_) nvtxRangePop();
+  }
+  void next(const char* name) {
+    close();
+    nvtxRangePushA(name);
+    open_ = true;
+  }
+  void close() {
+    if (open_) nvtxRangePop();
+    open_ = false;
+  }
+  NvtxStages(const NvtxStages&) = delete;
+  NvtxStages& operator=(const NvtxStages&) = delete;
+
+ private:
+  bool open_ = false;
+};
+
 
 // Device status codes written to the per-call status word.
 enum DeviceError : int {

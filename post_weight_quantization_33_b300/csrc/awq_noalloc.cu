@@ -89,6 +89,7 @@ awq_status awq_internal_cuda_fail(cudaError_t e, const char* what);
 
 extern "C" __attribute__((visibility("default"))) awq_status awq_stats_noalloc(
     const void* X, int64_t T, int64_t K, double* sX, void* stream) {
+  awq::NvtxScope nvtx("awq_stats_noalloc");
   if (T < 1)
     return awq_internal_fail(AWQ_ERR_INVALID, "T=%lld (must be >= 1)", static_cast<long long>(T));
   if (T > awq::kMaxStatTokens)
