@@ -81,3 +81,36 @@ def test_search_host_stream_failure_frees_in_flight_results():
     ref = awq.search_host(*layers[2], 4, 128)
     assert np.array_equal(got[2]["losses"], ref["losses"])
     assert torch.equal(got[2]["codes"][0], ref["codes"][0])
+
+
+def test_resumable_search_matches_host_stream(tmp_path):
+    """Checkpoint / resume: a run in chunks of two stores every layer; a
+    rerun reads them all back; after one file is removed only that layer is
+    searched again.  Every result equals the plain pipelined search's."""
+    from post_weight_quantization_33_b300 import checkpoint
+
+    layers = _layers()
+    ref = awq.search_host_stream(layers, 4, 128, 20)
+
+    def same(a, b):
+        assert a["best"] == b["best"] and a["alpha"] == b["alpha"]
+        assert np.array_equal(np.asarray(a["losses"]), np.asarray(b["losses"]))
+        assert np.array_equal(np.asarray(a["s"]), b["s"].numpy())
+        for key in ("codes", "scales", "zeros"):
+            for x, y in zip(a[key], b[key]):
+                assert np.array_equal(np.asarray(x), y.numpy())
+
+    first = checkpoint.search_layers_resumable(layers, str(tmp_path), 4, 128, 20, chunk=2)
+    assert not any(r["resumed"] for r in first)
+    again = checkpoint.search_layers_resumable(layers, str(tmp_path), 4, 128, 20, chunk=2)
+    assert all(r["resumed"] for r in again)
+    (tmp_path / "layer_00002.npz").unlink()
+    third = checkpoint.search_layers_resumable(layers, str(tmp_path), 4, 128, 20, chunk=2)
+    assert [r["resumed"] for r in third] == [True, True, False, True, True]
+    def host(v):
+        return v.numpy() if isinstance(v, torch.Tensor) else v
+
+    for runs in (first, again, third):
+        for r, g in zip(runs, ref):
+            same({k: [host(x) for x in v] if isinstance(v, list) else host(v)
+                  for k, v in r.items()}, g)
