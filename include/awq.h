@@ -380,6 +380,26 @@ awq_status awq_pool_usage(int64_t* used_bytes, int64_t* reserved_bytes);
  * Exists for testing the failure path without faulting the GPU. */
 awq_status awq_selftest_bounded_wait(int64_t limit_ns);
 
+/* The bounds-checked build: libawq_checked.so has the same interface and
+ * results, and in it the kernels of the statistic, scales, quantizers,
+ * decode product, losses and fold compare each computed global index with the
+ * extent of its buffer before the access; an out-of-range access is skipped
+ * and recorded (no trap).  A stand-in for a memory sanitizer, which is not
+ * available on every GPU host.
+ *   awq_bounds_checked : 1 in libawq_checked.so, 0 in libawq.so.
+ *   awq_bounds_report  : synchronises the current device and returns the
+ *     number of out-of-range accesses since the last reset (count) and the
+ *     first recorded one's check site, element index and buffer extent (-1
+ *     when count is 0); reset != 0 clears the records.  In libawq.so count is
+ *     always 0.  Any output pointer may be NULL. */
+int awq_bounds_checked(void);
+/* Bounds-checked build only: records one synthetic out-of-range index (site
+ * 0, index -1, extent 0) without touching memory, so that a test can see the
+ * record path work; AWQ_ERR_UNSUPPORTED in libawq.so. */
+awq_status awq_bounds_selftest(void);
+awq_status awq_bounds_report(int64_t* count, int* site, int64_t* index, int64_t* extent,
+                             int reset);
+
 #ifdef __cplusplus
 }
 #endif

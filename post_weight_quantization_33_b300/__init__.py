@@ -52,7 +52,7 @@ EXPORTED_SYMBOLS = (
     "awq_selftest_bounded_wait", "awq_result_kernel_launches", "awq_set_stage_timing",
     "awq_result_stage_ms", "awq_stats_noalloc", "awq_fold_scale", "awq_w4a16_matvec",
     "awq_search_layer_gram", "awq_search_host_layers", "awq_inject_allocation_failures",
-    "awq_pool_usage",
+    "awq_pool_usage", "awq_bounds_checked", "awq_bounds_report", "awq_bounds_selftest",
 )
 
 # Stage ids of awq_result_stage_ms (AWQ_STAGE_* in include/awq.h).
@@ -139,6 +139,10 @@ def lib() -> ctypes.CDLL:
                                         vp]),
         "awq_inject_allocation_failures": (None, [i32, i32]),
         "awq_pool_usage": (st, [ctypes.POINTER(i64), ctypes.POINTER(i64)]),
+        "awq_bounds_checked": (i32, []),
+        "awq_bounds_selftest": (st, []),
+        "awq_bounds_report": (st, [ctypes.POINTER(i64), ctypes.POINTER(i32), ctypes.POINTER(i64),
+                                   ctypes.POINTER(i64), i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -560,6 +564,18 @@ def set_stage_timing(enable: bool) -> None:
 
 def release_cached_memory() -> None:
     _check(lib().awq_release_cached_memory())
+
+
+def bounds_report(reset: bool = True) -> dict:
+    """Out-of-range accesses recorded by the bounds-checked build
+    (libawq_checked.so) since the last reset: ``count``, and the first one's
+    ``site``, ``index`` and ``extent``; ``checked`` is False (and the count 0)
+    for libawq.so."""
+    c, site, idx, ext = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().awq_bounds_report(ctypes.byref(c), ctypes.byref(site), ctypes.byref(idx),
+                                   ctypes.byref(ext), int(reset)))
+    return {"checked": bool(lib().awq_bounds_checked()), "count": c.value, "site": site.value,
+            "index": idx.value, "extent": ext.value}
 
 
 def selftest_bounded_wait(limit_ns: int = 20_000_000) -> int:

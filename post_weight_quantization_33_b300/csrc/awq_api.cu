@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "awq.h"
+#include "awq_bounds.cuh"
 #include "awq_internal.h"
 
 using namespace awq;
@@ -232,6 +233,16 @@ static void destroy_events(awq_result* r) {
   for (int e = 0; e <= AWQ_NUM_STAGES; ++e)
     if (r->ev[e]) cudaEventDestroy(r->ev[e]);
 }
+
+namespace awq {
+namespace {
+// One synthetic out-of-range index at site 0 (no memory access): shows the
+// record path of the bounds-checked build working.
+__global__ void k_bounds_selftest() { (void)in_bounds(kSiteSelfTest, -1, 0); }
+}  // namespace
+
+AWQ_BOUNDS_READER(bounds_api)
+}  // namespace awq
 
 extern "C" {
 
@@ -773,6 +784,50 @@ awq_status awq_pool_usage(int64_t* used_bytes, int64_t* reserved_bytes) {
     return cuda_fail(e, "pool attribute");
   *used_bytes = static_cast<int64_t>(used);
   *reserved_bytes = static_cast<int64_t>(reserved);
+  return ok();
+}
+
+awq_status awq_bounds_selftest(void) {
+#ifdef AWQ_CHECK_BOUNDS
+  NvtxScope nvtx("awq_bounds_selftest");
+  auto cleanup = [] {};
+  k_bounds_selftest<<<1, 1>>>();
+  AWQ_CUDA(cudaGetLastError(), "bounds self-test launch");
+  AWQ_CUDA(cudaDeviceSynchronize(), "device synchronisation");
+  return ok();
+#else
+  return fail(AWQ_ERR_UNSUPPORTED, "awq_bounds_selftest: not the bounds-checked build");
+#endif
+}
+
+int awq_bounds_checked(void) {
+#ifdef AWQ_CHECK_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+awq_status awq_bounds_report(int64_t* count, int* site, int64_t* index, int64_t* extent,
+                             int reset) {
+  NvtxScope nvtx("awq_bounds_report");
+  auto cleanup = [] {};
+  AWQ_CUDA(cudaDeviceSynchronize(), "device synchronisation");
+  typedef cudaError_t (*Reader)(BoundsRecord*, bool);
+  const Reader readers[] = {bounds_api,    bounds_stats,  bounds_quant,
+                            bounds_matvec, bounds_reduce, bounds_fold};
+  int64_t total = 0;
+  BoundsRecord first{0, -1, -1, -1};
+  for (Reader rd : readers) {
+    BoundsRecord rec{};
+    AWQ_CUDA(rd(&rec, reset != 0), "bounds record read");
+    if (rec.count != 0 && total == 0) first = rec;
+    total += static_cast<int64_t>(rec.count);
+  }
+  if (count) *count = total;
+  if (site) *site = static_cast<int>(first.site);
+  if (index) *index = first.index;
+  if (extent) *extent = first.extent;
   return ok();
 }
 

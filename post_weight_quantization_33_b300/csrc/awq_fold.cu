@@ -12,6 +12,7 @@
 // One HBM pass: 2 bytes read and 2 written per element.
 #include <algorithm>
 
+#include "awq_bounds.cuh"
 #include "awq_internal.h"
 
 namespace awq {
@@ -44,6 +45,9 @@ __global__ void __launch_bounds__(kFoldThreads)
   for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
     const float sr = __ldg(s + r);
     const int64_t base = r * cols + c0;
+    if (!in_bounds(kSiteFold, base + (VEC ? 8 : std::min<int64_t>(cols - c0, 8)) - 1,
+                   rows * cols))
+      continue;
     if (VEC) {
       const uint4 v = *reinterpret_cast<const uint4*>(V + base);
       uint4 o;
@@ -80,5 +84,7 @@ cudaError_t launch_fold(const __half* V, int64_t rows, int64_t cols, const float
     k_fold_rows<false><<<grid, kFoldThreads, 0, st>>>(V, rows, cols, s, out);
   return cudaGetLastError();
 }
+
+AWQ_BOUNDS_READER(bounds_fold)
 
 }  // namespace awq

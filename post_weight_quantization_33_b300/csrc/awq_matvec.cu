@@ -55,6 +55,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "awq_bounds.cuh"
 #include "awq_internal.h"
 #include "awq_ptx.cuh"
 
@@ -93,6 +94,11 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // product kernel start at once; the product waits for it (all of its writes
 // visible) before its first access to y.
 __device__ __forceinline__ void wait_for_zeroed_y() { grid_dependency_wait(); }
+
+// One fp32 addition into y[i] (y holds n = M x N values).
+__device__ __forceinline__ void add_y(float* y, int64_t i, int64_t n, float v) {
+  if (in_bounds(kSiteDecodeY, i, n)) atomicAdd(y + i, v);
+}
 
 __global__ void k_zero_y(float* __restrict__ y, int64_t n) {
   grid_dependents_launch();
@@ -232,9 +238,11 @@ __global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
     for (int q = threadIdx.x; q < M * per_tok; q += blockDim.x) {
       const int t = q / per_tok, r = q - t * per_tok;
       const int hc = r >> 2, cc = r & 3;
-      const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K +
-                                                        hc * kHalf + cc * 16);
-      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const int64_t xi = static_cast<int64_t>(t) * K + hc * kHalf + cc * 16;
+      const uint4* src = reinterpret_cast<const uint4*>(x + xi);
+      const bool xin = in_bounds(kSiteDecodeX, xi + 15, static_cast<int64_t>(M) * K);
+      const uint4 v0 = xin ? __ldg(src) : make_uint4(0, 0, 0, 0);
+      const uint4 v1 = xin ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
       const uint32_t X[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       uint32_t o[8];
 #pragma unroll
@@ -287,6 +295,13 @@ __global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
     };
     set_load_rows();
     auto load_next = [&](UnitWords<H>& u) {
+      if (!in_bounds(kSiteDecodeCodes, (pc1 - codes) + (H - 1) * kHalfWords + 1,
+                     N * words_per_row) ||
+          (GROUP != 0 && !in_bounds(kSiteDecodeParams, (pz1 - zeros) + kGroupsPerUnit - 1,
+                                    N * groups))) {
+        u = UnitWords<H>{};
+        return;
+      }
 #pragma unroll
       for (int h = 0; h < H; ++h) {
         if constexpr (BITS == 4) {
@@ -394,12 +409,12 @@ __global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
         for (int t = 0; t < NT; ++t) {
           const int m0 = t * 8 + 2 * c;
           if (r0 < N) {
-            if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
-            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
+            if (m0 < M) add_y(y, m0 * N + r0, static_cast<int64_t>(M) * N, acc[t][0]);
+            if (m0 + 1 < M) add_y(y, (m0 + 1) * N + r0, static_cast<int64_t>(M) * N, acc[t][1]);
           }
           if (r1 < N) {
-            if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
-            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
+            if (m0 < M) add_y(y, m0 * N + r1, static_cast<int64_t>(M) * N, acc[t][2]);
+            if (m0 + 1 < M) add_y(y, (m0 + 1) * N + r1, static_cast<int64_t>(M) * N, acc[t][3]);
           }
         }
       } else {
@@ -531,14 +546,14 @@ combine:
         const int64_t t = part_tile[w][s2];
         if (t < 0) continue;
         if (t != tl) {
-          if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+          if (tl >= 0 && tl * 16 + row < N && tok < M) add_y(y, tok * N + tl * 16 + row, static_cast<int64_t>(M) * N, sum);
           tl = t;
           sum = 0.f;
         }
         sum = __fadd_rn(sum, part_smem[w][s2][e]);
       }
     }
-    if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+    if (tl >= 0 && tl * 16 + row < N && tok < M) add_y(y, tok * N + tl * 16 + row, static_cast<int64_t>(M) * N, sum);
   }
 }
 
@@ -750,9 +765,11 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       const int hc = r >> 3, pos = r & 7;
       const int within = pos ^ ((t & 1) * 4);
       const int i = within >> 2, cc = within & 3;
-      const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K +
-                                                        part * kpart + hc * kHalf + cc * 16);
-      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const int64_t xi = static_cast<int64_t>(t) * K + part * kpart + hc * kHalf + cc * 16;
+      const uint4* src = reinterpret_cast<const uint4*>(x + xi);
+      const bool xin = in_bounds(kSiteDecodeX, xi + 15, static_cast<int64_t>(M) * K);
+      const uint4 v0 = xin ? __ldg(src) : make_uint4(0, 0, 0, 0);
+      const uint4 v1 = xin ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
       const uint32_t a0 = i ? v0.y : v0.x, a2 = i ? v0.w : v0.z;
       const uint32_t c0 = i ? v1.y : v1.x, c2 = i ? v1.w : v1.z;
       xs[q] = make_uint4(__byte_perm(a0, a2, 0x5410u), __byte_perm(c0, c2, 0x5410u),
@@ -782,6 +799,11 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
           sr1 = scales + l1 * groups;
         }
         const int64_t gi = static_cast<int64_t>(ubase + U) * kGPU;
+        if (!in_bounds(kSiteDecodeParams,
+                       min(static_cast<int64_t>(T) * 16 + g + 8, N - 1) * groups + gi +
+                           static_cast<int64_t>(nu == kStageUnits && vec ? GS : nu * kGPU) - 1,
+                       N * groups))
+          return;
         if (nu == kStageUnits && vec) {   // aligned: one load per row and array
           if constexpr (GS == 4) {
             p.z0[0] = __ldg(reinterpret_cast<const unsigned int*>(zr0 + gi));
@@ -890,12 +912,12 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         for (int t = 0; t < NT; ++t) {
           const int m0 = t * 8 + 2 * c;
           if (r0 < N) {
-            if (m0 < M) atomicAdd(y + m0 * N + r0, acc[t][0]);
-            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r0, acc[t][1]);
+            if (m0 < M) add_y(y, m0 * N + r0, static_cast<int64_t>(M) * N, acc[t][0]);
+            if (m0 + 1 < M) add_y(y, (m0 + 1) * N + r0, static_cast<int64_t>(M) * N, acc[t][1]);
           }
           if (r1 < N) {
-            if (m0 < M) atomicAdd(y + m0 * N + r1, acc[t][2]);
-            if (m0 + 1 < M) atomicAdd(y + (m0 + 1) * N + r1, acc[t][3]);
+            if (m0 < M) add_y(y, m0 * N + r1, static_cast<int64_t>(M) * N, acc[t][2]);
+            if (m0 + 1 < M) add_y(y, (m0 + 1) * N + r1, static_cast<int64_t>(M) * N, acc[t][3]);
           }
         }
       } else {
@@ -1131,14 +1153,14 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         const int64_t t = part_tile[2 * w + s2];
         if (t < 0) continue;
         if (t != tl) {
-          if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+          if (tl >= 0 && tl * 16 + row < N && tok < M) add_y(y, tok * N + tl * 16 + row, static_cast<int64_t>(M) * N, sum);
           tl = t;
           sum = 0.f;
         }
         sum = __fadd_rn(sum, part_all[(w * 2 + s2) * 16 * kTok + e]);
       }
     }
-    if (tl >= 0 && tl * 16 + row < N && tok < M) atomicAdd(y + tok * N + tl * 16 + row, sum);
+    if (tl >= 0 && tl * 16 + row < N && tok < M) add_y(y, tok * N + tl * 16 + row, static_cast<int64_t>(M) * N, sum);
   }
   if (*abort_flag) {
     // A wait expired: every output of the block's rows reads NaN.
@@ -1310,5 +1332,7 @@ cudaError_t launch_w4_matvec(const uint32_t* codes, const __half* scales, const 
                   : launch_wq<2, 3>(group, codes, scales, zeros, N, K, x, M, y, st);
   return cudaErrorInvalidValue;
 }
+
+AWQ_BOUNDS_READER(bounds_matvec)
 
 }  // namespace awq

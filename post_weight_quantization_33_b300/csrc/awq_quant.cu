@@ -24,6 +24,7 @@
 #include <type_traits>
 
 #include "awq_async.cuh"
+#include "awq_bounds.cuh"
 #include "awq_f32x2.cuh"
 #include "awq_internal.h"
 
@@ -297,11 +298,12 @@ __global__ void __launch_bounds__(kQuantThreads)
       const int64_t row0 = first + it * row_step;
 #pragma unroll
       for (int r = 0; r < kRowsPerLane; ++r) {   // a lone last row loads itself twice
-        const __half* src = W + min(row0 + r, N - 1) * K + kbase;
+        const int64_t w_off = min(row0 + r, N - 1) * K + kbase;
+        const __half* src = W + w_off;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int c = 32 * j + lane;
-          if (c < w_valid)
+          if (c < w_valid && in_bounds(kSiteResidualW, w_off + 8 * c + 7, N * K))
             cp_async16(ring_u32 + ((st * kRowsPerLane + r) * kRowChunks + fin_slot(c)) * 16,
                        src + 8 * c);
         }
@@ -316,6 +318,9 @@ __global__ void __launch_bounds__(kQuantThreads)
       const float* sp = s_grid + static_cast<int64_t>(a0 + a) * K + kbase;
       const float* rp = r_grid + static_cast<int64_t>(a0 + a) * K + kbase;
       for (int c = lane; c < s_valid; c += 32) {
+        if (!in_bounds(kSiteResidualS, static_cast<int64_t>(a0 + a) * K + kbase + 4 * c + 3,
+                       static_cast<int64_t>(n_alpha) * K))
+          continue;
         cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(
                        s_tile + a * kResSChunks + res_slot(c))), sp + 4 * c);
         cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(
@@ -369,7 +374,10 @@ __global__ void __launch_bounds__(kQuantThreads)
         if constexpr (GROUP == 0) {   // per-row groups: min / max of this grid point's rows
 #pragma unroll
           for (int r = 0; r < kRowsPerLane; ++r) {
-            const float2 m = rowmm[static_cast<int64_t>(ga) * N + min(row0 + r, N - 1)];
+            const int64_t im = static_cast<int64_t>(ga) * N + min(row0 + r, N - 1);
+            const float2 m = in_bounds(kSiteResidualRowmm, im, static_cast<int64_t>(n_alpha) * N)
+                                 ? rowmm[im]
+                                 : make_float2(0.f, 0.f);
             mn[r] = m.x;
             mx[r] = m.y;
           }
@@ -438,7 +446,11 @@ __global__ void __launch_bounds__(kQuantThreads)
             const __half2 hv = __floats2half2_rn(lo2(e), hi2(e));
             o[i / 2] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-          if (lw.active && row0 + r < N) st_v8(dst + r * K, o);
+          if (lw.active && row0 + r < N &&
+              in_bounds(kSiteResidualOut,
+                        static_cast<int64_t>(ga) * slab + (row_off + row0 + r) * K + lw.k0 + 15,
+                        static_cast<int64_t>(n_alpha) * slab))
+            st_v8(dst + r * K, o);
         }
       }
     }
@@ -499,11 +511,12 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
       const int64_t row0 = first + it * row_step;
 #pragma unroll
       for (int r = 0; r < kRowsPerLane; ++r) {   // a lone last row loads itself twice
-        const __half* src = W + min(row0 + r, N - 1) * K + kbase;
+        const int64_t w_off = min(row0 + r, N - 1) * K + kbase;
+        const __half* src = W + w_off;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int c = 32 * j + lane;
-          if (c < valid)
+          if (c < valid && in_bounds(kSiteFinalW, w_off + 8 * c + 7, N * K))
             cp_async16(ring_u32 + ((st * kRowsPerLane + r) * kRowChunks + fin_slot(c)) * 16,
                        src + 8 * c);
         }
@@ -600,7 +613,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
         }
         c0 -= base * 0x11111111u;
         c1 -= base * 0x11111111u;
-        if (store) {
+        if (store && in_bounds(kSiteFinalCodes, row * words + 2 * lw.lc + 1, N * words)) {
           uint32_t* dst = crow + 2 * lw.lc;
           if (codes8) {
             *reinterpret_cast<uint2*>(dst) = make_uint2(c0, c1);
@@ -623,7 +636,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
         for (int i = 14; i >= 11; --i) hi16 = hi16 * 8u + b[i];
         hi16 = (hi16 - base * 0x00001249u) * 2u + ((b[10] - base) >> 2);
         const uint32_t next_lo = __shfl_down_sync(0xFFFFFFFFu, lo32, 1);
-        if (store) {
+        if (store && in_bounds(kSiteFinalCodes, row * words + (lw.lc >> 1) * 3 + 2, N * words)) {
           uint32_t* dst = crow + (lw.lc >> 1) * 3;
           if ((lane & 1) == 0) {
             dst[0] = lo32;
@@ -643,7 +656,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
         group_lead = (lane % (GROUP / kPerLane)) == 0;
         gi = row * groups + lw.k0 / GROUP;
       }
-      if (store && group_lead) {
+      if (store && group_lead && in_bounds(kSiteFinalParams, gi, N * groups)) {
         scales[gi] = g.scale;
         zeros[gi] = static_cast<uint8_t>(__float2uint_rn(g.z));
       }
@@ -831,5 +844,7 @@ cudaError_t launch_unpack(const uint32_t* codes, int64_t N, int64_t K, int bits,
              kQuantThreads, 0, st>>>(codes, N, K, bits, q);
   return cudaGetLastError();
 }
+
+AWQ_BOUNDS_READER(bounds_quant)
 
 }  // namespace awq

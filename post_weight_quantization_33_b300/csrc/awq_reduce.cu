@@ -7,6 +7,7 @@
 // the per-row sums over token tiles, which are compensated fp32 (about 2^-48
 // relative) because this part has little fp64 throughput.  The argmin takes
 // the first minimum and treats NaN as +inf.
+#include "awq_bounds.cuh"
 #include "awq_internal.h"
 
 namespace awq {
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(kLossRows)
     }
     row = static_cast<double>(s) + static_cast<double>(c);
     if (row_scale != nullptr) row *= *row_scale;
-    row_losses[static_cast<int64_t>(a) * n_total + map.cum[w] + n] = row;
+    const int64_t ri = static_cast<int64_t>(a) * n_total + map.cum[w] + n;
+    if (in_bounds(kSiteLosses, ri, static_cast<int64_t>(n_grid) * n_total)) row_losses[ri] = row;
   }
   // Per-weight chunk sums (a chunk of 256 rows meets at most a few weights).
   const int64_t v0 = static_cast<int64_t>(c) * kLossRows;
@@ -142,5 +144,7 @@ cudaError_t launch_loss_reduce(const float* partials, int n_alpha, int n_tiles, 
                                        counter, row_scale, status);
   return cudaGetLastError();
 }
+
+AWQ_BOUNDS_READER(bounds_reduce)
 
 }  // namespace awq

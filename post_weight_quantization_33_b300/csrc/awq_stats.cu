@@ -14,6 +14,7 @@
 // mean of such a channel is +inf or NaN, as an IEEE fp64 sum would give it.
 #include <algorithm>
 
+#include "awq_bounds.cuh"
 #include "awq_f32x2.cuh"
 #include "awq_internal.h"
 #include "awq_ptx.cuh"
@@ -144,6 +145,7 @@ __device__ __forceinline__ bool flush_slab(LaneSums& a, int64_t slab, int64_t kc
 #pragma unroll
       for (int w = 0; w < kStatWarps; ++w) sum += sm.red[w][j][lane];
       const uint32_t fj = (f >> (2 * j)) & 3u;
+      if (!in_bounds(kSiteStatsAcc, chunk * 8 + j, kchunks * 8)) continue;
       if (fj) atomicOr(acc + chunk * 8 + j, (fj & 2u) ? kFlagNan : kFlagInf);
       else if (sum) atomicAdd(acc + chunk * 8 + j, sum);
     }
@@ -315,7 +317,7 @@ __global__ void k_stats_finalize(const unsigned long long* __restrict__ acc, int
   grid_dependency_wait();   // the accumulation, which this kernel may overlap, is complete
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   double v = 0.0;
-  if (k < K) {
+  if (k < K && in_bounds(kSiteStatsOut, k, K)) {
     const unsigned long long w = acc[k];
     if ((status != nullptr && *status != 0) || (w & kFlagNan)) v = __longlong_as_double(0x7FF8000000000000ll);
     else if (w & kFlagInf) v = __longlong_as_double(0x7FF0000000000000ll);
@@ -365,8 +367,11 @@ __global__ void k_scales(const double* __restrict__ sX, int64_t K, int n_grid,
   double u = 1.0;
   for (int a = 0; a < n_grid; ++a) {
     const float sv = __double2float_rn(u);
-    s[static_cast<int64_t>(a) * K + k] = sv;
-    if (r != nullptr) r[static_cast<int64_t>(a) * K + k] = __frcp_rn(sv);
+    const int64_t i = static_cast<int64_t>(a) * K + k;
+    if (in_bounds(kSiteScalesOut, i, static_cast<int64_t>(n_grid) * K)) {
+      s[i] = sv;
+      if (r != nullptr) r[i] = __frcp_rn(sv);
+    }
     u *= e;
   }
 }
@@ -435,5 +440,7 @@ cudaError_t launch_scales(const double* sX, int64_t K, int n_grid,
   k_scales<<<static_cast<unsigned>(ceil_div(K, 32)), 32, 0, st>>>(sX, K, n_grid, range, s, r);
   return cudaGetLastError();
 }
+
+AWQ_BOUNDS_READER(bounds_stats)
 
 }  // namespace awq

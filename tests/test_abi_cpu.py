@@ -36,6 +36,19 @@ def test_library_exports_every_declared_symbol(L):
         assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
 
 
+def test_bounds_checked_build_exports_the_same_interface(L):
+    """libawq_checked.so (the same sources with -DAWQ_CHECK_BOUNDS) loads and
+    exports every declared symbol; awq_bounds_checked tells the two apart, and
+    the report of the normal build is empty (no GPU needed for either)."""
+    path = awq_build.build(checked=True)
+    C = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(C, name), name
+    assert C.awq_bounds_checked() == 1
+    assert L.awq_bounds_checked() == 0
+    assert L.awq_bounds_selftest() == awq.AWQ_ERR_UNSUPPORTED
+
+
 def test_no_oracle_in_library_sources():
     csrc = os.path.join(ROOT, "post_weight_quantization_33_b300")
     for dirpath, _, files in os.walk(csrc):
