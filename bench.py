@@ -226,6 +226,33 @@ def cpu_baseline(data, wl, rows: int, steps: int = 2) -> dict:
             "sample": oracle_sample(rows, pool) + f"; {steps} timed steps, {dt:.1f} s"}
 
 
+def settle_clocks(gpu_id: str, max_s: float = 5.0) -> dict:
+    """Wait (at most max_s) until the SM clock is back within 5 % of its
+    maximum with no power-cap throttling: the power governor lags a heavy
+    phase by a second or more, and the HBM-bound calls timed next are partly
+    issue-bound, so they would be timed at the previous phase's capped clock
+    (measured: the statistic 46 us instead of 28 right after the 70B-class
+    searches, 28.0 again after a 3 s pause).  Returns the wait and the clock
+    it ended at; without nvidia-smi, waits max_s / 2."""
+    q = "clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap"
+    t0 = time.perf_counter()
+    last = None
+    while True:
+        try:
+            out = subprocess.run(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                  "-i", gpu_id], capture_output=True, text=True, timeout=10)
+            sm, smax, cap = [v.strip() for v in out.stdout.strip().split(",")[:3]]
+            last = {"sm_mhz": float(sm), "sm_max_mhz": float(smax), "sw_power_cap": cap}
+        except (OSError, ValueError, subprocess.SubprocessError):
+            time.sleep(max_s / 2)
+            return {"waited_s": round(time.perf_counter() - t0, 2), "clocks": "nvidia-smi unavailable"}
+        ok = last["sm_mhz"] >= 0.95 * last["sm_max_mhz"] and last["sw_power_cap"] != "Active"
+        waited = time.perf_counter() - t0
+        if ok or waited >= max_s:
+            return {"waited_s": round(waited, 2), "settled": ok, **last}
+        time.sleep(0.2)
+
+
 def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 5) -> dict:
     """Achieved HBM bandwidth of the HBM-bound entry points at the largest
     workload's sizes (X 8192x8192; W 28672x8192), called through the C ABI
@@ -638,7 +665,9 @@ def run_awq(args, rank: int, world: int, local_rank: int) -> None:
                     for c in wl.calls for w in c.ws)
     line["dequant_mainloop_bound"] = dequant_mainloop_bound(
         calls, flush, {k: v / args.steps for k, v in stage_sum.items()}, total_ms / args.steps)
+    settle = settle_clocks(gpu_id)
     line["hbm_kernels"] = hbm_kernels(dev, flush, pk["hbm_gbs"])
+    line["hbm_kernels"]["clock_settle"] = settle
     line["hbm_kernels"]["residual"] = {
         "shape": "this workload, every grid point", "ms": res_ms, "bytes": res_bytes,
         "gbs": res_bytes / res_ms / 1e6, "frac": res_bytes / res_ms / 1e6 / pk["hbm_gbs"]}
