@@ -205,8 +205,11 @@ awq_status awq_fold_scale(const void* V, int64_t rows, int64_t cols, const float
  *            (code - zero) * x is exact, the sums are fp32 on the tensor cores
  *            (mma.sync, fp16 operands), and each group's sum is scaled in fp32.
  *            Deterministic: run-to-run identical.
- * K % 64 == 0 and K % group == 0.  Allocates nothing (y is zeroed on the
- * stream by a kernel the product is launched behind, then accumulated).  K % 128 == 0 streams the codes through TMA
+ * K % 64 == 0 and K % group == 0.  Allocates nothing: y is zeroed on the
+ * stream by a small kernel, then accumulated; both kernels are launched with
+ * programmatic dependent launch behind the stream's previous kernel and wait
+ * for it before touching y or reading x, so inputs written by the kernel
+ * just before the call are seen.  K % 128 == 0 streams the codes through TMA
  * (a device wait bounded at 2 s: if one expires, the outputs of the rows
  * concerned read NaN); other K read them with plain loads. */
 awq_status awq_w4a16_matvec(const uint32_t* codes, const void* scales, const uint8_t* zeros,

@@ -208,10 +208,10 @@ EncodeTiledFn tensor_map_encoder();
 // the stream's previous kernel ends, and must call grid_dependency_wait()
 // before it touches anything that kernel writes.
 template <typename Kern, typename... Args>
-cudaError_t launch_dependent(Kern kern, int64_t blocks, int threads, int64_t smem,
-                             cudaStream_t st, Args... args) {
+cudaError_t launch_dependent(Kern kern, dim3 grid, int threads, int64_t smem, cudaStream_t st,
+                             Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = st;
@@ -221,6 +221,12 @@ cudaError_t launch_dependent(Kern kern, int64_t blocks, int threads, int64_t sme
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(Kern kern, int64_t blocks, int threads, int64_t smem,
+                             cudaStream_t st, Args... args) {
+  return launch_dependent(kern, dim3(static_cast<unsigned>(blocks)), threads, smem, st, args...);
 }
 
 }  // namespace awq

@@ -90,9 +90,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Programmatic dependent launch: y is zeroed by k_zero_y, which lets the
-// product kernel start at once; the product waits for it (all of its writes
-// visible) before its first access to y.
+// Programmatic dependent launch: k_zero_y is launched behind the stream's
+// previous kernel and the product behind k_zero_y, so both are resident early
+// and start as soon as their predecessor ends (no launch gap between calls).
+// k_zero_y waits for the previous kernel before it writes y (that kernel may
+// still read it); the product waits for k_zero_y, and so for everything
+// before it, before its first load (x, codes and parameters may come from
+// the kernel before) and its first access to y.
 __device__ __forceinline__ void wait_for_zeroed_y() { grid_dependency_wait(); }
 
 // One fp32 addition into y[i] (y holds n = M x N values).
@@ -102,6 +106,7 @@ __device__ __forceinline__ void add_y(float* y, int64_t i, int64_t n, float v) {
 
 __global__ void k_zero_y(float* __restrict__ y, int64_t n) {
   grid_dependents_launch();
+  grid_dependency_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     y[i] = 0.f;
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
   const int64_t i1 = b0 + (b1 - b0) * (warp + 1) / nwarps;
   const int64_t words_per_row = K * BITS / 32;
   const int64_t groups = GROUP ? K / GROUP : 1;
+  wait_for_zeroed_y();
 
   if constexpr (XPERM) {
     // Item q: token t, half hc, quad slot cc (channels 64 hc + 16 cc .. + 15).
@@ -262,7 +268,6 @@ __global__ void __launch_bounds__(block_warps<NT, XPERM>() * 32, 1)
     part_tile[warp][1] = -1;
   }
   __syncthreads();
-  wait_for_zeroed_y();
   if (i0 >= i1) goto combine;
   {
     // The first code word of this thread in a half: INT4 words 2c, 2c+1;
@@ -576,8 +581,8 @@ combine:
 // byte permute (0x64 | z in both halves is 1024 + z) and fp16 subtractions.
 // A group's first MMA starts from a zero accumulator.  y is zeroed by
 // k_zero_y, which the product is launched behind (programmatic dependent
-// launch: the product stages x and issues its first copies at once, and
-// waits for the zeroing only before its main loop).
+// launch, both chained to the stream's previous kernel: see
+// wait_for_zeroed_y).
 constexpr int kStageUnits = 4;        // 128-channel units per stage
 constexpr int kBoxBytes = 2048;       // one box: 16 rows x (INT4 128, INT3 96) bytes
 constexpr int kSlotBytes = 2 * kBoxBytes;
@@ -750,6 +755,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     }
     ++issued;
   };
+  wait_for_zeroed_y();
   // The first S stages go out before x is staged.
   for (int s = 0; s < S && pleft > 0; ++s) produce(s);
 
@@ -777,7 +783,6 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     }
   }
   __syncthreads();
-  wait_for_zeroed_y();
   bool failed = false;
   if (i0 < i1) {
     // Group parameters: row pointers of one tile (cached) and the loads of a
@@ -1261,11 +1266,11 @@ template <int NT, int BITS>
 cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
                       const uint8_t* zeros, int64_t N, int64_t K, const __half* x, int M,
                       float* y, cudaStream_t st) {
-  // y is zeroed by a kernel that lets the product start behind it.
+  // y is zeroed by a kernel launched behind the stream's previous kernel,
+  // and the product is launched behind it (see wait_for_zeroed_y).
   const int64_t ny = static_cast<int64_t>(M) * N;
-  k_zero_y<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(ny, 256), 4 * device_sm_count())),
-             256, 0, st>>>(y, ny);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(
+      k_zero_y, std::min<int64_t>(ceil_div(ny, 256), 4 * device_sm_count()), 256, 0, st, y, ny);
   if (e != cudaSuccess) return e;
   // One block per SM, at most one per 16-row tile (every block's range is
   // then at least a tile long: at most two blocks add into an output).

@@ -27,6 +27,7 @@
 #include "awq_bounds.cuh"
 #include "awq_f32x2.cuh"
 #include "awq_internal.h"
+#include "awq_ptx.cuh"
 
 namespace awq {
 namespace {
@@ -488,6 +489,10 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
                   uint32_t* __restrict__ codes, __half* __restrict__ scales,
                   uint8_t* __restrict__ zeros, bool codes8, const float2* __restrict__ rowmm) {
   extern __shared__ uint4 fin_ring[];
+  // Launched behind the stream's previous kernel (the chosen grid point, W
+  // and s may come from it).
+  grid_dependency_wait();
+  grid_dependents_launch();
   constexpr int LEVELS = (1 << BITS) - 1;
   const float L = static_cast<float>(LEVELS);
   const int64_t groups = GROUP == 0 ? 1 : K / (GROUP == 0 ? 1 : GROUP);
@@ -675,6 +680,8 @@ __global__ void __launch_bounds__(256)
                  const float* __restrict__ s_grid, const int* __restrict__ sel, int n_alpha,
                  float2* __restrict__ rowmm) {
   __shared__ float smn[8], smx[8];
+  grid_dependency_wait();   // launched behind the stream's previous kernel
+  grid_dependents_launch();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
     const uint4* wr = reinterpret_cast<const uint4*>(W + row * K);
@@ -760,8 +767,8 @@ cudaError_t launch_final(const __half* W, int64_t N, int64_t K, const float* s, 
   const cudaError_t e = one_wave_grid(reinterpret_cast<const void*>(kern), kFinSmem, N, K, &grid);
   if (e != cudaSuccess) return e;
   const bool c8 = (reinterpret_cast<uintptr_t>(codes) % 8) == 0;
-  kern<<<grid, kQuantThreads, kFinSmem, st>>>(W, N, K, s, sel, codes, scales, zeros, c8, rowmm);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, kQuantThreads, kFinSmem, st, W, N, K, s, sel, codes, scales,
+                          zeros, c8, rowmm);
 }
 
 template <int BITS, bool SYM>
@@ -779,8 +786,8 @@ cudaError_t launch_row_minmax(const __half* W, int64_t N, int64_t K, const float
                               const int* sel, int n_alpha, float2* rowmm, cudaStream_t st) {
   const unsigned grid =
       static_cast<unsigned>(std::min<int64_t>(N, static_cast<int64_t>(device_sm_count()) * 8));
-  k_row_minmax<<<grid, 256, 0, st>>>(W, N, K, s_grid, sel, n_alpha, rowmm);
-  return cudaGetLastError();
+  return launch_dependent(k_row_minmax, static_cast<int64_t>(grid), 256, 0, st, W, N, K, s_grid,
+                          sel, n_alpha, rowmm);
 }
 
 template <int GROUP, bool SYM>
