@@ -633,3 +633,43 @@ def test_bad_pointers_rejected_on_gpu():
     sx = torch.empty(128, dtype=torch.float64, device="cuda")
     host_buf = np.ones((8, 128), np.float16)
     assert L.awq_stats(host_buf.ctypes.data, 8, 128, sx.data_ptr(), None) == awq.AWQ_ERR_INVALID
+
+
+# --------------------------------------------------------------------------
+# Programmatic dependent launch: the calls chain their kernels to the
+# stream's previous kernel and wait for it before reading their inputs, so an
+# input written by the kernel just before the call must be seen.
+# --------------------------------------------------------------------------
+def test_inputs_written_just_before_the_call_are_seen():
+    rng = workloads.weight_rng(909)
+    N, K = 520, 8192
+    W0 = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    codes, sc, z = awq.quantize_pack(cuda(W0), cuda(s), 4, 128)
+    oc, osc, oz = O.quantize_groups(W0, s, 4, 128)
+    big = torch.randn(64 << 20, device="cuda")          # a long producer kernel before each call
+    for it in range(6):
+        x_host = rng.standard_normal((1 + it % 3, K)).astype(np.float16)
+        src = cuda(x_host)
+        x = torch.empty_like(src)
+        big.mul_(1.0)                                     # keeps the stream busy
+        x.copy_(src)                                      # the producer of x, just before the call
+        y = host(awq.w4a16_matvec(codes, sc, z, N, K, x, 128))
+        want = O.w4a16_matvec(oc, osc, oz, 128, x_host)
+        err = np.abs(y.astype(np.float64) - want)
+        assert np.all(err <= _matvec_bound(oc, osc, oz, 128, x_host) + 1e-30), it
+    # quantize + pack of a weight written by the previous kernel
+    Wd = torch.empty(N, K, dtype=torch.float16, device="cuda")
+    src = cuda(W0)
+    big.mul_(1.0)
+    Wd.copy_(src)
+    c2, s2, z2 = awq.quantize_pack(Wd, cuda(s), 4, 128)
+    assert np.array_equal(words_u32(c2), words_u32(codes))
+    assert np.array_equal(host(s2).view(np.uint16), host(sc).view(np.uint16))
+    # the statistic of activations written by the previous kernel
+    X0 = (rng.standard_normal((4096, 1024)) * 3).astype(np.float16)
+    Xd = torch.empty(4096, 1024, dtype=torch.float16, device="cuda")
+    srcx = cuda(X0)
+    big.mul_(1.0)
+    Xd.copy_(srcx)
+    assert np.array_equal(host(awq.stats(Xd)), O.channel_magnitude(X0))
