@@ -673,6 +673,13 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int g = lane >> 2, c = lane & 3;
+  // The box row that MMA row g takes (row g + 8 takes gr + 8).  INT4 boxes
+  // are 128-byte swizzled (16-byte chunk j of row r stored at j ^ (r & 7)),
+  // so the 8-byte code loads of lanes 0-15 (g = 0..3) cover all 32 banks
+  // when they read rows 0, 2, 4, 6, and only 16 of them (two wavefronts per
+  // half-warp) when they read rows 0..3.  INT3 rows (96 bytes, unswizzled)
+  // keep g.
+  const int gr = BITS == 4 ? ((g & 3) << 1) | (g >> 2) : g;
   constexpr int kRowBytes = box_row_bytes<BITS>();
   constexpr int kUnitBytes = 16 * BITS;               // bytes of a row per 128-channel unit
   constexpr int kTok = 8 * NT;
@@ -796,8 +803,8 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       if constexpr (GROUP != 0) {
         if (T != prow_tile) {
           prow_tile = T;
-          const int64_t l0 = min(static_cast<int64_t>(T) * 16 + g, N - 1);
-          const int64_t l1 = min(static_cast<int64_t>(T) * 16 + g + 8, N - 1);
+          const int64_t l0 = min(static_cast<int64_t>(T) * 16 + gr, N - 1);
+          const int64_t l1 = min(static_cast<int64_t>(T) * 16 + gr + 8, N - 1);
           zr0 = zeros + l0 * groups;
           zr1 = zeros + l1 * groups;
           sr0 = scales + l0 * groups;
@@ -805,7 +812,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         }
         const int64_t gi = static_cast<int64_t>(ubase + U) * kGPU;
         if (!in_bounds(kSiteDecodeParams,
-                       min(static_cast<int64_t>(T) * 16 + g + 8, N - 1) * groups + gi +
+                       min(static_cast<int64_t>(T) * 16 + gr + 8, N - 1) * groups + gi +
                            static_cast<int64_t>(nu == kStageUnits && vec ? GS : nu * kGPU) - 1,
                        N * groups))
           return;
@@ -856,8 +863,8 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     float rsf0 = 0.f, rsf1 = 0.f;
     auto set_rows = [&]() {
       if constexpr (GROUP == 0) {
-        const int64_t l0 = min(static_cast<int64_t>(tile) * 16 + g, N - 1);
-        const int64_t l1 = min(static_cast<int64_t>(tile) * 16 + g + 8, N - 1);
+        const int64_t l0 = min(static_cast<int64_t>(tile) * 16 + gr, N - 1);
+        const int64_t l1 = min(static_cast<int64_t>(tile) * 16 + gr + 8, N - 1);
         rz0 = zero_pairs_from_p<BITS>(magic_pair_of_byte(__ldg(zeros + l0), 0));
         rz1 = zero_pairs_from_p<BITS>(magic_pair_of_byte(__ldg(zeros + l1), 0));
         rsf0 = __half2float(__ldg(scales + l0));
@@ -880,17 +887,17 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         xb[t] = xa[t] + 1;
       }
     }
-    // Byte offsets of this thread's code words in a box, for row g (row
-    // g + 8 is 8 rows further), per (unit of the box, half): INT4, its 8
+    // Byte offsets of this thread's code words in a box, for row gr (row
+    // gr + 8 is 8 rows further), per (unit of the box, half): INT4, its 8
     // bytes in the swizzled layout; INT3, the first of its two words.
     uint32_t coff[4];
 #pragma unroll
     for (int uh = 0; uh < 4; ++uh) {
       if constexpr (BITS == 4) {
-        const uint32_t chunk = ((static_cast<uint32_t>(uh) ^ (g >> 1)) << 1) | ((c >> 1) ^ (g & 1));
-        coff[uh] = g * kRowBytes + chunk * 16 + (c & 1) * 8;
+        const uint32_t chunk = ((static_cast<uint32_t>(uh) << 1) | (c >> 1)) ^ gr;
+        coff[uh] = gr * kRowBytes + chunk * 16 + (c & 1) * 8;
       } else {
-        coff[uh] = g * kRowBytes + (uh >> 1) * kUnitBytes + (uh & 1) * 24 + 4 * ((3 * c) / 2);
+        coff[uh] = gr * kRowBytes + (uh >> 1) * kUnitBytes + (uh & 1) * 24 + 4 * ((3 * c) / 2);
       }
     }
     const bool odd = c & 1;
@@ -912,7 +919,7 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
         }
       }
       if (tile_u0 == 0 && end == upr) {
-        const int64_t r0 = static_cast<int64_t>(tile) * 16 + g, r1 = r0 + 8;
+        const int64_t r0 = static_cast<int64_t>(tile) * 16 + gr, r1 = r0 + 8;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int m0 = t * 8 + 2 * c;
@@ -931,10 +938,10 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int m0 = t * 8 + 2 * c;
-          ps[g * kTok + m0] = acc[t][0];
-          ps[g * kTok + m0 + 1] = acc[t][1];
-          ps[(g + 8) * kTok + m0] = acc[t][2];
-          ps[(g + 8) * kTok + m0 + 1] = acc[t][3];
+          ps[gr * kTok + m0] = acc[t][0];
+          ps[gr * kTok + m0 + 1] = acc[t][1];
+          ps[(gr + 8) * kTok + m0] = acc[t][2];
+          ps[(gr + 8) * kTok + m0 + 1] = acc[t][3];
         }
         if (lane == 0) part_tile[2 * warp + slot] = tile;
       }
@@ -1039,15 +1046,15 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       }
     };
 
-    // PT: the stage's group parameters from its parameter boxes (rows g and
-    // g + 8; box rows of 16 bytes: zeros of groups (gz & ~15) + 0..15, scales
+    // PT: the stage's group parameters from its parameter boxes (rows gr and
+    // gr + 8; box rows of 16 bytes: zeros of groups (gz & ~15) + 0..15, scales
     // of groups (gz & ~7) + 0..7).
     auto smem_params = [&](StageParams<GS>& p, int slot, int U, int n) {
       if constexpr (PT && GROUP != 0) {
         const uint32_t pz = pring_w + slot * kParamSlotBytes, ps = pz + kParamSlotBytes / 2;
         const int gz = (ubase + U) * kGPU, bz = gz & 15, bs = gz & 7;
-        const uint32_t rz0 = pz + g * 16, rz1 = pz + (g + 8) * 16;
-        const uint32_t rs0 = ps + g * 16, rs1 = ps + (g + 8) * 16;
+        const uint32_t rz0 = pz + gr * 16, rz1 = pz + (gr + 8) * 16;
+        const uint32_t rs0 = ps + gr * 16, rs1 = ps + (gr + 8) * 16;
         if (n == kStageUnits) {
           if constexpr (GS == 4) {
             asm volatile("ld.shared.u32 %0, [%1];" : "=r"(p.z0[0]) : "r"(rz0 + bz));
