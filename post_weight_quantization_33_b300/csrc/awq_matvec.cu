@@ -37,8 +37,10 @@
 // permuted so that a thread's B fragments for the four MMAs of a half are two
 // 16-byte loads (no byte permutes in the loop); for odd tokens the two
 // 64-byte halves of the staged 128 bytes are swapped, so the quads of a warp
-// (8 tokens) spread over all 32 banks.  Otherwise x is read through L1 and
-// its B fragments are formed by byte permutes.
+// (8 tokens) spread over all 32 banks.  When only half of it fits (and K is
+// a multiple of 1024), the grid is cut in two halves of K, each block staging
+// its half (k_wq_tma).  Otherwise x is read through L1 and its B fragments
+// are formed by byte permutes.
 //
 // Work split.  One block of 16 warps per SM (8 for 16 tokens, or x read
 // through L1).  The (row tile, unit) items, tile-major, are cut into equal
@@ -772,21 +774,56 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     // 2i + 1 of quad slot cc: {x[j], x[j+4]} and {x[8+j], x[12+j]} of the
     // slot's 16 channels 64 hc + 16 cc + (0..15).  One chunk per thread,
     // consecutive threads writing consecutive chunks.
+    //
+    // In the 9-16 token and K-split kernels the loads of kXBatch chunks per
+    // thread are all issued before the first is used: at 16 tokens with the
+    // K split a thread stages 32 chunks, and staged one at a time, each
+    // waiting for its own loads, they made the split slower than reading x
+    // through L1.  Chunks past the last whole batch go one at a time.  (The
+    // one-token kernel stages 2 chunks per thread; compiled into it, the
+    // batch loop cost INT3 1.2 us though it never ran.)
     const int per_tok = hcs * 8;
-    for (int q = threadIdx.x; q < M * per_tok; q += blockDim.x) {
+    const int nchunks = M * per_tok;
+    const int nthreads = static_cast<int>(blockDim.x);
+    auto chunk_src = [&](int q, int& i) -> const uint4* {
       const int t = q / per_tok, r = q - t * per_tok;
       const int hc = r >> 3, pos = r & 7;
       const int within = pos ^ ((t & 1) * 4);
-      const int i = within >> 2, cc = within & 3;
+      i = within >> 2;
+      const int cc = within & 3;
       const int64_t xi = static_cast<int64_t>(t) * K + part * kpart + hc * kHalf + cc * 16;
-      const uint4* src = reinterpret_cast<const uint4*>(x + xi);
-      const bool xin = in_bounds(kSiteDecodeX, xi + 15, static_cast<int64_t>(M) * K);
-      const uint4 v0 = xin ? __ldg(src) : make_uint4(0, 0, 0, 0);
-      const uint4 v1 = xin ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+      return in_bounds(kSiteDecodeX, xi + 15, static_cast<int64_t>(M) * K)
+                 ? reinterpret_cast<const uint4*>(x + xi)
+                 : nullptr;
+    };
+    auto store_chunk = [&](int q, int i, const uint4& v0, const uint4& v1) {
       const uint32_t a0 = i ? v0.y : v0.x, a2 = i ? v0.w : v0.z;
       const uint32_t c0 = i ? v1.y : v1.x, c2 = i ? v1.w : v1.z;
       xs[q] = make_uint4(__byte_perm(a0, a2, 0x5410u), __byte_perm(c0, c2, 0x5410u),
                          __byte_perm(a0, a2, 0x7632u), __byte_perm(c0, c2, 0x7632u));
+    };
+    constexpr int kXBatch = 8;
+    int q = threadIdx.x;
+    if constexpr (NT == 2 || SPLIT) {
+      for (; q + (kXBatch - 1) * nthreads < nchunks; q += kXBatch * nthreads) {
+        uint4 v0[kXBatch], v1[kXBatch];
+        int sel[kXBatch];
+#pragma unroll
+        for (int u = 0; u < kXBatch; ++u) {
+          const uint4* src = chunk_src(q + u * nthreads, sel[u]);
+          v0[u] = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
+          v1[u] = src ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kXBatch; ++u) store_chunk(q + u * nthreads, sel[u], v0[u], v1[u]);
+      }
+    }
+    for (; q < nchunks; q += nthreads) {
+      int i;
+      const uint4* src = chunk_src(q, i);
+      const uint4 v0 = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
+      const uint4 v1 = src ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+      store_chunk(q, i, v0, v1);
     }
   }
   __syncthreads();
@@ -1249,8 +1286,8 @@ cudaError_t launch_tma(int group, int64_t blocks, int S, int64_t smem, int vec, 
     return launch_dependent(kern, blocks, threads, smem, st, tmap, tmap_z, tmap_s, scales, zeros,
                             N, K, x, M, y, S, vec, kMagic);
   };
-  // The K split is compiled for up to 8 tokens with x staged only.
-  constexpr bool kCanSplit = NT == 1 && XPERM;
+  // The K split is compiled with x staged only.
+  constexpr bool kCanSplit = XPERM;
   if (kCanSplit && split) {
     if (group == 128)
       return pt ? go(k_wq_tma<NT, 128, BITS, XPERM, true, kCanSplit>)
@@ -1296,13 +1333,12 @@ cudaError_t launch_wq(int group, const uint32_t* codes, const __half* scales,
                     reinterpret_cast<uintptr_t>(zeros) % 16 == 0 &&
                     reinterpret_cast<uintptr_t>(scales) % 16 == 0;
     bool xperm = tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes, NT, pt) <= kDecodeSmemMax;
-    // Up to 8 tokens, when x does not fit but half of it does (K a multiple
-    // of 1024, so a half starts on a 4-unit stage boundary): half the blocks
-    // take the first K/2 channels and half the rest, each over whole row
-    // tiles, so every output gets exactly two sums (deterministic).  (For 9
-    // to 16 tokens x read through L1 measured faster.)
+    // When x does not fit but half of it does (K a multiple of 1024, so a
+    // half starts on a 4-unit stage boundary): half the blocks take the first
+    // K/2 channels and half the rest, each over whole row tiles, so every
+    // output gets exactly two sums (deterministic).
     int kp = 1;
-    if (NT == 1 && !xperm && K % 1024 == 0 && tiles >= 2 &&
+    if (!xperm && K % 1024 == 0 && tiles >= 2 &&
         tma_smem_bytes(tma_warps<NT, true>(), 2, xbytes / 2, NT, pt) <= kDecodeSmemMax) {
       kp = 2;
       xperm = true;

@@ -311,10 +311,13 @@ def test_decode_product_x_through_l1(M, N, K, group, bits):
 @pytest.mark.parametrize("M,N,K,group,unaligned", [
     (8, 300, 8192, 128, False), (6, 2048, 8192, 64, False), (7, 37, 8192, -1, False),
     (5, 520, 12288, 128, False), (8, 17, 8192, 128, False), (8, 100, 9216, 128, False),
-    (8, 70, 8192, 64, True)])
+    (8, 70, 8192, 64, True),
+    # 9-16 tokens (8 warps, two MMAs of 8 tokens per step)
+    (16, 300, 8192, 128, False), (10, 37, 12288, -1, False), (12, 2048, 8192, 64, False),
+    (12, 100, 9216, 128, False), (16, 70, 8192, 64, True), (16, 17, 8192, 128, False)])
 def test_decode_product_split_k(M, N, K, group, unaligned, bits):
-    """Up to 8 tokens, M x K fp16 too large for shared memory but half of it
-    fits (K a multiple of 1024): half the blocks take the first K/2 channels,
+    """M x K fp16 too large for shared memory but half of it fits (K a
+    multiple of 1024), at 5-8 and 9-16 tokens: half the blocks take the first K/2 channels,
     half the rest, over whole row tiles (2 row tiles upwards, ragged N; parameters by
     TMA, by vector loads (72 groups per row), one by one (unaligned arrays),
     and whole-row groups): within the bound, and identical on a second run."""
