@@ -325,9 +325,10 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 5) -> dict:
     ms = timed([lambda W=W: torch.amax(W) for W in Ws])
     out["read_only_context"]["W"] = {"bytes": 2 * N * K, "ms": ms, "gbs": 2 * N * K / ms / 1e6,
                                      "kernel": "torch.amax"}
-    # The packed layer consumed at decode: the W4A16 product for 1 and 16
+    # The packed layer consumed at decode: the W4A16 product for 1, 16 and 8
     # tokens and the W3A16 product for one token, each beside a cuBLAS fp16
-    # product with the dense weight of the same shape.
+    # product with the dense weight of the same shape (8 tokens last, so the
+    # launch indices of the others stay as profiled).
     cfg3 = awq.QConfig(3, 128, 1, N_GRID)
     codes3 = [torch.empty(N * 3 * K // 32, dtype=torch.int32, device=dev) for _ in Ws]
     sc3 = [torch.empty(N * K // 128, dtype=torch.float16, device=dev) for _ in Ws]
@@ -337,7 +338,7 @@ def hbm_kernels(dev, flush, hbm_gbs: float, reps: int = 5) -> dict:
                                        codes3[i].data_ptr(), sc3[i].data_ptr(), z3[i].data_ptr(),
                                        st))
     decode = {}
-    for bits, M in ((4, 1), (4, 16), (3, 1)):
+    for bits, M in ((4, 1), (4, 16), (3, 1), (4, 8)):
         c_, s_, z_, cf = (codes, sc, z, cfg) if bits == 4 else (codes3, sc3, z3, cfg3)
         x = torch.randn(M, K, generator=g, device=dev).half()
         y = torch.empty(M, N, dtype=torch.float32, device=dev)
