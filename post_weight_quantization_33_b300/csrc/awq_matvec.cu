@@ -775,11 +775,12 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
     // slot's 16 channels 64 hc + 16 cc + (0..15).  One chunk per thread,
     // consecutive threads writing consecutive chunks.
     //
-    // In the 9-16 token and K-split kernels the loads of kXBatch chunks per
-    // thread are all issued before the first is used: at 16 tokens with the
-    // K split a thread stages 32 chunks, and staged one at a time, each
+    // In the 9-16 token and K-split kernels the loads of a batch of 8 chunks
+    // per thread are all issued before the first is used: at 16 tokens with
+    // the K split a thread stages 32 chunks, and staged one at a time, each
     // waiting for its own loads, they made the split slower than reading x
-    // through L1.  Chunks past the last whole batch go one at a time.  (The
+    // through L1.  The 5-8 token split kernels (5-7 chunks per thread at 5-7
+    // tokens) then take a batch of 4; the rest go one at a time.  (The
     // one-token kernel stages 2 chunks per thread; compiled into it, the
     // batch loop cost INT3 1.2 us though it never ran.)
     const int per_tok = hcs * 8;
@@ -802,20 +803,25 @@ __global__ void __launch_bounds__(tma_warps<NT, XPERM>() * 32, 1)
       xs[q] = make_uint4(__byte_perm(a0, a2, 0x5410u), __byte_perm(c0, c2, 0x5410u),
                          __byte_perm(a0, a2, 0x7632u), __byte_perm(c0, c2, 0x7632u));
     };
-    constexpr int kXBatch = 8;
     int q = threadIdx.x;
+    auto stage_batch = [&](auto nb) {
+      constexpr int NB = decltype(nb)::value;
+      uint4 v0[NB], v1[NB];
+      int sel[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const uint4* src = chunk_src(q + u * nthreads, sel[u]);
+        v0[u] = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
+        v1[u] = src ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < NB; ++u) store_chunk(q + u * nthreads, sel[u], v0[u], v1[u]);
+      q += NB * nthreads;
+    };
     if constexpr (NT == 2 || SPLIT) {
-      for (; q + (kXBatch - 1) * nthreads < nchunks; q += kXBatch * nthreads) {
-        uint4 v0[kXBatch], v1[kXBatch];
-        int sel[kXBatch];
-#pragma unroll
-        for (int u = 0; u < kXBatch; ++u) {
-          const uint4* src = chunk_src(q + u * nthreads, sel[u]);
-          v0[u] = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
-          v1[u] = src ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kXBatch; ++u) store_chunk(q + u * nthreads, sel[u], v0[u], v1[u]);
+      while (q + 7 * nthreads < nchunks) stage_batch(std::integral_constant<int, 8>{});
+      if constexpr (NT == 1) {
+        if (q + 3 * nthreads < nchunks) stage_batch(std::integral_constant<int, 4>{});
       }
     }
     for (; q < nchunks; q += nthreads) {
