@@ -651,8 +651,10 @@ def test_inputs_written_just_before_the_call_are_seen():
     codes, sc, z = awq.quantize_pack(cuda(W0), cuda(s), 4, 128)
     oc, osc, oz = O.quantize_groups(W0, s, 4, 128)
     big = torch.randn(64 << 20, device="cuda")          # a long producer kernel before each call
-    for it in range(6):
-        x_host = rng.standard_normal((1 + it % 3, K)).astype(np.float16)
+    # 1-3 tokens stage x whole; 5 and 8 tokens (one MMA of 8 tokens) and 16
+    # (two) stage it in two halves of K.
+    for it, M in enumerate((1, 2, 3, 5, 8, 16)):
+        x_host = rng.standard_normal((M, K)).astype(np.float16)
         src = cuda(x_host)
         x = torch.empty_like(src)
         big.mul_(1.0)                                     # keeps the stream busy
